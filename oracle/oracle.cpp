@@ -1,0 +1,333 @@
+// FP64 CPU oracle for the mixture-of-experts decode-layer forward.
+//
+// TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+// calls this file; the test suite, the smoke check and the bench's CPU
+// baseline do.  It shares no code, header, table or constant with the CUDA
+// library: every decode below is written from the format definitions.
+//
+// What it computes (plain definition, no blocking, no fusion), following the
+// layer the pages describe:
+//   * forward_k3.rs, doc comment of MoeLayer::forward_k3 — the chain
+//     router logits -> top-k -> expert gate+up -> SiLU+down -> weighted sum
+//     + shared-expert blend;
+//   * forward_k3.rs, step "2. Batched topK" (moe_topk_sigmoid_batched /
+//     moe_topk_softmax_batched arguments) — softmax with optional
+//     renormalisation, or sigmoid + correction bias with norm_topk_prob and
+//     routed_scaling_factor;
+//   * forward_k3.rs, the E8M0 guard (GS16 vs GS32 scale groups) — NVFP4
+//     (E2M1 + per-16 E4M3) and MXFP4 (E2M1 + per-32 E8M0) expert formats;
+//   * forward_atomic_c4.rs, doc comment — routed outputs accumulated as
+//     routing-weighted sums, then cast to BF16 and blended with the shared
+//     expert;
+//   * forward_k3.rs, the EP all-reduce block ("Add shared expert with sigmoid
+//     gate") — a null shared_expert_gate adds the shared expert as is,
+//     otherwise it is blended with sigmoid(w_s . x).
+// Readings where the pages are silent (nibble order, tie order, bias only in
+// selection, scaling only on the sigmoid path) are stated at each function.
+//
+// All arithmetic is double precision; OpenMP only splits independent output
+// rows (each output element is still summed by one thread in index order).
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+#include <algorithm>
+#include <numeric>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+extern "C" {
+
+// ---------------------------------------------------------------- decoders
+
+// OCP Microscaling Formats (MX) v1.0, FP4 E2M1: sign(1) exponent(2, bias 1)
+// mantissa(1); exponent 0 is subnormal (0.5 * m); no inf or NaN.
+double oracle_e2m1(uint32_t nibble) {
+    const int s = (nibble >> 3) & 1, e = (nibble >> 1) & 3, m = nibble & 1;
+    const double mag = (e == 0) ? 0.5 * m : std::ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -mag : mag;
+}
+
+// OCP 8-bit Floating Point spec, E4M3 ("fn": bias 7, no inf, S.1111.111 = NaN,
+// max 448); exponent 0 is subnormal m/8 * 2^-6.
+double oracle_e4m3(uint32_t byte) {
+    const int s = (byte >> 7) & 1, e = (byte >> 3) & 15, m = byte & 7;
+    if (e == 15 && m == 7) return std::nan("");
+    const double mag = (e == 0) ? std::ldexp(m / 8.0, -6) : std::ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+// OCP MX v1.0 E8M0 shared scale: 2^(e-127); 0xFF is NaN.
+double oracle_e8m0(uint32_t byte) {
+    if ((byte & 0xFF) == 0xFF) return std::nan("");
+    return std::ldexp(1.0, (int)(byte & 0xFF) - 127);
+}
+
+// BF16 = the upper 16 bits of an IEEE binary32.
+double oracle_bf16(uint32_t bits16) {
+    const uint32_t u = (bits16 & 0xFFFFu) << 16;
+    float f;
+    std::memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+// Round a double to the nearest BF16 (8 significant bits, exponent range of
+// binary32), ties to even, overflow to infinity; returns the 16-bit pattern.
+uint32_t oracle_round_bf16(double v) {
+    if (std::isnan(v)) return 0x7FC0;
+    const uint32_t sign = std::signbit(v) ? 0x8000u : 0u;
+    double a = std::fabs(v);
+    if (a == 0.0) return sign;
+    // quantum of the bf16 grid at |v|: 2^(e-7) for normals (e = floor(log2 a)),
+    // 2^-133 below the smallest normal 2^-126.
+    int e = std::ilogb(a);
+    const double quantum = (e < -126) ? std::ldexp(1.0, -133) : std::ldexp(1.0, e - 7);
+    const double q = a / quantum;                 // exact (power-of-two division)
+    double r = std::floor(q);
+    const double frac = q - r;
+    if (frac > 0.5 || (frac == 0.5 && std::fmod(r, 2.0) != 0.0)) r += 1.0;
+    const double rounded = r * quantum;
+    if (rounded >= std::ldexp(1.0, 128)) return sign | 0x7F80u;   // inf
+    const float f = (float)rounded;               // exact: rounded is on the bf16 grid
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    return sign | ((u >> 16) & 0x7FFFu);
+}
+
+// ------------------------------------------------------------ dequantisation
+
+// Value of element (r, k) of one FP4 projection matrix [rows, K]:
+//   E2M1(code) * blockscale(scale[r, k/gs]) * scale2
+// with code = low nibble of byte q[r, k/2] for even k, high nibble for odd k
+// (element 2j in the low nibble: not stated on the pages; plainest reading),
+// and the scale group running along K, the input dimension (the pages size
+// the scale buffer as rows*K/16 for NVFP4 and rows*K/32 for E8M0).
+// fmt 0 = NVFP4 (gs 16, E4M3 scales), fmt 1 = MXFP4 (gs 32, E8M0 scales).
+double oracle_fp4_weight(const uint8_t* q, const uint8_t* s, double scale2,
+                         int K, int fmt, long r, long k) {
+    const int gs = (fmt == 0) ? 16 : 32;
+    const uint8_t byte = q[r * (K / 2) + k / 2];
+    const uint32_t code = (k % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+    const uint8_t sb = s[r * (K / gs) + k / gs];
+    const double bs = (fmt == 0) ? oracle_e4m3(sb) : oracle_e8m0(sb);
+    return oracle_e2m1(code) * bs * scale2;
+}
+
+void oracle_dequant(const uint8_t* q, const uint8_t* s, double scale2, int rows, int K,
+                    int fmt, double* out) {
+    for (long r = 0; r < rows; ++r)
+        for (long k = 0; k < K; ++k)
+            out[r * K + k] = oracle_fp4_weight(q, s, scale2, K, fmt, r, k);
+}
+
+// ------------------------------------------------------------------- router
+
+// logits[n, e] = sum_h x[n, h] * Wr[e, h]   (BF16 inputs, FP64 products/sums)
+void oracle_router_logits(const uint16_t* x, const uint16_t* wr, int N, int E, int H,
+                          double* logits) {
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int n = 0; n < N; ++n)
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h)
+                acc += oracle_bf16(x[(long)n * H + h]) * oracle_bf16(wr[(long)e * H + h]);
+            logits[(long)n * E + e] = acc;
+        }
+}
+
+// ------------------------------------------------------------------ routing
+
+// Routing of one token, from its logits row.
+//   scoring 0 (softmax): p = softmax(l); selection score = p;
+//       w = p of the selected experts, divided by their sum if norm != 0.
+//       The routed scaling factor is not applied (the softmax top-k op is not
+//       given it on the pages).
+//   scoring 1 (sigmoid + correction bias): s = 1/(1+exp(-l)); selection score
+//       = s + bias; w = s of the selected experts (bias only selects), divided
+//       by their sum if norm != 0, then multiplied by rsf.
+// Top-k: sort by selection score descending, ties to the lower expert index;
+// the first k in that order are the selected experts, in that order.
+// sel_score (optional, [E]) receives the selection score of every expert.
+void oracle_route_one(const double* l, const float* bias, int E, int k, int scoring,
+                      int norm, double rsf, int32_t* idx, double* w, double* sel_score) {
+    std::vector<double> score(E), base(E);
+    if (scoring == 0) {
+        double mx = l[0];
+        for (int e = 1; e < E; ++e) mx = std::max(mx, l[e]);
+        double den = 0.0;
+        for (int e = 0; e < E; ++e) den += std::exp(l[e] - mx);
+        for (int e = 0; e < E; ++e) {
+            base[e] = std::exp(l[e] - mx) / den;
+            score[e] = base[e];
+        }
+    } else {
+        for (int e = 0; e < E; ++e) {
+            base[e] = 1.0 / (1.0 + std::exp(-l[e]));
+            score[e] = base[e] + (bias ? (double)bias[e] : 0.0);
+        }
+    }
+    std::vector<int> order(E);
+    std::iota(order.begin(), order.end(), 0);
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+        if (score[a] != score[b]) return score[a] > score[b];
+        return a < b;
+    });
+    double sum = 0.0;
+    for (int j = 0; j < k; ++j) {
+        idx[j] = order[j];
+        w[j] = base[order[j]];
+        sum += w[j];
+    }
+    if (norm)
+        for (int j = 0; j < k; ++j) w[j] /= sum;
+    if (scoring == 1)
+        for (int j = 0; j < k; ++j) w[j] *= rsf;
+    if (sel_score)
+        for (int e = 0; e < E; ++e) sel_score[e] = score[e];
+}
+
+void oracle_route(const double* logits, const float* bias, int N, int E, int k, int scoring,
+                  int norm, double rsf, int32_t* idx, double* w, double* sel_score) {
+    for (int n = 0; n < N; ++n)
+        oracle_route_one(logits + (long)n * E, bias, E, k, scoring, norm, rsf,
+                         idx + (long)n * k, w + (long)n * k,
+                         sel_score ? sel_score + (long)n * E : nullptr);
+}
+
+// ------------------------------------------------------------------ experts
+
+static double silu(double g) { return g / (1.0 + std::exp(-g)); }
+
+// One routed expert on one token, FP4 weights:
+//   g = Dq(Wg) x,  u = Dq(Wu) x,  a = SiLU(g) * u,  y = Dq(Wd) a.
+// Wg, Wu are [inter, H]; Wd is [H, inter]; x is BF16 [H]; y is [H].
+void oracle_expert_fp4(const uint8_t* gq, const uint8_t* gsc, double g2,
+                       const uint8_t* uq, const uint8_t* usc, double u2,
+                       const uint8_t* dq, const uint8_t* dsc, double d2,
+                       int H, int inter, int fmt, const uint16_t* x, double* y) {
+    std::vector<double> xv(H), a(inter);
+    for (int h = 0; h < H; ++h) xv[h] = oracle_bf16(x[h]);
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < inter; ++i) {
+        double g = 0.0, u = 0.0;
+        for (int h = 0; h < H; ++h) {
+            g += oracle_fp4_weight(gq, gsc, g2, H, fmt, i, h) * xv[h];
+            u += oracle_fp4_weight(uq, usc, u2, H, fmt, i, h) * xv[h];
+        }
+        a[i] = silu(g) * u;
+    }
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < H; ++r) {
+        double acc = 0.0;
+        for (int i = 0; i < inter; ++i)
+            acc += oracle_fp4_weight(dq, dsc, d2, inter, fmt, r, i) * a[i];
+        y[r] = acc;
+    }
+}
+
+// Shared expert, BF16 weights: sh = Wd (SiLU(Wg x) * (Wu x)); Wg, Wu [Is, H],
+// Wd [H, Is].
+void oracle_shared_expert(const uint16_t* wg, const uint16_t* wu, const uint16_t* wd,
+                          int H, int Is, const uint16_t* x, double* sh) {
+    std::vector<double> xv(H), a(Is);
+    for (int h = 0; h < H; ++h) xv[h] = oracle_bf16(x[h]);
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < Is; ++i) {
+        double g = 0.0, u = 0.0;
+        for (int h = 0; h < H; ++h) {
+            g += oracle_bf16(wg[(long)i * H + h]) * xv[h];
+            u += oracle_bf16(wu[(long)i * H + h]) * xv[h];
+        }
+        a[i] = silu(g) * u;
+    }
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < H; ++r) {
+        double acc = 0.0;
+        for (int i = 0; i < Is; ++i) acc += oracle_bf16(wd[(long)r * Is + i]) * a[i];
+        sh[r] = acc;
+    }
+}
+
+// ------------------------------------------------------------- full forward
+
+// Weights of one layer, host memory, canonical layout:
+//   router [E, H] bf16; bias [E] f32 or null;
+//   gate_q/up_q [E, inter, H/2] u8, gate_s/up_s [E, inter, H/gs] u8,
+//   down_q [E, H, inter/2] u8, down_s [E, H, inter/gs] u8,
+//   *_s2 [E] f32 or null (null = 1.0; MXFP4 has none);
+//   sh_gate/sh_up [Is, H] bf16, sh_down [H, Is] bf16 (null when Is == 0);
+//   sh_gate_w [H] bf16 or null (null = ungated shared expert).
+struct oracle_weights {
+    const uint16_t* router;
+    const float* bias;
+    const uint8_t *gate_q, *up_q, *down_q;
+    const uint8_t *gate_s, *up_s, *down_s;
+    const float *gate_s2, *up_s2, *down_s2;
+    const uint16_t *sh_gate, *sh_up, *sh_down;
+    const uint16_t* sh_gate_w;
+};
+
+// out_f64 [N, H] = sum_j w[n,j] * expert_{idx[n,j]}(x_n) + g_s(x_n) * shared(x_n)
+// with g_s = sigmoid(w_s . x_n) when sh_gate_w is given, 1 otherwise, and no
+// shared term when Is == 0.  The routed scaling factor is not applied to the
+// shared expert.  out_bf16 is out_f64 rounded to BF16 (nearest even).
+// idx/w receive the routing ([N, k]); logits (optional) the router output.
+int oracle_moe_forward(int H, int inter, int E, int k, int scoring, int norm, double rsf,
+                       int fmt, int Is, const oracle_weights* W, const uint16_t* x, int N,
+                       double* out_f64, uint16_t* out_bf16, int32_t* idx, double* w,
+                       double* logits_out) {
+    if (H <= 0 || inter <= 0 || E <= 0 || k <= 0 || k > E || N < 0) return 1;
+    const int gs = (fmt == 0) ? 16 : 32;
+    std::vector<double> logits((size_t)N * E);
+    oracle_router_logits(x, W->router, N, E, H, logits.data());
+    if (logits_out) std::copy(logits.begin(), logits.end(), logits_out);
+    oracle_route(logits.data(), W->bias, N, E, k, scoring, norm, rsf, idx, w, nullptr);
+
+    const long gq_e = (long)inter * (H / 2), gs_e = (long)inter * (H / gs);
+    const long dq_e = (long)H * (inter / 2), ds_e = (long)H * (inter / gs);
+    std::vector<double> y(H), sh(H);
+    for (int n = 0; n < N; ++n) {
+        const uint16_t* xn = x + (long)n * H;
+        std::vector<double> acc(H, 0.0);
+        for (int j = 0; j < k; ++j) {
+            const int e = idx[(long)n * k + j];
+            const double g2 = W->gate_s2 ? W->gate_s2[e] : 1.0;
+            const double u2 = W->up_s2 ? W->up_s2[e] : 1.0;
+            const double d2 = W->down_s2 ? W->down_s2[e] : 1.0;
+            oracle_expert_fp4(W->gate_q + e * gq_e, W->gate_s + e * gs_e, g2,
+                              W->up_q + e * gq_e, W->up_s + e * gs_e, u2,
+                              W->down_q + e * dq_e, W->down_s + e * ds_e, d2,
+                              H, inter, fmt, xn, y.data());
+            const double wj = w[(long)n * k + j];
+            for (int h = 0; h < H; ++h) acc[h] += wj * y[h];
+        }
+        if (Is > 0) {
+            oracle_shared_expert(W->sh_gate, W->sh_up, W->sh_down, H, Is, xn, sh.data());
+            double gsig = 1.0;
+            if (W->sh_gate_w) {
+                double d = 0.0;
+                for (int h = 0; h < H; ++h) d += oracle_bf16(W->sh_gate_w[h]) * oracle_bf16(xn[h]);
+                gsig = 1.0 / (1.0 + std::exp(-d));
+            }
+            for (int h = 0; h < H; ++h) acc[h] += gsig * sh[h];
+        }
+        for (int h = 0; h < H; ++h) {
+            if (out_f64) out_f64[(long)n * H + h] = acc[h];
+            if (out_bf16) out_bf16[(long)n * H + h] = (uint16_t)oracle_round_bf16(acc[h]);
+        }
+    }
+    return 0;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+}  // extern "C"
