@@ -1,0 +1,184 @@
+/*
+ * moe.h — C ABI of the GB300 (sm_103a) mixture-of-experts decode-layer forward.
+ *
+ * One call computes, for N token rows x[N,H] (BF16):
+ *   1. router logits   l[n,e] = x[n,:] . Wr[e,:]                 (FP32 accumulate)
+ *   2. top-k routing   softmax (optionally renormalised over the selected k)
+ *                      or sigmoid + correction bias for selection, sigmoid
+ *                      for the weights, optional renormalisation, times the
+ *                      routed scaling factor;
+ *   3. routed experts  SwiGLU with block-scaled FP4 weights:
+ *                      h = SiLU(Dq(Wg) x) * (Dq(Wu) x),  y = Dq(Wd) h,
+ *                      Dq(w) = E2M1(code) * blockscale * scale2;
+ *   4. output          out[n] = BF16( sum_j w[n,j] * y_{idx[n,j]}
+ *                                     + g_s(x_n) * shared(x_n) ),
+ *                      g_s = sigmoid(w_s . x_n) if a shared-expert gate vector
+ *                      is given, 1 if not; no shared term without a shared
+ *                      expert.
+ *
+ * The layer follows the MoE forward of the pages this library is built from:
+ *   - forward_k3.rs (MoeLayer::forward_k3): the step chain "gate GEMV ->
+ *     batched topK -> expert gate+up -> silu+down -> weighted sum + blend", the
+ *     batched top-k calls (moe_topk_sigmoid_batched with bias, norm_topk_prob
+ *     and routed_scaling_factor; moe_topk_softmax_batched with norm_topk_prob),
+ *     the per-expert weight tables (packed_ptrs, scale_ptrs, scale2_vals), the
+ *     GS16/E4M3 vs GS32/E8M0 scale formats (the E8M0 guard), and the shared
+ *     expert blend (null shared_expert_gate -> residual add, else sigmoid gate);
+ *   - forward_atomic_c4.rs (forward_atomic_c4_decode): routing-weighted FP32
+ *     accumulation of the routed down projections, then a BF16 cast and the
+ *     shared-expert blend; the scratch carve-out and its size check;
+ *   - forward_batched.rs: one router GEMM for N rows, per-token routing, and
+ *     "each routed and shared expert streams its weights once for all rows".
+ *
+ * Memory: every pointer passed to moe_forward / moe_route is a DEVICE pointer
+ * (weights, x, out, topk outputs, workspace) unless the name says _host.  The
+ * caller owns all buffers.  The library never allocates device memory and
+ * never synchronises inside moe_forward/moe_route: work is enqueued on the
+ * given stream (a cudaStream_t passed as void*; NULL = legacy default stream).
+ *
+ * Weight layout (canonical, row-major, K contiguous):
+ *   router     [E, H]          bf16
+ *   bias       [E]             f32, sigmoid scoring only (NULL otherwise)
+ *   gate_q     [E, inter, H/2] u8  two E2M1 codes per byte, element 2j in the
+ *   up_q       [E, inter, H/2] u8  low nibble, 2j+1 in the high nibble
+ *   down_q     [E, H, inter/2] u8
+ *   gate_s     [E, inter, H/gs]   u8  block scales along K (the input dim),
+ *   up_s       [E, inter, H/gs]   u8  gs = 16 (E4M3, NVFP4) or 32 (E8M0, MXFP4)
+ *   down_s     [E, H, inter/gs]   u8
+ *   gate_s2, up_s2, down_s2 [E] f32 per-expert global scale (NULL = 1.0)
+ *   sh_gate, sh_up [Is, H] bf16; sh_down [H, Is] bf16  (NULL when Is == 0)
+ *   sh_gate_w  [H] bf16 or NULL (NULL = ungated, always-on shared expert)
+ * All weight, x, out and workspace pointers must be 16-byte aligned.
+ */
+#ifndef MOE_DECODE_LAYER_TOPK_GB300_MOE_H
+#define MOE_DECODE_LAYER_TOPK_GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  A refusal names what is wrong instead of computing a wrong
+ * answer (forward_k3.rs: "Named refusal, not silent wrongness"). */
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,          /* null required pointer, N < 1, bad alignment */
+  MOE_ERR_UNSUPPORTED = 2,          /* shape/format outside what the kernels take */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes < moe_workspace_size(desc, N) */
+  MOE_ERR_CUDA = 4,                 /* a CUDA runtime call failed */
+  MOE_ERR_TIMEOUT = 5               /* a bounded device-side wait gave up */
+} moe_status_t;
+
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID_BIAS = 1 } moe_scoring_t;
+typedef enum { MOE_W_NVFP4 = 0, MOE_W_MXFP4 = 1 } moe_wfmt_t;
+
+/* Layer configuration: the config fields the pages' MoE forward reads
+ * (hidden_size, moe_intermediate_size, num_experts, num_experts_per_tok,
+ * norm_topk_prob, routed_scaling_factor, the expert scale kind, and
+ * shared_expert_intermediate_size). */
+typedef struct {
+  int32_t H;                     /* hidden size, multiple of 32 */
+  int32_t inter;                 /* routed expert intermediate size, multiple of 32 */
+  int32_t E;                     /* number of routed experts, 1..1024 */
+  int32_t top_k;                 /* experts per token, 1..min(E, 32) */
+  int32_t scoring;               /* moe_scoring_t */
+  int32_t norm_topk_prob;        /* 0/1: renormalise the selected weights */
+  float routed_scaling_factor;   /* sigmoid scoring only; ignored for softmax */
+  int32_t wfmt;                  /* moe_wfmt_t */
+  int32_t shared_inter;          /* shared expert intermediate size; 0 = none */
+} moe_layer_desc_t;
+
+typedef struct {
+  const void* router;            /* bf16 [E, H] */
+  const float* bias;             /* f32 [E] (required iff scoring is sigmoid+bias) */
+  const uint8_t* gate_q;
+  const uint8_t* up_q;
+  const uint8_t* down_q;
+  const uint8_t* gate_s;
+  const uint8_t* up_s;
+  const uint8_t* down_s;
+  const float* gate_s2;          /* NULL = 1.0 */
+  const float* up_s2;
+  const float* down_s2;
+  const void* sh_gate;           /* bf16, NULL iff shared_inter == 0 */
+  const void* sh_up;
+  const void* sh_down;
+  const void* sh_gate_w;         /* bf16 [H] or NULL (ungated) */
+} moe_weights_t;
+
+/* Bytes of device workspace moe_forward needs for up to max_tokens rows.
+ * Returns 0 if the descriptor is invalid.  The workspace holds the router
+ * logits, the routing table, the gate/up activations, the FP32 output
+ * accumulator and the grid-barrier words (the scratch the pages carve out of
+ * ctx.buffers.scratch() in forward_atomic_c4.rs). */
+MOE_API size_t moe_workspace_size(const moe_layer_desc_t* desc, int32_t max_tokens);
+
+/* Zero a workspace before its first use (and after MOE_ERR_TIMEOUT).  Enqueues
+ * a memset on `stream`.  Afterwards moe_forward keeps the workspace's barrier
+ * and error words consistent by itself. */
+MOE_API moe_status_t moe_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+
+/* The layer forward for N token rows.
+ *   x         bf16 [N, H] device
+ *   out       bf16 [N, H] device, fully overwritten
+ *   topk_idx  int32 [N, top_k] device or NULL: selected experts, in order of
+ *             decreasing selection score (ties to the lower expert index)
+ *   topk_w    f32 [N, top_k] device or NULL: their routing weights
+ *   workspace device, >= moe_workspace_size(desc, N) bytes, zeroed once by
+ *             moe_workspace_init; one workspace per concurrently running call
+ * Supports 1 <= N and N*top_k <= 256.  Asynchronous on `stream`; no host
+ * synchronisation, no allocation, so it may be captured in a CUDA graph.
+ * Argument errors are returned before anything is enqueued; device-side
+ * timeouts are reported by moe_get_error. */
+MOE_API moe_status_t moe_forward(const moe_layer_desc_t* desc, const moe_weights_t* weights,
+                         const void* x, int32_t N, void* out,
+                         int32_t* topk_idx, float* topk_w,
+                         void* workspace, size_t ws_bytes, void* stream);
+
+/* Router logits and top-k routing only (steps 1-2): writes topk_idx/topk_w
+ * (both required).  Same constraints and ownership as moe_forward. */
+MOE_API moe_status_t moe_route(const moe_layer_desc_t* desc, const moe_weights_t* weights,
+                       const void* x, int32_t N, int32_t* topk_idx, float* topk_w,
+                       void* workspace, size_t ws_bytes, void* stream);
+
+/* End-to-end convenience call with HOST activations: copies x_host (bf16
+ * [N,H], pinned memory recommended) to the device through the workspace,
+ * runs moe_forward, copies the result to out_host and synchronises `stream`
+ * before returning.  Weights and workspace stay device pointers.  Needs
+ * moe_workspace_size(desc, N) + moe_host_staging_size(desc, N) bytes. */
+MOE_API size_t moe_host_staging_size(const moe_layer_desc_t* desc, int32_t max_tokens);
+MOE_API moe_status_t moe_forward_host(const moe_layer_desc_t* desc, const moe_weights_t* weights,
+                              const void* x_host, int32_t N, void* out_host,
+                              void* workspace, size_t ws_bytes, void* stream);
+
+/* Sticky device-side error of a workspace (MOE_OK or MOE_ERR_TIMEOUT).
+ * Enqueues a 4-byte read on `stream`, synchronises the stream, clears the
+ * word, and returns the status of the calls that ran since the last check. */
+MOE_API moe_status_t moe_get_error(void* workspace, void* stream);
+
+/* Static description of a status code. */
+MOE_API const char* moe_status_string(moe_status_t status);
+
+/* Library version, for the binding to check it loaded the library it expects. */
+MOE_API int32_t moe_abi_version(void);
+
+/* Test hook: time budget, in nanoseconds, of every bounded device-side wait
+ * (grid barrier, stage arrival) for calls enqueued afterwards; default 1e9.
+ * A budget of 0 makes a wait that is not already satisfied expire at once, so
+ * a test can drive the MOE_ERR_TIMEOUT path without stalling the GPU.  After
+ * such a call, re-initialise the workspace with moe_workspace_init. */
+MOE_API void moe_debug_set_wait_budget_ns(unsigned long long ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_DECODE_LAYER_TOPK_GB300_MOE_H */

@@ -1,0 +1,269 @@
+// C ABI of the MoE decode-layer forward (include/moe.h): argument checks,
+// workspace carve-out, and the launch of the fused decode kernel.
+//
+// Checks follow the pages' "named refusal, not silent wrongness" rule
+// (forward_k3.rs, the zero-expert guard) and the scratch-size check of
+// forward_atomic_c4.rs: every refusal returns a status before anything is
+// enqueued.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "moe_internal.h"
+
+namespace {
+
+constexpr int32_t kAbiVersion = 1;
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct WsLayout {
+  size_t ctrl, logits, x16, xexp, gsig, h, hs, acc, rbcnt, total;
+};
+
+WsLayout ws_layout(const moe_layer_desc_t& d, int32_t N) {
+  WsLayout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, kAlign);
+    return o;
+  };
+  L.ctrl = take(256);
+  L.logits = take((size_t)N * d.E * 4);
+  L.x16 = take((size_t)N * d.H * 2);
+  L.xexp = take((size_t)N * 4);
+  L.gsig = take((size_t)N * 4);
+  L.h = take((size_t)N * d.top_k * d.inter * 4);
+  L.hs = take((size_t)N * std::max(d.shared_inter, 0) * 4);
+  L.acc = take((size_t)N * d.H * 4);
+  L.rbcnt = take((size_t)(d.H / 32) * 4);
+  L.total = off;
+  return L;
+}
+
+moe_status_t check_desc(const moe_layer_desc_t* d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->H <= 0 || d->inter <= 0 || d->E <= 0 || d->top_k <= 0) return MOE_ERR_INVALID_ARG;
+  if (d->scoring != MOE_SCORE_SOFTMAX && d->scoring != MOE_SCORE_SIGMOID_BIAS)
+    return MOE_ERR_INVALID_ARG;
+  if (d->wfmt != MOE_W_NVFP4 && d->wfmt != MOE_W_MXFP4) return MOE_ERR_INVALID_ARG;
+  if (d->shared_inter < 0) return MOE_ERR_INVALID_ARG;
+  if (d->H % 32 || d->inter % 32 || d->shared_inter % 32) return MOE_ERR_UNSUPPORTED;
+  if (d->E > moe::kMaxE || d->top_k > d->E || d->top_k > moe::kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status_t check_weights(const moe_layer_desc_t* d, const moe_weights_t* w) {
+  if (!w) return MOE_ERR_INVALID_ARG;
+  const void* req[] = {w->router, w->gate_q, w->up_q, w->down_q, w->gate_s, w->up_s, w->down_s};
+  for (const void* p : req)
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (d->scoring == MOE_SCORE_SIGMOID_BIAS && !w->bias) return MOE_ERR_INVALID_ARG;
+  if (d->shared_inter > 0) {
+    const void* sh[] = {w->sh_gate, w->sh_up, w->sh_down};
+    for (const void* p : sh)
+      if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (w->sh_gate_w && !aligned16(w->sh_gate_w)) return MOE_ERR_INVALID_ARG;
+  } else if (w->sh_gate || w->sh_up || w->sh_down || w->sh_gate_w) {
+    return MOE_ERR_INVALID_ARG;   // shared weights without a shared size
+  }
+  return MOE_OK;
+}
+
+struct DeviceInfo {
+  int budget = 0;
+  int grid = 0;
+  bool ready = false;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+
+moe_status_t device_info(int* budget, int* grid) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ready) {
+    di.budget = moe::decode_smem_budget(dev);
+    if (di.budget <= 0) return MOE_ERR_CUDA;
+    di.grid = moe::decode_grid(dev, di.budget);
+    if (di.grid <= 0) return MOE_ERR_CUDA;
+    di.ready = true;
+  }
+  *budget = di.budget;
+  *grid = di.grid;
+  return MOE_OK;
+}
+
+unsigned long long g_timeout_ns = 1000000000ull;   // bounded waits: 1 s
+
+moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* x, int32_t N,
+                 void* out, int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
+                 void* stream, int route_only) {
+  moe_status_t st = check_desc(d);
+  if (st != MOE_OK) return st;
+  st = check_weights(d, w);
+  if (st != MOE_OK) return st;
+  if (N < 1) return MOE_ERR_INVALID_ARG;
+  if ((long long)N * d->top_k > moe::kMaxSlots) return MOE_ERR_UNSUPPORTED;
+  if (!x || !aligned16(x) || !ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (!route_only && (!out || !aligned16(out))) return MOE_ERR_INVALID_ARG;
+  if (route_only && (!topk_idx || !topk_w)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*d, N);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+
+  int budget = 0, grid = 0;
+  st = device_info(&budget, &grid);
+  if (st != MOE_OK) return st;
+
+  moe::Params p;
+  memset(&p, 0, sizeof(p));
+  p.H = d->H;
+  p.inter = d->inter;
+  p.E = d->E;
+  p.k = d->top_k;
+  p.scoring = d->scoring;
+  p.norm = d->norm_topk_prob ? 1 : 0;
+  p.rsf = d->routed_scaling_factor;
+  p.fmt = d->wfmt;
+  p.Is = d->shared_inter;
+  p.N = N;
+  p.route_only = route_only;
+  p.router = static_cast<const uint16_t*>(w->router);
+  p.bias = d->scoring == MOE_SCORE_SIGMOID_BIAS ? w->bias : nullptr;
+  p.gq = w->gate_q;
+  p.uq = w->up_q;
+  p.dq = w->down_q;
+  p.gsc = w->gate_s;
+  p.usc = w->up_s;
+  p.dsc = w->down_s;
+  p.g2 = w->gate_s2;
+  p.u2 = w->up_s2;
+  p.d2 = w->down_s2;
+  p.shg = static_cast<const uint16_t*>(w->sh_gate);
+  p.shu = static_cast<const uint16_t*>(w->sh_up);
+  p.shd = static_cast<const uint16_t*>(w->sh_down);
+  p.shw = d->shared_inter > 0 ? static_cast<const uint16_t*>(w->sh_gate_w) : nullptr;
+  p.x = static_cast<const uint16_t*>(x);
+  p.out = static_cast<uint16_t*>(out);
+  p.topk_idx = topk_idx;
+  p.topk_w = topk_w;
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  p.ctrl = reinterpret_cast<uint32_t*>(b + L.ctrl);
+  p.logits = reinterpret_cast<float*>(b + L.logits);
+  p.x16 = reinterpret_cast<uint16_t*>(b + L.x16);
+  p.xexp = reinterpret_cast<int*>(b + L.xexp);
+  p.gsig = reinterpret_cast<float*>(b + L.gsig);
+  p.h = reinterpret_cast<float*>(b + L.h);
+  p.hs = reinterpret_cast<float*>(b + L.hs);
+  p.acc = reinterpret_cast<float*>(b + L.acc);
+  p.rbcnt = reinterpret_cast<uint32_t*>(b + L.rbcnt);
+  p.timeout_ns = g_timeout_ns;
+  if (!moe::plan_decode(p, budget)) return MOE_ERR_UNSUPPORTED;
+  if (moe::launch_decode(p, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_layer_desc_t* desc, int32_t max_tokens) {
+  if (check_desc(desc) != MOE_OK || max_tokens < 1) return 0;
+  return ws_layout(*desc, max_tokens).total;
+}
+
+size_t moe_host_staging_size(const moe_layer_desc_t* desc, int32_t max_tokens) {
+  if (check_desc(desc) != MOE_OK || max_tokens < 1) return 0;
+  return 2 * align_up((size_t)max_tokens * desc->H * 2, kAlign);
+}
+
+moe_status_t moe_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+  if (!workspace || ws_bytes == 0) return MOE_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(workspace, 0, ws_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_forward(const moe_layer_desc_t* desc, const moe_weights_t* weights, const void* x,
+                         int32_t N, void* out, int32_t* topk_idx, float* topk_w, void* workspace,
+                         size_t ws_bytes, void* stream) {
+  return run(desc, weights, x, N, out, topk_idx, topk_w, workspace, ws_bytes, stream, 0);
+}
+
+moe_status_t moe_route(const moe_layer_desc_t* desc, const moe_weights_t* weights, const void* x,
+                       int32_t N, int32_t* topk_idx, float* topk_w, void* workspace,
+                       size_t ws_bytes, void* stream) {
+  return run(desc, weights, x, N, nullptr, topk_idx, topk_w, workspace, ws_bytes, stream, 1);
+}
+
+moe_status_t moe_forward_host(const moe_layer_desc_t* desc, const moe_weights_t* weights,
+                              const void* x_host, int32_t N, void* out_host, void* workspace,
+                              size_t ws_bytes, void* stream) {
+  moe_status_t st = check_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!x_host || !out_host || N < 1 || !workspace) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_workspace_size(desc, N);
+  const size_t stage = align_up((size_t)N * desc->H * 2, kAlign);
+  if (ws_bytes < need + 2 * stage) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* b = static_cast<uint8_t*>(workspace);
+  void* xd = b + need;
+  void* od = b + need + stage;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)N * desc->H * 2;
+  if (cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  st = run(desc, weights, xd, N, od, nullptr, nullptr, workspace, need, stream, 0);
+  if (st != MOE_OK) return st;
+  if (cudaMemcpyAsync(out_host, od, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_get_error(void* workspace, void* stream) {
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  uint32_t* ctrl = static_cast<uint32_t*>(workspace);
+  if (cudaMemcpyAsync(&word, ctrl + 2, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (word == 0) return MOE_OK;
+  if (cudaMemsetAsync(ctrl + 2, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_ERR_TIMEOUT;
+}
+
+const char* moe_status_string(moe_status_t status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null pointer, N < 1 or misaligned buffer)";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or format";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than moe_workspace_size()";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_TIMEOUT: return "a bounded device-side wait expired";
+  }
+  return "unknown status";
+}
+
+int32_t moe_abi_version(void) { return kAbiVersion; }
+
+/* Test hook: budget of every bounded device wait, in nanoseconds, for calls
+ * enqueued afterwards (default 1e9).  A budget of 0 makes any wait that is not
+ * already satisfied expire at once, which exercises the MOE_ERR_TIMEOUT path
+ * without hanging the GPU. */
+void moe_debug_set_wait_budget_ns(unsigned long long ns) { g_timeout_ns = ns; }
+
+}  // extern "C"

@@ -1,0 +1,98 @@
+// Internal interface between the C ABI layer (moe_api.cu) and the fused
+// decode kernel (decode_kernel.cu).  Host and device code.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kConsumerWarps = 8;                 // compute warps per CTA
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;   // + one producer (TMA) warp
+constexpr int kTB = 4;                            // token rows per weight pass
+constexpr int kRows = 32;                         // weight rows per row group
+constexpr int kMaxSlots = 256;                    // N * top_k per call
+constexpr int kMaxE = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kMaxStages = 8;
+
+enum Kind { KIND_AS = 0, KIND_AR = 1, KIND_BR = 2, KIND_BS = 3 };
+enum Fmt { FMT_NVFP4 = 0, FMT_MXFP4 = 1, FMT_BF16 = 2 };
+enum ScaleMode { SCALES_NONE = 0, SCALES_PER_ROW = 1, SCALES_BLOCK = 2 };
+
+// Device-side error word bits (workspace control block).
+constexpr uint32_t kErrTimeoutBarrier = 1u;
+constexpr uint32_t kErrTimeoutStage = 2u;
+constexpr uint32_t kErrTimeoutProducer = 4u;
+
+// Stage geometry of one kind of row group (see decode_kernel.cu).
+struct Geo {
+  int fmt;          // Fmt
+  int nproj;        // weight matrices streamed together (2 = gate+up, 1 = down)
+  int K;            // reduction length (input dim of the projection)
+  int Kc;           // K elements per stage (chunk)
+  int nchunks;      // K / Kc
+  int row_bytes;    // bytes of one weight row's chunk
+  int row_stride;   // padded stride of weight rows in the stage (odd x 16 B)
+  int scale_mode;   // ScaleMode
+  int sr;           // scale bytes per full weight row (K / gs); 0 for bf16
+  int scale_bytes;  // per-row chunk scale bytes (PER_ROW) or sr (BLOCK)
+  int scale_stride; // stride of scale rows in the stage
+  int scale_off;    // offset of the scale region in the stage
+  int opnd_off;     // offset of the activation chunk region (-1: from hbuf)
+  int stage_bytes;  // bytes used in a stage
+  int rows_total;   // weight rows of one projection (inter, H or Is)
+};
+
+struct Params {
+  // layer
+  int H, inter, E, k, scoring, norm;
+  float rsf;
+  int fmt;   // FMT_NVFP4 / FMT_MXFP4 for the routed experts
+  int Is;    // shared expert intermediate size (0 = none)
+  int N;
+  int route_only;
+  // weights (device)
+  const uint16_t* router;
+  const float* bias;
+  const uint8_t *gq, *uq, *dq, *gsc, *usc, *dsc;
+  const float *g2, *u2, *d2;
+  const uint16_t *shg, *shu, *shd, *shw;
+  // activations / outputs (device)
+  const uint16_t* x;
+  uint16_t* out;
+  int32_t* topk_idx;
+  float* topk_w;
+  // workspace (device)
+  uint32_t* ctrl;    // [0] barrier count, [1] barrier generation, [2] error word
+  float* logits;     // [N, E]
+  uint16_t* x16;     // [N, H] f16, x * 2^-xexp[n]
+  int* xexp;         // [N]
+  float* gsig;       // [N] shared-expert gate
+  float* h;          // [N*k, inter] routed SiLU(g)*u, by (expert, token) slot
+  float* hs;         // [N, Is] shared expert SiLU(g)*u
+  float* acc;        // [N, H] routed + shared FP32 accumulator
+  uint32_t* rbcnt;   // [H/32] completion counters of output row blocks
+  // geometry
+  Geo geo[4];
+  int nstages, stage_bytes;
+  int smem_ring_off, smem_red_off, smem_hbuf_off, smem_tab_off, smem_bar_off, smem_total;
+  int hbuf_bytes;
+  unsigned long long timeout_ns;
+};
+
+// Fills p.geo / ring / smem layout from the layer shape; returns false if
+// the shape does not fit the kernel's shared-memory budget.
+bool plan_decode(Params& p, int smem_budget);
+
+// Shared memory the decode kernel may use on this device.
+int decode_smem_budget(int device);
+
+// Enqueue the fused decode kernel; returns a CUDA error code.
+cudaError_t launch_decode(const Params& p, int grid, cudaStream_t stream);
+
+// Number of CTAs the decode kernel runs with on `device` (one per SM).
+int decode_grid(int device, int smem_bytes);
+
+}  // namespace moe

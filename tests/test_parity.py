@@ -1,0 +1,111 @@
+"""GPU path vs the FP64 oracle, element by element, through the C ABI.
+
+Small cases use shapes that span several 32-row groups, several K chunks and
+a ragged token tail (N not a multiple of the 4-token batch), both scale
+layouts, both formats and every routing / shared-expert variant; the
+full-size cases are the five layer shapes at their token counts, in the same
+launch configuration the benchmark times.  Indices must match bit for bit,
+BF16 outputs within 1e-2*max|ref| + 2^-8.
+"""
+import numpy as np
+import pytest
+
+from moe_decode_layer_topk_gb300 import synth
+from moe_decode_layer_topk_gb300.device import DeviceLayer
+from oracle import compare, margin, oracle
+
+from .gpu_util import full_layer, run_forward, spec_from
+
+NV, MX = synth.NVFP4, synth.MXFP4
+SM, SB = synth.SOFTMAX, synth.SIGMOID_BIAS
+
+SMALL = {
+    "tiny": (dict(), 1),
+    "block_scales_ragged": (dict(H=160, inter=96, E=13, top_k=3), 5),
+    "block_scales_gated_shared": (dict(H=160, inter=96, E=13, top_k=3, shared_inter=64,
+                                       shared_gated=True), 5),
+    "per_row_scales_5_chunks": (dict(H=1280, inter=256, E=16, top_k=4), 3),
+    "mxfp4_block_scales": (dict(H=192, inter=160, E=9, top_k=2, wfmt=MX), 6),
+    "mxfp4_per_row_scales": (dict(H=1024, inter=512, E=8, top_k=2, wfmt=MX), 2),
+    "mxfp4_shared": (dict(H=2880 // 5, inter=2880 // 9, E=12, top_k=4, wfmt=MX,
+                          shared_inter=96, shared_gated=True), 4),
+    "sigmoid_bias_ungated_shared": (dict(H=256, inter=128, E=32, top_k=4, scoring=SB,
+                                         routed_scaling_factor=2.5, shared_inter=96), 4),
+    "sigmoid_bias_no_norm": (dict(H=256, inter=128, E=32, top_k=3, scoring=SB,
+                                  norm_topk_prob=False, routed_scaling_factor=1.7), 3),
+    "softmax_no_norm": (dict(H=256, inter=128, E=16, top_k=3, norm_topk_prob=False), 3),
+    "single_expert": (dict(E=1, top_k=1), 2),
+    "k_equals_E": (dict(E=4, top_k=4), 3),
+    "max_slots_k32": (dict(H=128, inter=64, E=64, top_k=32), 8),
+    "max_experts_1024": (dict(H=64, inter=32, E=1024, top_k=4), 3),
+    "n64_sweep_shape": (dict(H=128, inter=64, E=32, top_k=4), 64),
+    "zero_routed_weight": (dict(H=256, inter=128, E=8, top_k=2, scoring=SB,
+                                routed_scaling_factor=0.0, shared_inter=64, shared_gated=True), 3),
+}
+
+
+def _check(host, dev, x):
+    ref = oracle.moe_forward(host, x)
+    out, idx, w = run_forward(dev, x)
+    keys = margin.selection_keys(host, x)
+    compare.check_routing(idx, w, ref["idx"], ref["w"], keys)
+    return compare.check_output(out, ref["out_f64"])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", sorted(SMALL))
+def test_small_case(case):
+    kw, N = SMALL[case]
+    spec = spec_from("tiny", name=case, **kw)
+    host = synth.make_layer(spec, seed=7000 + len(case))
+    dev = DeviceLayer.upload(host)
+    x = margin.tokens_with_margin(host, N, seed=8000 + len(case))
+    _check(host, dev, x)
+
+
+@pytest.mark.gpu
+def test_many_tokens_on_one_expert():
+    """Identical rows route every token to the same experts: each expert gets
+    N = 9 tokens, i.e. three 4-token weight passes (ragged last pass)."""
+    spec = spec_from("tiny", name="same_rows", H=256, inter=128, E=8, top_k=2,
+                     shared_inter=64, shared_gated=True)
+    host = synth.make_layer(spec, seed=11)
+    dev = DeviceLayer.upload(host)
+    x1 = margin.tokens_with_margin(host, 1, seed=12)
+    x = np.repeat(x1, 9, axis=0)
+    _check(host, dev, x)
+
+
+@pytest.mark.gpu
+def test_zero_down_codes_gives_shared_alone():
+    spec = spec_from("tiny", name="zero_down", H=256, inter=128, E=8, top_k=2, shared_inter=64)
+    host = synth.make_layer(spec, seed=13)
+    host.down_q[:] = 0
+    dev = DeviceLayer.upload(host)
+    x = margin.tokens_with_margin(host, 2, seed=14)
+    _check(host, dev, x)
+
+
+@pytest.mark.gpu
+def test_scale2_is_applied():
+    spec = spec_from("tiny", name="scale2", H=256, inter=128, E=8, top_k=2)
+    host = synth.make_layer(spec, seed=15)
+    rng = np.random.default_rng(16)
+    host.gate_s2[:] = rng.uniform(0.5, 2, 8).astype(np.float32)
+    host.up_s2[:] = rng.uniform(0.5, 2, 8).astype(np.float32)
+    host.down_s2[:] = rng.uniform(0.5, 2, 8).astype(np.float32)
+    dev = DeviceLayer.upload(host)
+    x = margin.tokens_with_margin(host, 3, seed=17)
+    _check(host, dev, x)
+
+
+FULL = [(name, N) for name in ("tiny", "qwen3_30b_a3b", "mtp_verify", "deepseek_v3", "gpt_oss_120b")
+        for N in synth.CONFIGS[name].tokens if N <= 64]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name,N", FULL)
+def test_full_size(name, N):
+    host, dev = full_layer(name)
+    x = margin.tokens_with_margin(host, N)
+    _check(host, dev, x)
