@@ -1,0 +1,390 @@
+"""Benchmark of the MoE decode-layer forward on one GB300 (or N replicas).
+
+Workload: the Qwen3-30B-A3B-shaped layer (H 2048, inter 768, 128 NVFP4
+experts, top-8 softmax with renormalisation) at N = 1, 2, 3, 4 tokens.  One
+step = four moe_forward calls, N = 1, 2, 3, 4, on one layer copy; successive
+steps use different layer copies (L2 defeat: one cycle of copies touches many
+times the 129 MB L2).  The metric is the achieved HBM rate over algorithmic
+bytes:
+    bytes(call) = U * expert_bytes + router_bytes + shared_bytes + x/out bytes
+with U the number of distinct routed experts the call's tokens touched (read
+back from the routing outputs before timing).  value = sum of bytes / time.
+
+Timed region: K steps replayed from a captured CUDA graph, bracketed by a
+barrier and torch.cuda.synchronize(), CUDA events on the launch stream; the
+maximum over ranks is taken.  --impl reference times the FP64 CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PEAK_FALLBACK_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+METRIC = "MoE layer us and expert-weight HBM GB/s (fraction of 8 TB/s) at N=1-4 tokens"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return PEAK_FALLBACK_GBS, "fallback"
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        self.path = os.path.join("/tmp", f"moe_clocks_{os.getpid()}.csv")
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if not self.path or not os.path.exists(self.path):
+            return out
+        sms, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if sms:
+            out.update(sm_mhz=float(np.median(sms)), sm_max_mhz=float(max(mx)),
+                       reasons=sorted(reasons), samples=len(sms))
+        return out
+
+
+def algorithmic_bytes(spec, idx: np.ndarray, N: int) -> dict:
+    """Bytes one call must move: touched routed experts, router, shared expert,
+    x in and out."""
+    U = len(np.unique(idx))
+    routed = U * spec.expert_bytes()
+    other = spec.router_bytes() + spec.shared_bytes() + 2 * N * spec.H * 2
+    return {"U": U, "routed": routed, "total": routed + other}
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    from moe_decode_layer_topk_gb300 import _lib, synth
+    from moe_decode_layer_topk_gb300.device import DeviceLayer, bf16_tensor, workspace
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    spec = synth.CONFIGS[args.config]
+    tokens = [n for n in spec.tokens if n <= 64] if args.tokens is None else args.tokens
+    base = DeviceLayer.upload(synth.make_layer(spec))
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    R = args.copies
+    copies = [base] + [base.clone() for _ in range(R - 1)]
+    stream = torch.cuda.Stream()
+    maxN = max(tokens)
+    calls = []   # [layer copy, N, x, out, ws, bytes]
+    for r in range(R):
+        for N in tokens:
+            x = bf16_tensor(synth.make_tokens(spec, N, seed=90000 + 1000 * rank + 17 * r + N))
+            calls.append([copies[r], N, x, torch.empty_like(x), workspace(spec, maxN)])
+    # routing of every call (untimed) to count its algorithmic bytes
+    per_cycle_bytes = 0
+    for c in calls:
+        dev, N, x, out, ws = c
+        idx = torch.empty((N, spec.top_k), dtype=torch.int32, device="cuda")
+        w = torch.empty((N, spec.top_k), dtype=torch.float32, device="cuda")
+        _lib.moe_forward(dev.desc, dev.weights, x, out, ws, idx, w)
+        torch.cuda.synchronize()
+        c.append(algorithmic_bytes(spec, idx.cpu().numpy(), N))
+        per_cycle_bytes += c[-1]["total"]
+    for c in calls:
+        assert _lib.moe_get_error(c[4]) == _lib.MOE_OK
+    launches_per_cycle = len(calls)
+
+    def enqueue_cycle():
+        for dev, N, x, out, ws, _ in calls:
+            _lib.moe_forward(dev.desc, dev.weights, x, out, ws, stream=stream)
+
+    graph = None
+    if not args.no_graph:
+        with torch.cuda.stream(stream):
+            enqueue_cycle()
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            enqueue_cycle()
+
+    def run_cycle():
+        if graph is not None:
+            graph.replay()
+        else:
+            enqueue_cycle()
+
+    steps_per_cycle = R          # a step is one N sweep on one layer copy
+    cycles_warm = max(1, -(-args.warmup // steps_per_cycle))
+    cycles = max(1, -(-args.steps // steps_per_cycle))
+    with torch.cuda.stream(stream):
+        for _ in range(cycles_warm):
+            run_cycle()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(cycles):
+                run_cycle()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    for c in calls:
+        assert _lib.moe_get_error(c[4]) == _lib.MOE_OK, "device-side wait expired during timing"
+    steps = cycles * steps_per_cycle
+    value = cycles * per_cycle_bytes * world / (ms / 1e3) / 1e9
+    launches = cycles * launches_per_cycle
+    avg_launch_us = ms * 1e3 / launches
+    achieved = per_cycle_bytes / launches_per_cycle / (avg_launch_us * 1e-6) / 1e9
+
+    # per-token-count latency (separate loop after the timed region)
+    per_n = {}
+    for N in tokens:
+        sub = [c for c in calls if c[1] == N]
+        reps = max(32, min(args.steps, 400))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g = None
+        if not args.no_graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for dev, n_, x, out, ws, _ in sub:
+                    _lib.moe_forward(dev.desc, dev.weights, x, out, ws, stream=stream)
+        rounds = max(1, reps // len(sub))
+        with torch.cuda.stream(stream):
+            if g is not None:
+                g.replay()
+            e0.record(stream)
+            for _ in range(rounds):
+                if g is not None:
+                    g.replay()
+                else:
+                    for dev, n_, x, out, ws, _ in sub:
+                        _lib.moe_forward(dev.desc, dev.weights, x, out, ws, stream=stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (rounds * len(sub))
+        b = float(np.mean([c[5]["total"] for c in sub]))
+        br = float(np.mean([c[5]["routed"] for c in sub]))
+        per_n[str(N)] = {"us_per_layer": round(us, 3), "tokens_per_s": round(N / us * 1e6, 1),
+                         "GBps": round(b / us / 1e3, 1),
+                         "frac_of_8TBs": round(b / us / 1e3 / NOMINAL_HBM_GBS, 4),
+                         "U_mean": float(np.mean([c[5]["U"] for c in sub])),
+                         "bytes_mean": int(b), "routed_bytes_mean": int(br)}
+
+    # end to end through the host-buffer entry point (pinned host x / out)
+    e2e = None
+    if rank == 0 and not args.no_e2e:
+        wsh = workspace(spec, maxN, host_staging=True)
+        hx = [calls[i][2].cpu().pin_memory() for i in range(len(tokens))]
+        ho = [torch.empty_like(h).pin_memory() for h in hx]
+        for i in range(len(tokens)):
+            _lib.moe_forward_host(base.desc, base.weights, hx[i], ho[i], wsh, stream=stream)
+        e2e_steps = max(3, min(args.steps, 100))
+        t0 = time.perf_counter()
+        for s_ in range(e2e_steps):
+            cp = copies[s_ % R]
+            for i in range(len(tokens)):
+                _lib.moe_forward_host(cp.desc, cp.weights, hx[i], ho[i], wsh, stream=stream)
+        dt = time.perf_counter() - t0
+        b_step = sum(c[5]["total"] for c in calls[: len(tokens)])
+        io = int(sum(N * spec.H * 2 for N in tokens))
+        e2e = {"value": round(b_step * e2e_steps / dt / 1e9, 2), "unit": "GB/s",
+               "us_per_step": round(dt / e2e_steps * 1e6, 2),
+               "h2d_bytes_per_step": io, "d2h_bytes_per_step": io}
+
+    peak, peak_kind = _peaks()
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": cycles_warm * steps_per_cycle,
+        "ms_per_step": round(ms / steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e2m1/e4m3 weights, f16x2 block sums, f32 accumulate",
+        "data": "synthetic (seeded N(0,0.02) NVFP4 experts, N(0,1/H) bf16 router, RMS-normed bf16 x)",
+        "config": {"workload": f"{spec.name} layer, one step = moe_forward at N={','.join(map(str, tokens))}",
+                   "H": spec.H, "inter": spec.inter, "E": spec.E, "top_k": spec.top_k,
+                   "wfmt": spec.wfmt, "shared_inter": spec.shared_inter,
+                   "layer_copies": R, "l2_bytes": l2,
+                   "l2_defeat": f"inputs larger than L2: {R} layer copies cycled, "
+                                f"{per_cycle_bytes / l2:.1f}x L2 touched per cycle",
+                   "cuda_graph": graph is not None,
+                   "parallelism": f"{world} replicas" if world > 1 else "single GPU"},
+        "frac_of_8TBs": round(value / world / NOMINAL_HBM_GBS, 4),
+        "us_per_layer_mean": round(avg_launch_us, 3),
+        "per_n": per_n,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": args.traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
+                     "kernel": "moe::moe_decode_kernel"},
+        "gpu_launches": launches,
+        "e2e": e2e,
+    }
+    if rank == 0:
+        result["clocks"] = clk.summary()
+        if not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(spec, tokens, args.cpu_seconds)
+        print(json.dumps(result))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def cpu_baseline(spec, tokens, budget_s: float):
+    """The FP64 oracle (as it stands) on a bounded sample of the workload."""
+    from moe_decode_layer_topk_gb300 import synth
+    from oracle import oracle
+    host = synth.make_layer(spec)
+    nbytes, t_total, steps = 0, 0.0, 0
+    while t_total < budget_s:
+        for N in tokens:
+            x = synth.make_tokens(spec, N, seed=70000 + 31 * steps + N)
+            t0 = time.perf_counter()
+            r = oracle.moe_forward(host, x)
+            t_total += time.perf_counter() - t0
+            nbytes += algorithmic_bytes(spec, r["idx"], N)["total"]
+        steps += 1
+    return {"value": round(nbytes / t_total / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{steps} steps of moe_forward at N={','.join(map(str, tokens))} on "
+                      f"{spec.name} ({t_total:.1f} s of CPU time)"}
+
+
+def run_reference(args):
+    """Reference arm: the FP64 oracle on the host cores (rank 0 only); one step
+    is the same N sweep as our arm; K steps after W warm-up steps, stopped
+    early (and reported as such) once the sample reaches its time budget."""
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    from moe_decode_layer_topk_gb300 import synth
+    from oracle import oracle
+    spec = synth.CONFIGS[args.config]
+    tokens = [n for n in spec.tokens if n <= 64] if args.tokens is None else args.tokens
+    host = synth.make_layer(spec)
+    xs = [synth.make_tokens(spec, N, seed=70000 + N) for N in tokens]
+    for _ in range(min(args.warmup, 2)):
+        for x in xs:
+            oracle.moe_forward(host, x)
+    nbytes, steps, t0 = 0, 0, time.perf_counter()
+    while steps < args.steps:
+        for N, x in zip(tokens, xs):
+            r = oracle.moe_forward(host, x)
+            nbytes += algorithmic_bytes(spec, r["idx"], N)["total"]
+        steps += 1
+        if time.perf_counter() - t0 > args.ref_seconds:
+            break
+    dt = time.perf_counter() - t0
+    v = nbytes / dt / 1e9
+    sample = (f"{steps} of {args.steps} steps of moe_forward at N={','.join(map(str, tokens))} on "
+              f"{spec.name} ({dt:.1f} s)")
+    print(json.dumps({
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": min(args.warmup, 2), "ms_per_step": round(dt / steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (same seeded layer as our arm)",
+        "config": {"workload": f"{spec.name} layer, one step = moe_forward at N={','.join(map(str, tokens))}"},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="qwen3_30b_a3b")
+    ap.add_argument("--tokens", type=int, nargs="*", default=None)
+    ap.add_argument("--copies", type=int, default=16)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=120.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram read+write bytes per launch from an ncu capture of this kernel")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        import __graft_entry__
+        __graft_entry__.build()
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
