@@ -170,6 +170,35 @@ MOE_API const char* moe_status_string(moe_status_t status);
 /* Library version, for the binding to check it loaded the library it expects. */
 MOE_API int32_t moe_abi_version(void);
 
+/* moe_forward for callers that cannot allocate device memory.  Some callers
+ * have no way to obtain a workspace: an allocator-free embedded runtime, a
+ * plug-in that is handed only its input and output buffers, or code that must
+ * not call cudaMalloc or touch a framework's memory pool.  This entry point
+ * computes exactly what moe_forward computes (same arguments minus the
+ * workspace, same constraints, same outputs) but runs in a fixed 8 MiB scratch
+ * array that the library keeps in device memory (a file-scope __device__
+ * array: every GPU that loads the library holds it until the process exits).
+ * It calls no cudaMalloc, cudaFree or allocating library routine.
+ *   - A shape whose moe_workspace_size(desc, N) exceeds 8 MiB is refused with
+ *     MOE_ERR_WORKSPACE_TOO_SMALL; use moe_forward with a caller workspace.
+ *   - The first call on a device looks up the array's device address with
+ *     cudaGetSymbolAddress (once per device, with that device current); make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one array and it keeps the last call's
+ *     contents; each call clears its control words (an async memset on
+ *     `stream`) and the kernel zeroes its accumulator, so nothing carries over
+ *     between calls that run one after another.  Calls that overlap on the GPU
+ *     (different streams, no ordering between them) race on the array: order
+ *     them on one stream.
+ *   - Device-side wait timeouts are not reported for this variant (there is no
+ *     caller workspace to hand to moe_get_error).
+ * The pages have no counterpart of this entry point; it exists for callers
+ * that cannot allocate. */
+MOE_API moe_status_t moe_forward_noalloc(const moe_layer_desc_t* desc,
+                                         const moe_weights_t* weights, const void* x,
+                                         int32_t N, void* out, int32_t* topk_idx,
+                                         float* topk_w, void* stream);
+
 /* Test hook: time budget, in nanoseconds, of every bounded device-side wait
  * (grid barrier, stage arrival) for calls enqueued afterwards; default 1e9.
  * A budget of 0 makes a wait that is not already satisfied expire at once, so

@@ -28,7 +28,7 @@ MOE_W_MXFP4 = 1
 
 EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_forward", "moe_route",
             "moe_host_staging_size", "moe_forward_host", "moe_get_error", "moe_status_string",
-            "moe_abi_version", "moe_debug_set_wait_budget_ns")
+            "moe_abi_version", "moe_debug_set_wait_budget_ns", "moe_forward_noalloc")
 
 
 class MoeError(RuntimeError):
@@ -83,6 +83,8 @@ def load() -> ctypes.CDLL:
         L.moe_status_string.argtypes = [i32]
         L.moe_abi_version.restype = i32
         L.moe_abi_version.argtypes = []
+        L.moe_forward_noalloc.restype = i32
+        L.moe_forward_noalloc.argtypes = [pd, pw, vp, i32, vp, vp, vp, vp]
         L.moe_debug_set_wait_budget_ns.restype = None
         L.moe_debug_set_wait_budget_ns.argtypes = [ctypes.c_ulonglong]
         if L.moe_abi_version() != ABI_VERSION:
@@ -159,6 +161,18 @@ def moe_forward_host(desc: LayerDesc, weights: Weights, x_host, out_host, ws, st
                                  ws.numel() * ws.element_size(), _stream(stream))
     if check:
         _check(st, "moe_forward_host")
+    return st
+
+
+def moe_forward_noalloc(desc: LayerDesc, weights: Weights, x, out, topk_idx=None, topk_w=None,
+                        stream=None, check: bool = True) -> int:
+    """moe_forward in the library's built-in device scratch (no workspace
+    argument, no allocation); for callers that cannot allocate device memory."""
+    st = load().moe_forward_noalloc(ctypes.byref(desc), ctypes.byref(weights), _ptr(x),
+                                    int(x.shape[0]), _ptr(out), _ptr(topk_idx), _ptr(topk_w),
+                                    _stream(stream))
+    if check:
+        _check(st, "moe_forward_noalloc")
     return st
 
 

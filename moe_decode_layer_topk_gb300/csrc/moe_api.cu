@@ -175,6 +175,34 @@ moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* 
   return MOE_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Built-in scratch for moe_forward_noalloc.  Some callers cannot allocate
+// device memory at all (an allocator-free runtime, a plug-in that only
+// receives input/output buffers, code that must not touch the CUDA memory
+// pool); this array stands in for the caller workspace.  It is zero at module
+// load, lives on every GPU that loads the library until the process exits,
+// and is shared by every call on that GPU.  In host code its name is only a
+// host-side stand-in: the device address is obtained with
+// cudaGetSymbolAddress, once per device, with that device current.
+constexpr size_t kNoAllocScratchBytes = 8u << 20;   // 8 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {nullptr};
+
+moe_status_t noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -259,6 +287,29 @@ const char* moe_status_string(moe_status_t status) {
 }
 
 int32_t moe_abi_version(void) { return kAbiVersion; }
+
+/* moe_forward without a caller workspace: the scratch is the library's
+ * built-in 8 MiB device array (see the declaration in moe.h). */
+moe_status_t moe_forward_noalloc(const moe_layer_desc_t* desc, const moe_weights_t* weights,
+                                 const void* x, int32_t N, void* out, int32_t* topk_idx,
+                                 float* topk_w, void* stream) {
+  moe_status_t st = check_desc(desc);
+  if (st != MOE_OK) return st;
+  st = check_weights(desc, weights);
+  if (st != MOE_OK) return st;
+  if (N < 1) return MOE_ERR_INVALID_ARG;
+  if ((long long)N * desc->top_k > moe::kMaxSlots) return MOE_ERR_UNSUPPORTED;
+  if (!x || !aligned16(x) || !out || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if (ws_layout(*desc, N).total > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  void* ws = nullptr;
+  st = noalloc_scratch(&ws);
+  if (st != MOE_OK) return st;
+  // the control block (grid-barrier words, error word) must start at zero;
+  // the kernel itself zeroes its accumulator and counters every call
+  if (cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return run(desc, weights, x, N, out, topk_idx, topk_w, ws, kNoAllocScratchBytes, stream, 0);
+}
 
 /* Test hook: budget of every bounded device wait, in nanoseconds, for calls
  * enqueued afterwards (default 1e9).  A budget of 0 makes any wait that is not
