@@ -6,6 +6,7 @@
 // forward_atomic_c4.rs: every refusal returns a status before anything is
 // enqueued.
 
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -107,6 +108,88 @@ moe_status_t device_info(int* budget, int* grid) {
 
 unsigned long long g_timeout_ns = 1000000000ull;   // bounded waits: 1 s
 
+// ------------------------------------------------------------ tensor maps
+// 2D views of the weight tensors for the kernel's TMA loads: rows of `inner`
+// bytes, `rows` rows, boxes of 32 rows x `box` bytes (128-byte swizzle when
+// the box is a full 128-byte line).  Encodings are cached by their key.
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+struct TmKey {
+  const void* ptr;
+  uint64_t inner, rows;
+  uint32_t box;
+  int swz;
+  bool operator==(const TmKey& o) const {
+    return ptr == o.ptr && inner == o.inner && rows == o.rows && box == o.box && swz == o.swz;
+  }
+};
+struct TmEntry {
+  TmKey key;
+  CUtensorMap map;
+  bool used;
+};
+constexpr int kTmCache = 64;
+TmEntry g_tm_cache[kTmCache];
+int g_tm_next = 0;
+
+bool encode_2d(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box,
+               int swz) {   // swz: 0 none, 64 or 128 (bytes)
+  const TmKey key{ptr, inner, rows, box, swz};
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& e : g_tm_cache)
+    if (e.used && e.key == key) {
+      *out = e.map;
+      return true;
+    }
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t boxd[2] = {box, (cuuint32_t)moe::kRows};
+  cuuint32_t es[2] = {1, 1};
+  CUtensorMap m;
+  if (g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, boxd,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               swz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                          : swz == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  TmEntry& e = g_tm_cache[g_tm_next];
+  g_tm_next = (g_tm_next + 1) % kTmCache;
+  e.key = key;
+  e.map = m;
+  e.used = true;
+  *out = m;
+  return true;
+}
+
+// Weight-row map of one projection (packed FP4 or BF16 bytes).
+bool encode_rows(moe::Params& p, int slot, const void* ptr, const moe::Geo& g, uint64_t rows) {
+  const bool sw = g.kb >= moe::kBoxBytes;
+  if (!encode_2d(&p.tm[slot], ptr, (uint64_t)g.kb, rows, sw ? moe::kBoxBytes : (uint32_t)g.kb,
+                 sw ? 128 : 0))
+    return false;
+  p.tm_valid |= 1u << slot;
+  return true;
+}
+
+// Block-scale map of one projection (tensor-map scale mode only); 64-byte box
+// rows are swizzled so the kernel's per-lane scale loads avoid bank conflicts.
+bool encode_scales(moe::Params& p, int slot, const void* ptr, const moe::Geo& g, uint64_t rows) {
+  if (g.scale_mode != moe::SCALES_TMAP) return true;
+  if (!encode_2d(&p.tm[slot], ptr, (uint64_t)g.sr, rows, (uint32_t)g.scb, g.scb == 64 ? 64 : 0))
+    return false;
+  p.tm_valid |= 1u << slot;
+  return true;
+}
+
 moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* x, int32_t N,
                  void* out, int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
                  void* stream, int route_only) {
@@ -141,25 +224,19 @@ moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* 
   p.route_only = route_only;
   p.router = static_cast<const uint16_t*>(w->router);
   p.bias = d->scoring == MOE_SCORE_SIGMOID_BIAS ? w->bias : nullptr;
-  p.gq = w->gate_q;
-  p.uq = w->up_q;
-  p.dq = w->down_q;
   p.gsc = w->gate_s;
   p.usc = w->up_s;
   p.dsc = w->down_s;
   p.g2 = w->gate_s2;
   p.u2 = w->up_s2;
   p.d2 = w->down_s2;
-  p.shg = static_cast<const uint16_t*>(w->sh_gate);
-  p.shu = static_cast<const uint16_t*>(w->sh_up);
-  p.shd = static_cast<const uint16_t*>(w->sh_down);
   p.shw = d->shared_inter > 0 ? static_cast<const uint16_t*>(w->sh_gate_w) : nullptr;
   p.x = static_cast<const uint16_t*>(x);
   p.out = static_cast<uint16_t*>(out);
   p.topk_idx = topk_idx;
   p.topk_w = topk_w;
   uint8_t* b = static_cast<uint8_t*>(ws);
-  p.ctrl = reinterpret_cast<uint32_t*>(b + L.ctrl);
+  p.ctrl = reinterpret_cast<moe::Ctrl*>(b + L.ctrl);
   p.logits = reinterpret_cast<float*>(b + L.logits);
   p.x16 = reinterpret_cast<uint16_t*>(b + L.x16);
   p.xexp = reinterpret_cast<int*>(b + L.xexp);
@@ -170,6 +247,22 @@ moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* 
   p.rbcnt = reinterpret_cast<uint32_t*>(b + L.rbcnt);
   p.timeout_ns = g_timeout_ns;
   if (!moe::plan_decode(p, budget)) return MOE_ERR_UNSUPPORTED;
+  if (!route_only) {
+    const uint64_t ER = (uint64_t)d->E;
+    const moe::Geo& ga = p.geo[moe::KIND_AR];
+    const moe::Geo& gb = p.geo[moe::KIND_BR];
+    bool ok = encode_rows(p, moe::TM_GQ, w->gate_q, ga, ER * d->inter) &&
+              encode_rows(p, moe::TM_UQ, w->up_q, ga, ER * d->inter) &&
+              encode_rows(p, moe::TM_DQ, w->down_q, gb, ER * d->H) &&
+              encode_scales(p, moe::TM_GS, w->gate_s, ga, ER * d->inter) &&
+              encode_scales(p, moe::TM_US, w->up_s, ga, ER * d->inter) &&
+              encode_scales(p, moe::TM_DS, w->down_s, gb, ER * d->H);
+    if (ok && d->shared_inter > 0)
+      ok = encode_rows(p, moe::TM_SG, w->sh_gate, p.geo[moe::KIND_AS], (uint64_t)d->shared_inter) &&
+           encode_rows(p, moe::TM_SU, w->sh_up, p.geo[moe::KIND_AS], (uint64_t)d->shared_inter) &&
+           encode_rows(p, moe::TM_SD, w->sh_down, p.geo[moe::KIND_BS], (uint64_t)d->H);
+    if (!ok) return MOE_ERR_CUDA;
+  }
   if (moe::launch_decode(p, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
@@ -264,12 +357,12 @@ moe_status_t moe_get_error(void* workspace, void* stream) {
   if (!workspace) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint32_t word = 0;
-  uint32_t* ctrl = static_cast<uint32_t*>(workspace);
-  if (cudaMemcpyAsync(&word, ctrl + 2, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+  uint32_t* err = &static_cast<moe::Ctrl*>(workspace)->error;
+  if (cudaMemcpyAsync(&word, err, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   if (word == 0) return MOE_OK;
-  if (cudaMemsetAsync(ctrl + 2, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(err, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_ERR_TIMEOUT;
 }

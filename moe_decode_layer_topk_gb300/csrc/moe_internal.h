@@ -1,6 +1,7 @@
 // Internal interface between the C ABI layer (moe_api.cu) and the fused
 // decode kernel (decode_kernel.cu).  Host and device code.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -16,29 +17,41 @@ constexpr int kMaxSlots = 256;                    // N * top_k per call
 constexpr int kMaxE = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxStages = 8;
+constexpr int kBoxBytes = 128;                    // inner extent of a weight box
+constexpr int kBoxesPerChunk = 4;                 // chunk = 512 bytes of each row
+constexpr int kChunkBytes = kBoxBytes * kBoxesPerChunk;
+constexpr int kBoxTileBytes = kRows * kBoxBytes;  // 4 KB: one 32-row box in smem
+constexpr int kMaxRgList = 512;                   // down row groups tracked per CTA
 
 enum Kind { KIND_AS = 0, KIND_AR = 1, KIND_BR = 2, KIND_BS = 3 };
 enum Fmt { FMT_NVFP4 = 0, FMT_MXFP4 = 1, FMT_BF16 = 2 };
-enum ScaleMode { SCALES_NONE = 0, SCALES_PER_ROW = 1, SCALES_BLOCK = 2 };
+enum ScaleMode { SCALES_NONE = 0, SCALES_TMAP = 1, SCALES_BLOCK = 2 };
+// tensor map slots
+enum TMap { TM_GQ = 0, TM_UQ, TM_DQ, TM_GS, TM_US, TM_DS, TM_SG, TM_SU, TM_SD, TM_COUNT };
 
 // Device-side error word bits (workspace control block).
 constexpr uint32_t kErrTimeoutBarrier = 1u;
 constexpr uint32_t kErrTimeoutStage = 2u;
 constexpr uint32_t kErrTimeoutProducer = 4u;
 
+// Workspace control block (first 256 bytes of the workspace).
+struct Ctrl {
+  unsigned long long arrivals;   // grid-barrier arrivals, monotonic (2 per CTA per call)
+  uint32_t error;                // sticky error bits
+  uint32_t pad[61];
+};
+
 // Stage geometry of one kind of row group (see decode_kernel.cu).
 struct Geo {
   int fmt;          // Fmt
   int nproj;        // weight matrices streamed together (2 = gate+up, 1 = down)
   int K;            // reduction length (input dim of the projection)
-  int Kc;           // K elements per stage (chunk)
-  int nchunks;      // K / Kc
-  int row_bytes;    // bytes of one weight row's chunk
-  int row_stride;   // padded stride of weight rows in the stage (odd x 16 B)
+  int kb;           // bytes of one full weight row
+  int Kc;           // K elements per full chunk (512 bytes of row)
+  int nchunks;      // ceil(kb / 512)
   int scale_mode;   // ScaleMode
   int sr;           // scale bytes per full weight row (K / gs); 0 for bf16
-  int scale_bytes;  // per-row chunk scale bytes (PER_ROW) or sr (BLOCK)
-  int scale_stride; // stride of scale rows in the stage
+  int scb;          // scale bytes per row per chunk (TMAP mode)
   int scale_off;    // offset of the scale region in the stage
   int opnd_off;     // offset of the activation chunk region (-1: from hbuf)
   int stage_bytes;  // bytes used in a stage
@@ -46,6 +59,8 @@ struct Geo {
 };
 
 struct Params {
+  CUtensorMap tm[TM_COUNT];   // 2D maps: packed/bf16 weights (swizzle 128B), scales
+  uint32_t tm_valid;          // bit i set when tm[i] is encoded
   // layer
   int H, inter, E, k, scoring, norm;
   float rsf;
@@ -56,16 +71,16 @@ struct Params {
   // weights (device)
   const uint16_t* router;
   const float* bias;
-  const uint8_t *gq, *uq, *dq, *gsc, *usc, *dsc;
+  const uint8_t *gsc, *usc, *dsc;   // scales, for 1D block copies
   const float *g2, *u2, *d2;
-  const uint16_t *shg, *shu, *shd, *shw;
+  const uint16_t* shw;
   // activations / outputs (device)
   const uint16_t* x;
   uint16_t* out;
   int32_t* topk_idx;
   float* topk_w;
   // workspace (device)
-  uint32_t* ctrl;    // [0] barrier count, [1] barrier generation, [2] error word
+  Ctrl* ctrl;
   float* logits;     // [N, E]
   uint16_t* x16;     // [N, H] f16, x * 2^-xexp[n]
   int* xexp;         // [N]
@@ -89,10 +104,11 @@ bool plan_decode(Params& p, int smem_budget);
 // Shared memory the decode kernel may use on this device.
 int decode_smem_budget(int device);
 
+// Number of CTAs the decode kernel runs with on `device` (one per SM); also
+// raises the kernels' dynamic shared-memory limit to `smem_bytes`.
+int decode_grid(int device, int smem_bytes);
+
 // Enqueue the fused decode kernel; returns a CUDA error code.
 cudaError_t launch_decode(const Params& p, int grid, cudaStream_t stream);
-
-// Number of CTAs the decode kernel runs with on `device` (one per SM).
-int decode_grid(int device, int smem_bytes);
 
 }  // namespace moe
