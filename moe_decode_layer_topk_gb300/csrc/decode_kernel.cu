@@ -263,16 +263,15 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 // all E, optionally renormalised over the selected) or sigmoid + bias
 // (selection by sigmoid(l) + bias, weights sigmoid(l), optional
 // renormalisation, times the routed scaling factor).  Ties go to the lower
-// expert index.  Results to tb.sel_e / tb.sel_w in selection order.
+// expert index.  The k selections are k rounds of a warp arg-max (lane j keeps
+// the j-th winner); the weights are then computed by lanes j < k in parallel.
 template <int PER>
-__device__ void topk_token(const Params& p, int n, Tables& tb, int lane) {
-  const int E = p.E, k = p.k, scoring = p.scoring, norm = p.norm;
-  const float rsf = p.rsf;
-  const float* bias = p.bias;
-  const float* lrow = p.logits + (size_t)n * E;
+__device__ __forceinline__ void topk_token(int E, int k, int scoring, int norm, float rsf,
+                                           const float* bias, const float* lrow, int n,
+                                           Tables& tb, int lane) {
   uint32_t key[PER];
+  float mx = -INFINITY, den = 0.f;
   float lg[PER];
-  float mx = -INFINITY;
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int e = lane + 32 * i;
@@ -282,118 +281,208 @@ __device__ void topk_token(const Params& p, int n, Tables& tb, int lane) {
       const float l = ld_cg_f32(lrow + e);
       lg[i] = l;
       mx = fmaxf(mx, l);
-      float s = l;
-      if (scoring == 1) s = 1.0f / (1.0f + expf(-l)) + bias[e];
-      key[i] = order_key(s);
+      key[i] = order_key(scoring == 1 ? 1.0f / (1.0f + expf(-l)) + bias[e] : l);
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float den = 0.f;
-  if (scoring == 0) {
-#pragma unroll
-    for (int i = 0; i < PER; ++i)
-      if (lane + 32 * i < E) den += expf(lg[i] - mx);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-  }
-  uint32_t bk = 0u, be = 0xFFFFFFFFu;   // lane-local best (lowest index among equals)
+  uint32_t bk = 0u, be = 0xFFFFFFFFu;   // lane-local best, lowest index among equals
 #pragma unroll
   for (int i = 0; i < PER; ++i)
     if (key[i] > bk) { bk = key[i]; be = lane + 32 * i; }
-  float wsum = 0.f, wsel = 0.f;
-  int esel = 0;
+  uint32_t mine = 0u;                   // lane j: expert of selection j
   for (int j = 0; j < k; ++j) {
     const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
     uint32_t we = __reduce_min_sync(0xffffffffu, (bk == m) ? be : 0xFFFFFFFFu);
-    if (we >= (uint32_t)E) we = 0;   // only if fewer than k keys are valid (k <= E is checked)
-    float lw = 0.f;
-    if (lane == (int)(we & 31u)) {
+    if (we >= (uint32_t)E) we = 0;      // only if fewer than k valid keys (k <= E is checked)
+    if (lane == j) mine = we;
+    if ((we & 31u) == (uint32_t)lane) {
 #pragma unroll
       for (int i = 0; i < PER; ++i)
-        if (lane + 32 * i == (int)we) { lw = lg[i]; key[i] = 0u; }
+        if (lane + 32 * i == (int)we) key[i] = 0u;
       bk = 0u;
       be = 0xFFFFFFFFu;
 #pragma unroll
       for (int i = 0; i < PER; ++i)
         if (key[i] > bk) { bk = key[i]; be = lane + 32 * i; }
     }
-    lw = __shfl_sync(0xffffffffu, lw, we & 31u);
-    const float w = (scoring == 0) ? expf(lw - mx) / den : 1.0f / (1.0f + expf(-lw));
-    wsum += w;
-    if (lane == j) { wsel = w; esel = (int)we; }
   }
+  if (scoring == 0) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      if (lane + 32 * i < E) den += expf(lg[i] - mx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  }
+  // logit of this lane's selection, from the lane that holds it
+  float l = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const float v = __shfl_sync(0xffffffffu, lg[i], mine & 31u);
+    if ((int)(mine >> 5) == i) l = v;
+  }
+  float w = 0.f;
+  if (lane < k) w = (scoring == 0) ? expf(l - mx) / den : 1.0f / (1.0f + expf(-l));
+  float wsum = w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
   if (lane < k) {
-    float w = wsel;
     if (norm) w = w / wsum;
     if (scoring == 1) w *= rsf;
-    tb.sel_e[n * k + lane] = (int16_t)esel;
+    tb.sel_e[n * k + lane] = (int16_t)mine;
     tb.sel_w[n * k + lane] = w;
   }
 }
 
-// Routing for all tokens + unique-expert tables (identical in every CTA).
-__device__ __noinline__ void routing_phase(const Params& p, int cta, Tables& tb, int ctid) {
-  const int warp = ctid >> 5, lane = ctid & 31;
-  const int E = p.E, k = p.k, S = p.N * p.k;
-  for (int n = warp; n < p.N; n += kConsumerWarps) {
-    if (E <= 128) topk_token<4>(p, n, tb, lane);
-    else if (E <= 256) topk_token<8>(p, n, tb, lane);
-    else if (E <= 512) topk_token<16>(p, n, tb, lane);
-    else topk_token<32>(p, n, tb, lane);
+// Small case (S = N*k <= 32, every expert has <= kTB tokens): the same tables
+// as build_tables, from one slot per lane in registers.
+__device__ __forceinline__ bool build_tables_small(int k, int S, Tables& tb, int lane) {
+  const bool v = lane < S;
+  const int e = v ? tb.sel_e[lane] : -1 - lane;
+  const float wv = v ? tb.sel_w[lane] : 0.f;
+  const uint32_t lt = (1u << lane) - 1u;
+  const uint32_t peers = __match_any_sync(0xffffffffu, e);
+  const int cnt = __popc(peers), pos = __popc(peers & lt);
+  if (!__all_sync(0xffffffffu, !v || cnt <= kTB)) return false;
+  const bool isfirst = v && pos == 0;
+  const uint32_t fmask = __ballot_sync(0xffffffffu, isfirst);
+  const int leader = __ffs(peers) - 1;
+  const int u = __shfl_sync(0xffffffffu, __popc(fmask & lt), leader);   // unique index
+  int inc = isfirst ? cnt : 0;                       // slot offsets over first lanes
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += t;
   }
-  for (int e = ctid; e < E; e += kConsumerThreads) tb.cnt[e] = 0u;
-  consumer_sync();
-  for (int s = ctid; s < S; s += kConsumerThreads) atomicAdd(&tb.cnt[tb.sel_e[s]], 1u);
-  consumer_sync();
-  // scan over experts of (present, count) packed as (1 << 16) | count
-  const int per = (E + kConsumerThreads - 1) / kConsumerThreads;   // <= 4
-  const int e0 = ctid * per;
-  uint32_t loc = 0;
-  for (int i = 0; i < per; ++i) {
-    const int e = e0 + i;
-    if (e < E && tb.cnt[e]) loc += (1u << 16) | tb.cnt[e];
+  const int hoff = __shfl_sync(0xffffffffu, inc - (isfirst ? cnt : 0), leader);
+  if (v) {
+    tb.utok[hoff + pos] = (uint8_t)(lane / k);
+    tb.uw[hoff + pos] = wv;
   }
-  uint32_t tot;
-  uint32_t pre = block_excl_scan(loc, tb, ctid, &tot);
-  for (int i = 0; i < per; ++i) {
-    const int e = e0 + i;
-    if (e < E && tb.cnt[e]) {
-      const uint32_t u = pre >> 16, off = pre & 0xFFFFu, c = tb.cnt[e];
+  if (isfirst) {
+    tb.uexp[u] = (int16_t)e;
+    tb.ucnt[u] = (uint16_t)cnt;
+    tb.hoff[u] = (uint16_t)hoff;
+    tb.unit_u[u] = (uint16_t)u;
+    tb.unit_tb[u] = 0;
+  }
+  if (lane == 0) {
+    tb.U = __popc(fmask);
+    tb.n_units = __popc(fmask);
+  }
+  return true;
+}
+
+// Unique experts and per-expert token lists from the S = N*k selections, by
+// one warp.  Unique experts are ordered by their first selection slot
+// (token-major), tokens of an expert by token index; every CTA builds the
+// same tables from the same routing.
+__device__ __forceinline__ void build_tables(int E, int k, int S, Tables& tb, int lane) {
+  uint32_t* first = tb.cnt;              // first slot of each expert, then its unique index
+  for (int e = lane; e < E; e += 32) first[e] = 0xFFFFFFFFu;
+  __syncwarp();
+  for (int s = lane; s < S; s += 32) atomicMin(&first[tb.sel_e[s]], (uint32_t)s);
+  __syncwarp();
+  const uint32_t lt = (1u << lane) - 1u;
+  int U = 0;
+  for (int b = 0; b < S; b += 32) {          // unique experts in first-slot order
+    const int s = b + lane;
+    const int e = (s < S) ? tb.sel_e[s] : 0;
+    const bool isfirst = (s < S) && first[e] == (uint32_t)s;
+    const uint32_t mask = __ballot_sync(0xffffffffu, isfirst);
+    if (isfirst) {
+      const int u = U + __popc(mask & lt);
       tb.uexp[u] = (int16_t)e;
-      tb.ucnt[u] = (uint16_t)c;
-      tb.hoff[u] = (uint16_t)off;
-      tb.cnt[e] = u;
-      pre += (1u << 16) | c;
+      tb.ucnt[u] = 0;
+      first[e] = 0x80000000u | (uint32_t)u;   // from now on: the expert's unique index
     }
+    U += __popc(mask);
+    __syncwarp();
   }
-  const int U = (int)(tot >> 16);
-  consumer_sync();
-  // slot -> hoff[u] + (number of earlier slots routed to the same expert)
-  for (int s = ctid; s < S; s += kConsumerThreads) {
-    const int e = tb.sel_e[s];
-    int pos = 0;
-    for (int s2 = 0; s2 < s; ++s2) pos += (tb.sel_e[s2] == e);
-    const int u = (int)tb.cnt[e];
-    tb.utok[tb.hoff[u] + pos] = (uint8_t)(s / k);
-    tb.uw[tb.hoff[u] + pos] = tb.sel_w[s];
+  // token positions within each expert, in slot order (peers = same expert)
+  for (int b = 0; b < S; b += 32) {
+    const int s = b + lane;
+    const bool v = s < S;
+    const int e = v ? tb.sel_e[s] : -1 - lane;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    int u = 0, pos = 0;
+    if (v) {
+      u = (int)(first[e] & 0x7FFFFFFFu);
+      pos = tb.ucnt[u] + __popc(peers & lt);
+    }
+    __syncwarp();
+    if (v) {
+      tb.unit_tb[s] = (uint8_t)pos;        // position of slot s within its expert
+      if ((peers & lt) == 0) tb.ucnt[u] = (uint16_t)(pos + __popc(peers));
+    }
+    __syncwarp();
   }
+  // slot offsets hoff[u] = sum of ucnt over earlier unique experts
+  int run = 0;
+  for (int b = 0; b < U; b += 32) {
+    const int u = b + lane;
+    const int c = (u < U) ? tb.ucnt[u] : 0;
+    int inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    if (u < U) tb.hoff[u] = (uint16_t)(run + inc - c);
+    run += __shfl_sync(0xffffffffu, inc, 31);
+  }
+  __syncwarp();
+  for (int s = lane; s < S; s += 32) {
+    const int u = (int)(first[tb.sel_e[s]] & 0x7FFFFFFFu);
+    const int slot = tb.hoff[u] + tb.unit_tb[s];
+    tb.utok[slot] = (uint8_t)(s / k);
+    tb.uw[slot] = tb.sel_w[s];
+  }
+  __syncwarp();
   // units (u, token batch), u-major
-  uint32_t nb = 0;
-  if (ctid < U) nb = (tb.ucnt[ctid] + kTB - 1) / kTB;
-  uint32_t ntot;
-  const uint32_t ub = block_excl_scan(nb, tb, ctid, &ntot);
-  if (ctid < U)
-    for (uint32_t b = 0; b < nb; ++b) {
-      tb.unit_u[ub + b] = (uint16_t)ctid;
-      tb.unit_tb[ub + b] = (uint8_t)b;
+  int nu = 0;
+  for (int b = 0; b < U; b += 32) {
+    const int u = b + lane;
+    const int nb = (u < U) ? (tb.ucnt[u] + kTB - 1) / kTB : 0;
+    int inc = nb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
     }
-  if (ctid == 0) {
-    tb.U = U;
-    tb.n_units = (int)ntot;
+    if (u < U)
+      for (int q = 0; q < nb; ++q) {
+        tb.unit_u[nu + inc - nb + q] = (uint16_t)u;
+        tb.unit_tb[nu + inc - nb + q] = (uint8_t)q;
+      }
+    nu += __shfl_sync(0xffffffffu, inc, 31);
   }
-  if (cta == 0) {
-    for (int s = ctid; s < S; s += kConsumerThreads) {
+  if (lane == 0) {
+    tb.U = U;
+    tb.n_units = nu;
+  }
+}
+
+// Routing for all tokens + unique-expert tables (identical in every CTA).
+__device__ __noinline__ void routing_phase(const Params& p, int write_out, Tables& tb, int ctid) {
+  const int warp = ctid >> 5, lane = ctid & 31;
+  const int E = p.E, k = p.k, S = p.N * p.k, scoring = p.scoring, norm = p.norm;
+  const float rsf = p.rsf;
+  const float* bias = p.bias;
+  for (int n = warp; n < p.N; n += kConsumerWarps) {
+    const float* lrow = p.logits + (size_t)n * E;
+    if (E <= 128) topk_token<4>(E, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
+    else if (E <= 256) topk_token<8>(E, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
+    else if (E <= 512) topk_token<16>(E, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
+    else topk_token<32>(E, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
+  }
+  consumer_sync();
+  if (warp == 0) {
+    const bool done = (S <= 32) && build_tables_small(k, S, tb, lane);
+    if (!done) build_tables(E, k, S, tb, lane);
+  }
+  if (write_out && warp == 1) {
+    for (int s = lane; s < S; s += 32) {
       if (p.topk_idx) p.topk_idx[s] = tb.sel_e[s];
       if (p.topk_w) p.topk_w[s] = tb.sel_w[s];
     }
@@ -419,10 +508,10 @@ __device__ __forceinline__ int kind_units(const Params& p, const Tables& tb) {
 template <int KIND>
 __device__ __forceinline__ void kind_range(const Params& p, const Tables& tb, int cta, int G,
                                            int& lo, int& hi) {
-  const int rpu = p.geo[KIND].rows_total / kRows;
-  const long long T = (long long)kind_units<KIND>(p, tb) * rpu;
-  lo = (int)(T * cta / G);
-  hi = (int)(T * (cta + 1) / G);
+  const uint32_t rpu = (uint32_t)(p.geo[KIND].rows_total / kRows);
+  const uint32_t T = (uint32_t)kind_units<KIND>(p, tb) * rpu;   // < 2^22: products fit 32 bits
+  lo = (int)(T * (uint32_t)cta / (uint32_t)G);
+  hi = (int)(T * (uint32_t)(cta + 1) / (uint32_t)G);
 }
 
 template <int KIND>
@@ -827,9 +916,32 @@ __device__ __noinline__ void flush_row_blocks(const Params& p, Tables& tb, int c
 
 // Reduce the 8 warps' partial sums of an RG (already in `red`) and apply the
 // epilogue of its kind.
+// Per-thread epilogue factors of an RG (thread ctid < nt*32 serves token
+// ctid/32), loaded when the RG starts so their latency hides behind the
+// stage compute: gate/up scales for AR, output weight for BR/BS.
+template <int KIND>
+__device__ __forceinline__ float2 epi_factors(const Params& p, const Tables& tb, const RG& r,
+                                              int ctid) {
+  float2 f = make_float2(1.f, 1.f);
+  if (ctid >= r.nt * 32) return f;
+  const int t = ctid >> 5;
+  const int n = rg_token<KIND>(tb, r, t);
+  if (KIND == KIND_AR) {
+    const float xs = ldexpf(1.0f, ld_cg_s32(p.xexp + n));
+    f.x = xs * (p.g2 ? __ldg(p.g2 + r.e) : 1.0f);
+    f.y = xs * (p.u2 ? __ldg(p.u2 + r.e) : 1.0f);
+  } else if (KIND == KIND_BR) {
+    f.x = ldexpf(1.0f, tb.hexp[t]) * (p.d2 ? __ldg(p.d2 + r.e) : 1.0f) *
+          tb.uw[tb.hoff[r.u] + r.tb * kTB + t];
+  } else if (KIND == KIND_BS) {
+    f.x = ld_cg_f32(p.gsig + n);
+  }
+  return f;
+}
+
 template <int KIND>
 __device__ __noinline__ void rg_epilogue(const Params& p, Tables& tb, const RG& r,
-                                         const float* red, int ctid, uint32_t b_units) {
+                                         const float* red, int ctid, uint32_t b_units, float2 ef) {
   const Geo& g = p.geo[KIND];
   if (ctid < r.nt * 32 && !aborted(tb)) {
     const int t = ctid >> 5, j = ctid & 31;
@@ -842,17 +954,11 @@ __device__ __noinline__ void rg_epilogue(const Params& p, Tables& tb, const RG& 
     const int row = r.rg * kRows + j;
     const int n = rg_token<KIND>(tb, r, t);
     if (KIND == KIND_AR) {
-      const float xs = ldexpf(1.0f, ld_cg_s32(p.xexp + n));
-      const float gg = s0 * xs * (p.g2 ? p.g2[r.e] : 1.0f);
-      const float uu = s1 * xs * (p.u2 ? p.u2[r.e] : 1.0f);
-      p.h[(size_t)(tb.hoff[r.u] + r.tb * kTB + t) * p.inter + row] = silu(gg) * uu;
+      p.h[(size_t)(tb.hoff[r.u] + r.tb * kTB + t) * p.inter + row] = silu(s0 * ef.x) * (s1 * ef.y);
     } else if (KIND == KIND_AS) {
       p.hs[(size_t)n * p.Is + row] = silu(s0) * s1;
-    } else if (KIND == KIND_BR) {
-      const float y = s0 * ldexpf(1.0f, tb.hexp[t]) * (p.d2 ? p.d2[r.e] : 1.0f);
-      red_add_f32(p.acc + (size_t)n * p.H + row, y * tb.uw[tb.hoff[r.u] + r.tb * kTB + t]);
     } else {
-      red_add_f32(p.acc + (size_t)n * p.H + row, s0 * ld_cg_f32(p.gsig + n));
+      red_add_f32(p.acc + (size_t)n * p.H + row, s0 * ef.x);
     }
   }
   consumer_sync();
@@ -930,6 +1036,7 @@ __device__ __noinline__ void consume_kind(const Params& p, Tables& tb, const Con
       }
       consumer_sync();
     }
+    const float2 ef = epi_factors<KIND>(p, tb, r, ctid);
     switch (r.nt) {
       case 1: consume_rg<FMT, NPROJ, KIND, 1>(p, tb, cx, g, ctr, warp, lane); break;
       case 2: consume_rg<FMT, NPROJ, KIND, 2>(p, tb, cx, g, ctr, warp, lane); break;
@@ -937,7 +1044,7 @@ __device__ __noinline__ void consume_kind(const Params& p, Tables& tb, const Con
       default: consume_rg<FMT, NPROJ, KIND, 4>(p, tb, cx, g, ctr, warp, lane); break;
     }
     consumer_sync();
-    rg_epilogue<KIND>(p, tb, r, cx.red, ctid, b_units);
+    rg_epilogue<KIND>(p, tb, r, cx.red, ctid, b_units, ef);
   }
   *ctr_io = ctr;
 }
@@ -1044,7 +1151,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
   }
 
   // P1: routing
-  routing_phase(p, cta, tb, ctid);
+  routing_phase(p, cta == 0, tb, ctid);
   if (p.route_only) {
     if (ctid == 0) grid_arrive(p.ctrl);   // B2 arrival, nothing waits on it
     return;
