@@ -1,0 +1,705 @@
+// Grouped MoE layer forward for many tokens (prefill-sized N) on sm_103a.
+//
+// Same mathematics as the decode kernel (forward chain of forward_k3.rs:
+// router GEMV -> top-k -> expert gate+up -> SiLU -> down -> weighted sum),
+// organised as per-expert token groups so that each routed expert's weights
+// are streamed once for all of its tokens ("grouped GEMM (more than 64
+// rows)", forward_batched.rs) and the contractions run on the tcgen05 tensor
+// cores.  Stream-ordered launches:
+//
+//   router    logits[n,e] (FP32, CUDA cores), per-token power-of-two exponent
+//             of x, warp top-k per token
+//   plan      per-expert token counts, expert-sorted positions of the
+//             (token, slot) pairs, token tiles of <= 64 positions (one CTA)
+//   gather    xg[pos] = x[token(pos)] * 2^-xexp as f16, in expert order
+//   gemm(2)   per (token tile, 128-row block): g = Dq(Wg) xg^T, u = Dq(Wu) xg^T,
+//             h = SiLU(g) * u (FP32)
+//   pack      h16[pos] = h[pos] * 2^-hexp as f16 (per-row power of two)
+//   gemm(1)   y = w(pos) * Dq(Wd) h16^T (FP32, one row per position)
+//   combine   out[n] = bf16(sum over the k slots of n of y)
+//
+// GEMM kernel (persistent, one CTA per SM, 14 warps):
+//   warp 0      TMA producer: FP4 weight boxes (64 bytes x 128 rows, 64-byte
+//               swizzle), activation boxes (64 f16 x 64 rows, 128-byte
+//               swizzle), the unit's block scales (1D bulk copy)
+//   warp 1      TMEM allocation; lane 0 issues tcgen05.mma kind::f16
+//               (A from tensor memory, B from shared memory, FP32 accumulators
+//               in tensor memory, M = 128 weight rows, N = tokens rounded to 16)
+//   warps 2-9   dequantisation: thread = weight row; E2M1 -> f16 with
+//               cvt.rn.f16x2.e2m1x2, times the block scale (E4M3 as f16:
+//               exact; E8M0 as a power of two relative to the row's largest
+//               scale), written to tensor memory with tcgen05.st
+//   warps 10-13 epilogue: tcgen05.ld of the accumulators, scale factors,
+//               SiLU(g)*u or the routing weight, FP32 stores
+//
+// The f16 A and B operands are exact images of the FP4 weights and of the
+// BF16 activations (up to f16 subnormal flushing of values more than ~2^28
+// below the row maximum), and f16 x f16 products are exact in FP32, so the
+// only rounding besides FP32 accumulation is the f16 image of h.
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "moe_internal.h"
+#include "ptx.cuh"
+#include "routing.cuh"
+#include "tc.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRtTok = 8;          // tokens per router CTA
+constexpr int kGThreads = 448;     // GEMM kernel: 14 warps
+constexpr int kTileRows = 128;     // weight rows per unit (MMA M)
+constexpr int kKChunk = 128;       // K elements per stage
+constexpr int kABox = 8192;        // 128 rows x 64 bytes of FP4
+constexpr int kBBox = 8192;        // 64 positions x 128 bytes of f16
+constexpr int kNA = 4;             // A slots (64 K each) in tensor memory
+constexpr uint32_t kTmemCols = 512;
+
+// power-of-two exponent e with max * 2^-e in [2^14, 2^15) (0 for max == 0)
+__device__ __forceinline__ int f16_exponent(float mx) {
+  if (!(mx > 0.f) || isinf(mx)) return 0;
+  int ex;
+  frexpf(mx, &ex);   // mx = f * 2^ex, f in [0.5, 1)
+  return ex - 15;
+}
+
+__device__ __forceinline__ uint32_t f16x2_pack(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ router
+__global__ void __launch_bounds__(256) grouped_router_kernel(const GroupedParams p) {
+  extern __shared__ __align__(1024) uint8_t rsmem[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(rsmem);                       // [8][H]
+  float* ls = reinterpret_cast<float*>(rsmem + (size_t)kRtTok * p.H * 2);  // [8][E]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n0 = blockIdx.x * kRtTok;
+  const int nt = min(kRtTok, p.N - n0);
+  const int H = p.H, E = p.E;
+  for (int i = tid * 8; i < nt * H; i += 256 * 8)
+    *reinterpret_cast<uint4*>(xs + i) = ld_nc_u4(p.x + (size_t)n0 * H + i);
+  __syncthreads();
+  if (warp < nt) {   // per-token exponent of the f16 image of x
+    float mx = 0.f;
+    for (int h = lane; h < H; h += 32) mx = fmaxf(mx, fabsf(__uint_as_float((uint32_t)xs[warp * H + h] << 16)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) p.xexp[n0 + warp] = f16_exponent(mx);
+  }
+  for (int e = warp; e < E; e += 8) {
+    float acc[kRtTok];
+#pragma unroll
+    for (int t = 0; t < kRtTok; ++t) acc[t] = 0.f;
+    const uint16_t* wr = p.router + (size_t)e * H;
+    for (int h = lane * 8; h < H; h += 256) {
+      const uint4 wv = ld_nc_u4(wr + h);
+      const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int t = 0; t < kRtTok; ++t) {
+        if (t < nt) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(xs + t * H + h);
+          const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w};
+          float a = acc[t];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            a = fmaf(__uint_as_float(wa[q] << 16), __uint_as_float(xa[q] << 16), a);
+            a = fmaf(__uint_as_float(wa[q] & 0xFFFF0000u), __uint_as_float(xa[q] & 0xFFFF0000u), a);
+          }
+          acc[t] = a;
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kRtTok; ++t) {
+      float v = acc[t];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0 && t < nt) {
+        ls[t * E + e] = v;
+        p.logits[(size_t)(n0 + t) * E + e] = v;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp < nt) {
+    const int n = n0 + warp;
+    const float* lrow = ls + warp * E;
+    int se = 0;
+    float sw = 0.f;
+#define MOE_TOPK_CASE(PER)                                                              \
+  {                                                                                     \
+    float lg[PER];                                                                      \
+    _Pragma("unroll") for (int i = 0; i < PER; ++i) {                                   \
+      const int e = lane + 32 * i;                                                      \
+      lg[i] = (e < E) ? lrow[e] : -INFINITY;                                            \
+    }                                                                                   \
+    topk_warp<PER>(E, p.k, p.scoring, p.norm, p.rsf, p.bias, lg, lane, &se, &sw);      \
+  }
+    if (E <= 128) MOE_TOPK_CASE(4)
+    else if (E <= 256) MOE_TOPK_CASE(8)
+    else if (E <= 512) MOE_TOPK_CASE(16)
+    else MOE_TOPK_CASE(32)
+#undef MOE_TOPK_CASE
+    if (lane < p.k) {
+      p.sel_e[n * p.k + lane] = se;
+      p.sel_w[n * p.k + lane] = sw;
+      if (p.topk_idx) p.topk_idx[n * p.k + lane] = se;
+      if (p.topk_w) p.topk_w[n * p.k + lane] = sw;
+    }
+  }
+}
+
+// -------------------------------------------------------------------- plan
+// Block-wide exclusive scan of one value per thread (1024 threads).
+__device__ int scan1024(int v, int* sh, int* total) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += t;
+  }
+  if (lane == 31) sh[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int w = sh[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += t;
+    }
+    sh[32 + lane] = wi - w;
+    if (lane == 31) sh[64] = wi;
+  }
+  __syncthreads();
+  const int r = sh[32 + warp] + inc - v;
+  *total = sh[64];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(1024) grouped_plan_kernel(const GroupedParams p) {
+  __shared__ int cnt[kMaxE];
+  __shared__ int cursor[kMaxE];
+  __shared__ int sh[96];
+  const int tid = threadIdx.x;
+  const int S = p.N * p.k;
+  for (int e = tid; e < p.E; e += 1024) cnt[e] = 0;
+  __syncthreads();
+  for (int s = tid; s < S; s += 1024) atomicAdd(&cnt[p.sel_e[s]], 1);
+  __syncthreads();
+  const int c = (tid < p.E) ? cnt[tid] : 0;
+  const int nt = (c + kGTileTok - 1) / kGTileTok;
+  int tot_pos = 0, tot_tiles = 0;
+  const int off = scan1024(c, sh, &tot_pos);
+  const int toff = scan1024(nt, sh, &tot_tiles);
+  if (tid < p.E) {
+    cursor[tid] = off;
+    for (int q = 0; q < nt; ++q) {
+      int* t = p.tiles + 3 * (toff + q);
+      t[0] = tid;
+      t[1] = off + q * kGTileTok;
+      t[2] = min(kGTileTok, c - q * kGTileTok);
+    }
+  }
+  if (tid == 0) p.ntiles[0] = tot_tiles;
+  __syncthreads();
+  for (int s = tid; s < S; s += 1024) {
+    const int pos = atomicAdd(&cursor[p.sel_e[s]], 1);
+    p.pos_of[s] = pos;
+    p.tok_of[pos] = s / p.k;
+    p.w_of[pos] = p.sel_w[s];
+  }
+}
+
+// ------------------------------------------------------------------ gather
+__global__ void __launch_bounds__(128) grouped_gather_kernel(const GroupedParams p) {
+  const int pos = blockIdx.x;
+  const int n = p.tok_of[pos];
+  const int ex = p.xexp[n];
+  if (threadIdx.x == 0) p.bexp[pos] = ex;
+  const uint16_t* src = p.x + (size_t)n * p.H;
+  uint16_t* dst = p.xg + (size_t)pos * p.H;
+  for (int h = threadIdx.x * 8; h < p.H; h += 128 * 8) {
+    const uint4 v = ld_nc_u4(src + h);
+    const uint32_t a[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      o[q] = f16x2_pack(ldexpf(__uint_as_float(a[q] << 16), -ex),
+                        ldexpf(__uint_as_float(a[q] & 0xFFFF0000u), -ex));
+    *reinterpret_cast<uint4*>(dst + h) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// -------------------------------------------------------------------- pack
+__global__ void __launch_bounds__(256) grouped_pack_kernel(const GroupedParams p) {
+  __shared__ float red[8];
+  const int pos = blockIdx.x, tid = threadIdx.x;
+  const float* src = p.hbuf + (size_t)pos * p.inter;
+  float mx = 0.f;
+  for (int i = tid * 4; i < p.inter; i += 256 * 4) {
+    const float4 v = *reinterpret_cast<const float4*>(src + i);
+    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((tid & 31) == 0) red[tid >> 5] = mx;
+  __syncthreads();
+  mx = red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) mx = fmaxf(mx, red[w]);
+  const int ex = f16_exponent(mx);
+  if (tid == 0) p.hexp[pos] = ex;
+  uint16_t* dst = p.h16 + (size_t)pos * p.inter;
+  for (int i = tid * 4; i < p.inter; i += 256 * 4) {
+    const float4 v = *reinterpret_cast<const float4*>(src + i);
+    *reinterpret_cast<uint2*>(dst + i) =
+        make_uint2(f16x2_pack(ldexpf(v.x, -ex), ldexpf(v.y, -ex)),
+                   f16x2_pack(ldexpf(v.z, -ex), ldexpf(v.w, -ex)));
+  }
+}
+
+// ----------------------------------------------------------------- combine
+__global__ void __launch_bounds__(256) grouped_combine_kernel(const GroupedParams p) {
+  const int n = blockIdx.x;
+  int pos[kMaxTopK];
+  for (int j = 0; j < p.k; ++j) pos[j] = p.pos_of[n * p.k + j];
+  for (int r = threadIdx.x; r < p.H; r += 256) {
+    float s = 0.f;
+    for (int j = 0; j < p.k; ++j) s += p.hbuf[(size_t)pos[j] * p.H + r];
+    const __nv_bfloat16 b = __float2bfloat16_rn(s);
+    p.out[(size_t)n * p.H + r] = *reinterpret_cast<const uint16_t*>(&b);
+  }
+}
+
+// -------------------------------------------------------------------- GEMM
+namespace {
+
+struct GBars {
+  uint64_t* full;     // [8]   stage ring: TMA -> dequant + MMA
+  uint64_t* empty;    // [8]   8 dequant warps + MMA commit -> producer
+  uint64_t* afull;    // [4]   dequant -> MMA (tensor-memory A slot written)
+  uint64_t* aempty;   // [4]   MMA commit -> dequant
+  uint64_t* dfull;    // [2]   MMA commit -> epilogue (accumulator ready)
+  uint64_t* dempty;   // [2]   epilogue -> MMA
+  uint64_t* scfull;   // [2]   unit scales landed
+  uint64_t* scempty;  // [2]   dequant + epilogue done with the unit's scales
+  uint64_t* fin;      // final MMA commit
+  uint32_t* tslot;
+  int* abort;
+};
+
+struct GUnit {
+  int e, p0, nt, rt;
+};
+
+__device__ __forceinline__ GUnit gunit(const GemmParams& p, int u, int RT) {
+  const int t = u / RT;
+  GUnit r;
+  r.e = p.tiles[3 * t];
+  r.p0 = p.tiles[3 * t + 1];
+  r.nt = p.tiles[3 * t + 2];
+  r.rt = u - t * RT;
+  return r;
+}
+
+__device__ __forceinline__ bool gwait(const GemmParams& p, const GBars& b, uint64_t* bar,
+                                      uint32_t parity) {
+  if (*reinterpret_cast<volatile int*>(b.abort)) return false;
+  if (mbar_wait_bounded(bar, parity, p.timeout_ns)) return true;
+  atomicExch(b.abort, 1);
+  atomicOr(p.err, kErrTimeoutStage);
+  return false;
+}
+// all lanes wait; the warp agrees on the outcome
+__device__ __forceinline__ bool gwait_warp(const GemmParams& p, const GBars& b, uint64_t* bar,
+                                           uint32_t parity) {
+  const bool ok = gwait(p, b, bar, parity);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ uint8_t* gstage(uint8_t* smem, const GemmParams& p, int s) {
+  return smem + (size_t)s * p.stage_bytes;
+}
+__device__ __forceinline__ uint8_t* gscbuf(uint8_t* smem, const GemmParams& p, int ub) {
+  return smem + p.off_sc + (size_t)ub * p.sc_bytes;
+}
+// tensor-memory columns: accumulators [2 buffers][2 proj][64], A slots [4][2 proj][32]
+__device__ __forceinline__ int dcol(int b, int pj) { return b * 128 + pj * 64; }
+__device__ __forceinline__ int acol(int a, int pj) { return 256 + a * 64 + pj * 32; }
+
+// largest non-NaN E8M0 code of a row's scales (0 if none)
+__device__ __forceinline__ int row_max_e8m0(const uint8_t* s, int n) {
+  int mx = 0;
+  for (int i = 0; i < n; ++i) {
+    const int v = s[i];
+    if (v != 0xFF) mx = max(mx, v);
+  }
+  return mx;
+}
+
+template <int NPROJ>
+__device__ void g_producer(const GemmParams& p, uint8_t* smem, const GBars& b, int RT,
+                           int nunits) {
+  for (int i = 0; i < NPROJ; ++i) prefetch_tensormap(&p.tmA[i]);
+  prefetch_tensormap(&p.tmB);
+  const int nch = (p.K + kKChunk - 1) / kKChunk;
+  int sctr = 0, it = 0, nsc = 0;   // stages and scale copies issued
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x, ++it) {
+    const GUnit un = gunit(p, u, RT);
+    const int rv = min(kTileRows, p.rows - un.rt * kTileRows);
+    const int ub = it % p.nscbuf;
+    const uint32_t ur = (uint32_t)(it / p.nscbuf);
+    if (!gwait(p, b, b.scempty + ub, (ur & 1u) ^ 1u)) { ok = false; break; }
+    mbar_arrive_expect_tx(b.scfull + ub, (uint32_t)(NPROJ * rv * p.sr));
+    const size_t srow = ((size_t)un.e * p.rows + (size_t)un.rt * kTileRows) * p.sr;
+    for (int pj = 0; pj < NPROJ; ++pj)
+      bulk_g2s(gscbuf(smem, p, ub) + pj * kTileRows * p.sr, p.sc[pj] + srow,
+               (uint32_t)(rv * p.sr), b.scfull + ub);
+    ++nsc;
+    const int arow = un.e * p.rows + un.rt * kTileRows;
+    for (int c = 0; c < nch; ++c, ++sctr) {
+      const int s = sctr % p.nstages;
+      const uint32_t r = (uint32_t)(sctr / p.nstages);
+      if (!gwait(p, b, b.empty + s, (r & 1u) ^ 1u)) { ok = false; break; }
+      const int nsub = min(2, (p.K - c * kKChunk + 63) / 64);
+      mbar_arrive_expect_tx(b.full + s, (uint32_t)(NPROJ * kABox + nsub * kBBox));
+      uint8_t* st = gstage(smem, p, s);
+      for (int pj = 0; pj < NPROJ; ++pj)
+        tma_load_2d(st + pj * kABox, &p.tmA[pj], c * (kKChunk / 2), arow, b.full + s);
+      for (int j = 0; j < nsub; ++j)
+        tma_load_2d(st + NPROJ * kABox + j * kBBox, &p.tmB, (c * kKChunk + j * 64) * 2, un.p0,
+                    b.full + s);
+    }
+  }
+  if (!ok) {   // drain copies still in flight into our buffers
+    const int first = sctr > p.nstages ? sctr - p.nstages : 0;
+    for (int i = first; i < sctr; ++i)
+      mbar_wait_bounded(b.full + (i % p.nstages), (uint32_t)(i / p.nstages) & 1u, p.timeout_ns);
+    const int f2 = nsc > p.nscbuf ? nsc - p.nscbuf : 0;
+    for (int i = f2; i < nsc; ++i)
+      mbar_wait_bounded(b.scfull + (i % p.nscbuf), (uint32_t)(i / p.nscbuf) & 1u, p.timeout_ns);
+  }
+}
+
+template <int NPROJ, int FMT>
+__device__ void g_dequant(const GemmParams& p, uint8_t* smem, const GBars& b, uint32_t tbase,
+                          int RT, int nunits) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = (warp - 2) >> 2;   // 0: warps 2-5, 1: warps 6-9
+  const int q = warp & 3;            // tensor-memory lane quarter
+  const int m = q * 32 + lane;       // weight row within the tile
+  const int pj = (NPROJ == 2) ? grp : 0;
+  const int pc0 = (NPROJ == 2) ? 0 : grp, pcs = (NPROJ == 2) ? 1 : 2;   // pieces handled
+  const int nch = (p.K + kKChunk - 1) / kKChunk;
+  int sctr = 0, actr = 0, it = 0;
+  for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++it) {
+    const GUnit un = gunit(p, u, RT);
+    const int rv = min(kTileRows, p.rows - un.rt * kTileRows);
+    const bool live = m < rv;   // warp-uniform: rv is a multiple of 32
+    const int ub = it % p.nscbuf;
+    if (!gwait_warp(p, b, b.scfull + ub, (uint32_t)(it / p.nscbuf) & 1u)) return;
+    const uint8_t* srow = gscbuf(smem, p, ub) + pj * kTileRows * p.sr + m * p.sr;
+    int mref = 0;
+    if (FMT == FMT_MXFP4 && live) mref = row_max_e8m0(srow, p.sr) - 13;
+    for (int c = 0; c < nch; ++c, ++sctr) {
+      const int s = sctr % p.nstages;
+      if (!gwait_warp(p, b, b.full + s, (uint32_t)(sctr / p.nstages) & 1u)) return;
+      const uint8_t* at = gstage(smem, p, s) + pj * kABox + m * 64;
+      const int nsub = min(2, (p.K - c * kKChunk + 63) / 64);
+      for (int j = 0; j < nsub; ++j, ++actr) {
+        const int a = actr % kNA;
+        if (!gwait_warp(p, b, b.aempty + a, ((uint32_t)(actr / kNA) & 1u) ^ 1u)) return;
+        tc_fence_after();
+        for (int pc = pc0; pc < 2; pc += pcs) {
+          const int k0 = c * kKChunk + j * 64 + pc * 32;
+          if (!live || k0 >= p.K) continue;
+          const int pi = j * 2 + pc;   // 16-byte piece of the 64-byte row
+          const uint4 w = *reinterpret_cast<const uint4*>(at + ((pi ^ ((m >> 1) & 3)) << 4));
+          uint32_t v[16];
+          uint32_t o[4];
+          e2m1x8_to_f16x2x4(w.x, o);
+          v[0] = o[0]; v[1] = o[1]; v[2] = o[2]; v[3] = o[3];
+          e2m1x8_to_f16x2x4(w.y, o);
+          v[4] = o[0]; v[5] = o[1]; v[6] = o[2]; v[7] = o[3];
+          e2m1x8_to_f16x2x4(w.z, o);
+          v[8] = o[0]; v[9] = o[1]; v[10] = o[2]; v[11] = o[3];
+          e2m1x8_to_f16x2x4(w.w, o);
+          v[12] = o[0]; v[13] = o[1]; v[14] = o[2]; v[15] = o[3];
+          uint32_t s0, s1;
+          if (FMT == FMT_NVFP4) {
+            const uint32_t sv = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(srow + k0 / 16));
+            s0 = __byte_perm(sv, 0, 0x1010);
+            s1 = __byte_perm(sv, 0, 0x3232);
+          } else {
+            // 2^j2 as f16, j2 = code - (row max code - 13) <= 13
+            const int code = srow[k0 / 32];
+            const int j2 = code - mref;
+            uint32_t bits;
+            if (code == 0xFF) bits = 0x7E00u;                      // NaN scale
+            else if (j2 >= -14) bits = (uint32_t)(j2 + 15) << 10;  // normal
+            else if (j2 >= -24) bits = 1u << (j2 + 24);            // subnormal
+            else bits = 0u;                                        // below f16: flushed
+            s0 = s1 = bits | (bits << 16);
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = hmul2(v[i], s0);
+#pragma unroll
+          for (int i = 8; i < 16; ++i) v[i] = hmul2(v[i], s1);
+          tmem_st16(tmem_addr(tbase, q * 32, acol(a, pj) + pc * 16), v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b.afull + a);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b.empty + s);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(b.scempty + ub);
+  }
+}
+
+template <int NPROJ>
+__device__ void g_mma(const GemmParams& p, uint8_t* smem, const GBars& b, uint32_t tbase, int RT,
+                      int nunits) {
+  const int nch = (p.K + kKChunk - 1) / kKChunk;
+  int sctr = 0, actr = 0, it = 0;
+  for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++it) {
+    const GUnit un = gunit(p, u, RT);
+    const int db = it & 1;
+    if (!gwait(p, b, b.dempty + db, ((uint32_t)(it >> 1) & 1u) ^ 1u)) break;
+    tc_fence_after();
+    const int nmma = (un.nt + 15) & ~15;
+    const uint32_t idesc = idesc_f16_f32(kTileRows, nmma);
+    bool first = true;
+    bool ok = true;
+    for (int c = 0; c < nch && ok; ++c, ++sctr) {
+      const int s = sctr % p.nstages;
+      if (!gwait(p, b, b.full + s, (uint32_t)(sctr / p.nstages) & 1u)) { ok = false; break; }
+      const uint32_t bst = smem_u32(gstage(smem, p, s) + NPROJ * kABox);
+      const int nsub = min(2, (p.K - c * kKChunk + 63) / 64);
+      for (int j = 0; j < nsub; ++j, ++actr) {
+        const int a = actr % kNA;
+        if (!gwait(p, b, b.afull + a, (uint32_t)(actr / kNA) & 1u)) { ok = false; break; }
+        tc_fence_after();
+        for (int ks = 0; ks < 4; ++ks) {
+          if (c * kKChunk + j * 64 + ks * 16 >= p.K) break;
+          const uint64_t bd = sdesc_sw128(bst + j * kBBox + ks * 32);
+          for (int pj = 0; pj < NPROJ; ++pj)
+            mma_f16_ts(tmem_addr(tbase, 0, dcol(db, pj)), tmem_addr(tbase, 0, acol(a, pj) + ks * 8),
+                       bd, idesc, first ? 0u : 1u);
+          first = false;
+        }
+        mma_commit(b.aempty + a);
+      }
+      if (ok) mma_commit(b.empty + s);
+    }
+    if (!ok) break;
+    mma_commit(b.dfull + db);
+  }
+  mma_commit(b.fin);   // completes once every MMA issued above has finished
+  mbar_wait_bounded(b.fin, 0, p.timeout_ns);
+}
+
+template <int NPROJ, int FMT>
+__device__ void g_epilogue(const GemmParams& p, uint8_t* smem, const GBars& b, uint32_t tbase,
+                           int RT, int nunits) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3;
+  const int m = q * 32 + lane;
+  int it = 0;
+  for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++it) {
+    const GUnit un = gunit(p, u, RT);
+    const int rv = min(kTileRows, p.rows - un.rt * kTileRows);
+    const bool live = m < rv;
+    const int db = it & 1;
+    const int ub = it % p.nscbuf;
+    if (!gwait_warp(p, b, b.dfull + db, (uint32_t)(it >> 1) & 1u)) return;
+    tc_fence_after();
+    if (!gwait_warp(p, b, b.scfull + ub, (uint32_t)(it / p.nscbuf) & 1u)) return;
+    // per-row factors: scale2 (NVFP4) or 2^(row reference exponent - 127) (MXFP4)
+    float fs[2] = {1.f, 1.f};
+    int fe[2] = {0, 0};
+#pragma unroll
+    for (int pj = 0; pj < NPROJ; ++pj) {
+      if (FMT == FMT_NVFP4) {
+        fs[pj] = p.s2[pj] ? __ldg(p.s2[pj] + un.e) : 1.0f;
+      } else if (live) {
+        const uint8_t* srow = gscbuf(smem, p, ub) + pj * kTileRows * p.sr + m * p.sr;
+        fe[pj] = row_max_e8m0(srow, p.sr) - 13 - 127;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(b.scempty + ub);
+    const int nmma = (un.nt + 15) & ~15;
+    const int r = un.rt * kTileRows + m;
+    for (int cb = 0; cb < nmma; cb += 16) {
+      uint32_t v0[16], v1[16];
+      tmem_ld16(tmem_addr(tbase, q * 32, dcol(db, 0) + cb), v0);
+      if (NPROJ == 2) tmem_ld16(tmem_addr(tbase, q * 32, dcol(db, 1) + cb), v1);
+      tmem_wait_ld();
+      if (live) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int t = cb + i;
+          if (t >= un.nt) continue;
+          const int pos = un.p0 + t;
+          const int be = __ldg(p.bexp + pos);
+          float* dst = p.out + (size_t)pos * p.rows + r;
+          if (NPROJ == 2) {
+            const float g = ldexpf(__uint_as_float(v0[i]) * fs[0], fe[0] + be);
+            const float uu = ldexpf(__uint_as_float(v1[i]) * fs[1], fe[1] + be);
+            *dst = g / (1.0f + expf(-g)) * uu;
+          } else {
+            const float y = ldexpf(__uint_as_float(v0[i]) * fs[0], fe[0] + be);
+            *dst = y * __ldg(p.wpos + pos);
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(b.dempty + db);
+  }
+}
+
+}  // namespace
+
+template <int NPROJ, int FMT>
+__global__ void __launch_bounds__(kGThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
+  GBars b;
+  b.full = bars;
+  b.empty = bars + 8;
+  b.afull = bars + 16;
+  b.aempty = bars + 20;
+  b.dfull = bars + 24;
+  b.dempty = bars + 26;
+  b.scfull = bars + 28;
+  b.scempty = bars + 30;
+  b.fin = bars + 32;
+  b.tslot = reinterpret_cast<uint32_t*>(bars + 33);
+  b.abort = reinterpret_cast<int*>(bars + 34);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) {
+    for (int s = 0; s < p.nstages; ++s) {
+      mbar_init(b.full + s, 1);
+      mbar_init(b.empty + s, 8 + 1);
+    }
+    for (int a = 0; a < kNA; ++a) {
+      mbar_init(b.afull + a, 8);
+      mbar_init(b.aempty + a, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b.dfull + i, 1);
+      mbar_init(b.dempty + i, 4);
+      mbar_init(b.scfull + i, 1);
+      mbar_init(b.scempty + i, 8 + 4);
+    }
+    mbar_init(b.fin, 1);
+    *b.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(b.tslot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *b.tslot;
+  const int RT = (p.rows + kTileRows - 1) / kTileRows;
+  const int nunits = p.ntiles[0] * RT;
+
+  if (warp == 0) {
+    if ((tid & 31) == 0) g_producer<NPROJ>(p, smem, b, RT, nunits);
+  } else if (warp == 1) {
+    if ((tid & 31) == 0) g_mma<NPROJ>(p, smem, b, tbase, RT, nunits);
+  } else if (warp < 10) {
+    g_dequant<NPROJ, FMT>(p, smem, b, tbase, RT, nunits);
+  } else {
+    g_epilogue<NPROJ, FMT>(p, smem, b, tbase, RT, nunits);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+// -------------------------------------------------------------------- host
+int grouped_plan_gemm(GemmParams& g, int nproj, int smem_budget) {
+  g.stage_bytes = nproj * kABox + 2 * kBBox;
+  const int scb = ((nproj * kTileRows * g.sr) + 1023) / 1024 * 1024;
+  g.sc_bytes = scb;
+  const int bar_bytes = 1024;
+  for (int nsc = 2; nsc >= 1; --nsc) {
+    const int room = smem_budget - nsc * scb - bar_bytes;
+    int ns = room / g.stage_bytes;
+    ns = std::min(ns, 8);
+    if (ns >= 2) {
+      g.nscbuf = nsc;
+      g.nstages = ns;
+      g.off_sc = ns * g.stage_bytes;
+      g.off_bar = g.off_sc + nsc * scb;
+      return g.off_bar + bar_bytes;
+    }
+  }
+  return 0;
+}
+
+cudaError_t grouped_set_smem(int smem_bytes) {
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<2, FMT_NVFP4>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<2, FMT_MXFP4>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<1, FMT_NVFP4>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<1, FMT_MXFP4>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(grouped_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes);
+  return e;
+}
+
+cudaError_t launch_grouped(const GroupedParams& gp, GemmParams gu, GemmParams gd, int grid,
+                           int smem_gu, int smem_gd, cudaStream_t st) {
+  const int S = gp.N * gp.k;
+  const int rsmem = kRtTok * gp.H * 2 + kRtTok * gp.E * 4;
+  grouped_router_kernel<<<(gp.N + kRtTok - 1) / kRtTok, 256, rsmem, st>>>(gp);
+  if (gp.route_only) return cudaGetLastError();
+  grouped_plan_kernel<<<1, 1024, 0, st>>>(gp);
+  grouped_gather_kernel<<<S, 128, 0, st>>>(gp);
+  // gate/up: smem + 1024 for the manual 1024-byte alignment
+  if (gp.fmt == FMT_NVFP4)
+    grouped_gemm_kernel<2, FMT_NVFP4><<<grid, kGThreads, smem_gu + 1024, st>>>(gu);
+  else
+    grouped_gemm_kernel<2, FMT_MXFP4><<<grid, kGThreads, smem_gu + 1024, st>>>(gu);
+  grouped_pack_kernel<<<S, 256, 0, st>>>(gp);
+  if (gp.fmt == FMT_NVFP4)
+    grouped_gemm_kernel<1, FMT_NVFP4><<<grid, kGThreads, smem_gd + 1024, st>>>(gd);
+  else
+    grouped_gemm_kernel<1, FMT_MXFP4><<<grid, kGThreads, smem_gd + 1024, st>>>(gd);
+  grouped_combine_kernel<<<gp.N, 256, 0, st>>>(gp);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -51,6 +51,55 @@ WsLayout ws_layout(const moe_layer_desc_t& d, int32_t N) {
   return L;
 }
 
+// Workspace of the grouped (many-token) path.  The control block sits at the
+// same offset as in the decode layout so moe_get_error reads both.
+struct GWsLayout {
+  size_t ctrl, logits, xexp, sel_e, sel_w, tiles, ntiles, pos_of, tok_of, w_of, bexp, hexp, xg,
+      hbuf, h16, total;
+};
+
+GWsLayout gws_layout(const moe_layer_desc_t& d, int32_t N) {
+  GWsLayout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, kAlign);
+    return o;
+  };
+  const size_t S = (size_t)N * d.top_k;
+  const size_t T = S / moe::kGTileTok + std::min((size_t)d.E, S) + 1;   // token tiles, bound
+  L.ctrl = take(256);
+  L.logits = take((size_t)N * d.E * 4);
+  L.xexp = take((size_t)N * 4);
+  L.sel_e = take(S * 4);
+  L.sel_w = take(S * 4);
+  L.tiles = take(T * 3 * 4);
+  L.ntiles = take(4);
+  L.pos_of = take(S * 4);
+  L.tok_of = take(S * 4);
+  L.w_of = take(S * 4);
+  L.bexp = take(S * 4);
+  L.hexp = take(S * 4);
+  L.xg = take(S * d.H * 2);
+  L.hbuf = take(S * std::max(d.inter, d.H) * 4);
+  L.h16 = take(S * d.inter * 2);
+  L.total = off;
+  return L;
+}
+
+bool grouped_path(const moe_layer_desc_t& d, int32_t N) {
+  return (long long)N * d.top_k > moe::kMaxSlots;
+}
+
+// Workspace bytes for any N <= max_tokens (decode layout up to the slot
+// limit, grouped layout beyond it).
+size_t ws_total(const moe_layer_desc_t& d, int32_t max_tokens) {
+  const int32_t ndec = std::min(max_tokens, (int32_t)(moe::kMaxSlots / d.top_k));
+  size_t t = ndec >= 1 ? ws_layout(d, ndec).total : 0;
+  if (grouped_path(d, max_tokens)) t = std::max(t, gws_layout(d, max_tokens).total);
+  return t;
+}
+
 moe_status_t check_desc(const moe_layer_desc_t* d) {
   if (!d) return MOE_ERR_INVALID_ARG;
   if (d->H <= 0 || d->inter <= 0 || d->E <= 0 || d->top_k <= 0) return MOE_ERR_INVALID_ARG;
@@ -99,6 +148,7 @@ moe_status_t device_info(int* budget, int* grid) {
     if (di.budget <= 0) return MOE_ERR_CUDA;
     di.grid = moe::decode_grid(dev, di.budget);
     if (di.grid <= 0) return MOE_ERR_CUDA;
+    if (moe::grouped_set_smem(di.budget + 1024) != cudaSuccess) return MOE_ERR_CUDA;
     di.ready = true;
   }
   *budget = di.budget;
@@ -117,10 +167,11 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 struct TmKey {
   const void* ptr;
   uint64_t inner, rows;
-  uint32_t box;
+  uint32_t box, box_rows;
   int swz;
   bool operator==(const TmKey& o) const {
-    return ptr == o.ptr && inner == o.inner && rows == o.rows && box == o.box && swz == o.swz;
+    return ptr == o.ptr && inner == o.inner && rows == o.rows && box == o.box &&
+           box_rows == o.box_rows && swz == o.swz;
   }
 };
 struct TmEntry {
@@ -133,8 +184,8 @@ TmEntry g_tm_cache[kTmCache];
 int g_tm_next = 0;
 
 bool encode_2d(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box,
-               int swz) {   // swz: 0 none, 64 or 128 (bytes)
-  const TmKey key{ptr, inner, rows, box, swz};
+               int swz, uint32_t box_rows = moe::kRows) {   // swz: 0 none, 64 or 128 (bytes)
+  const TmKey key{ptr, inner, rows, box, box_rows, swz};
   std::lock_guard<std::mutex> lk(g_mu);
   for (auto& e : g_tm_cache)
     if (e.used && e.key == key) {
@@ -152,7 +203,7 @@ bool encode_2d(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t rows,
   }
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {inner};
-  cuuint32_t boxd[2] = {box, (cuuint32_t)moe::kRows};
+  cuuint32_t boxd[2] = {box, box_rows};
   cuuint32_t es[2] = {1, 1};
   CUtensorMap m;
   if (g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, boxd,
@@ -190,6 +241,106 @@ bool encode_scales(moe::Params& p, int slot, const void* ptr, const moe::Geo& g,
   return true;
 }
 
+// Grouped path: router/top-k, plan, gather, gate/up GEMM, pack, down GEMM,
+// combine (grouped_kernel.cu).  Arguments are already checked.
+moe_status_t run_grouped(const moe_layer_desc_t* d, const moe_weights_t* w, const void* x,
+                         int32_t N, void* out, int32_t* topk_idx, float* topk_w, void* ws,
+                         size_t ws_bytes, void* stream, int route_only) {
+  if (d->shared_inter > 0) return MOE_ERR_UNSUPPORTED;   // shared expert: decode sizes only
+  const GWsLayout L = gws_layout(*d, N);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  int budget = 0, grid = 0;
+  moe_status_t st = device_info(&budget, &grid);
+  if (st != MOE_OK) return st;
+  if ((size_t)8 * d->H * 2 + (size_t)8 * d->E * 4 > (size_t)budget) return MOE_ERR_UNSUPPORTED;
+
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  moe::GroupedParams gp;
+  memset(&gp, 0, sizeof(gp));
+  gp.N = N;
+  gp.H = d->H;
+  gp.inter = d->inter;
+  gp.E = d->E;
+  gp.k = d->top_k;
+  gp.scoring = d->scoring;
+  gp.norm = d->norm_topk_prob ? 1 : 0;
+  gp.rsf = d->routed_scaling_factor;
+  gp.fmt = d->wfmt;
+  gp.route_only = route_only;
+  gp.x = static_cast<const uint16_t*>(x);
+  gp.router = static_cast<const uint16_t*>(w->router);
+  gp.bias = d->scoring == MOE_SCORE_SIGMOID_BIAS ? w->bias : nullptr;
+  gp.topk_idx = topk_idx;
+  gp.topk_w = topk_w;
+  gp.out = static_cast<uint16_t*>(out);
+  gp.logits = reinterpret_cast<float*>(b + L.logits);
+  gp.xexp = reinterpret_cast<int*>(b + L.xexp);
+  gp.sel_e = reinterpret_cast<int*>(b + L.sel_e);
+  gp.sel_w = reinterpret_cast<float*>(b + L.sel_w);
+  gp.tiles = reinterpret_cast<int*>(b + L.tiles);
+  gp.ntiles = reinterpret_cast<int*>(b + L.ntiles);
+  gp.pos_of = reinterpret_cast<int*>(b + L.pos_of);
+  gp.tok_of = reinterpret_cast<int*>(b + L.tok_of);
+  gp.w_of = reinterpret_cast<float*>(b + L.w_of);
+  gp.bexp = reinterpret_cast<int*>(b + L.bexp);
+  gp.hexp = reinterpret_cast<int*>(b + L.hexp);
+  gp.xg = reinterpret_cast<uint16_t*>(b + L.xg);
+  gp.hbuf = reinterpret_cast<float*>(b + L.hbuf);
+  gp.h16 = reinterpret_cast<uint16_t*>(b + L.h16);
+
+  const int gs = d->wfmt == MOE_W_NVFP4 ? 16 : 32;
+  const uint64_t S = (uint64_t)N * d->top_k;
+  moe::GemmParams gu, gd;
+  memset(&gu, 0, sizeof(gu));
+  memset(&gd, 0, sizeof(gd));
+  uint32_t* err = &reinterpret_cast<moe::Ctrl*>(b + L.ctrl)->error;
+  int smem_gu = 0, smem_gd = 0;
+  if (!route_only) {
+    gu.sc[0] = w->gate_s;
+    gu.sc[1] = w->up_s;
+    gu.s2[0] = w->gate_s2;
+    gu.s2[1] = w->up_s2;
+    gu.tiles = gp.tiles;
+    gu.ntiles = gp.ntiles;
+    gu.bexp = gp.bexp;
+    gu.wpos = nullptr;
+    gu.out = gp.hbuf;
+    gu.err = err;
+    gu.rows = d->inter;
+    gu.K = d->H;
+    gu.sr = d->H / gs;
+    gu.timeout_ns = g_timeout_ns;
+    gd = gu;
+    gd.sc[0] = w->down_s;
+    gd.sc[1] = nullptr;
+    gd.s2[0] = w->down_s2;
+    gd.s2[1] = nullptr;
+    gd.bexp = gp.hexp;
+    gd.wpos = gp.w_of;
+    gd.rows = d->H;
+    gd.K = d->inter;
+    gd.sr = d->inter / gs;
+    smem_gu = moe::grouped_plan_gemm(gu, 2, budget);
+    smem_gd = moe::grouped_plan_gemm(gd, 1, budget);
+    if (!smem_gu || !smem_gd) return MOE_ERR_UNSUPPORTED;
+    // at least half of the SM's shared memory, so one CTA (and one TMEM
+    // allocation of all 512 columns) per SM
+    smem_gu = std::max(smem_gu, budget / 2 + 1024);
+    smem_gd = std::max(smem_gd, budget / 2 + 1024);
+    const uint64_t ER = (uint64_t)d->E;
+    bool ok = encode_2d(&gu.tmA[0], w->gate_q, (uint64_t)d->H / 2, ER * d->inter, 64, 64, 128) &&
+              encode_2d(&gu.tmA[1], w->up_q, (uint64_t)d->H / 2, ER * d->inter, 64, 64, 128) &&
+              encode_2d(&gu.tmB, gp.xg, (uint64_t)d->H * 2, S, 128, 128, 64) &&
+              encode_2d(&gd.tmA[0], w->down_q, (uint64_t)d->inter / 2, ER * d->H, 64, 64, 128) &&
+              encode_2d(&gd.tmB, gp.h16, (uint64_t)d->inter * 2, S, 128, 128, 64);
+    if (!ok) return MOE_ERR_CUDA;
+  }
+  if (moe::launch_grouped(gp, gu, gd, grid, smem_gu, smem_gd,
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* x, int32_t N,
                  void* out, int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
                  void* stream, int route_only) {
@@ -198,10 +349,11 @@ moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* 
   st = check_weights(d, w);
   if (st != MOE_OK) return st;
   if (N < 1) return MOE_ERR_INVALID_ARG;
-  if ((long long)N * d->top_k > moe::kMaxSlots) return MOE_ERR_UNSUPPORTED;
   if (!x || !aligned16(x) || !ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
   if (!route_only && (!out || !aligned16(out))) return MOE_ERR_INVALID_ARG;
   if (route_only && (!topk_idx || !topk_w)) return MOE_ERR_INVALID_ARG;
+  if (grouped_path(*d, N))
+    return run_grouped(d, w, x, N, out, topk_idx, topk_w, ws, ws_bytes, stream, route_only);
   const WsLayout L = ws_layout(*d, N);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
 
@@ -302,7 +454,7 @@ extern "C" {
 
 size_t moe_workspace_size(const moe_layer_desc_t* desc, int32_t max_tokens) {
   if (check_desc(desc) != MOE_OK || max_tokens < 1) return 0;
-  return ws_layout(*desc, max_tokens).total;
+  return ws_total(*desc, max_tokens);
 }
 
 size_t moe_host_staging_size(const moe_layer_desc_t* desc, int32_t max_tokens) {
@@ -391,9 +543,8 @@ moe_status_t moe_forward_noalloc(const moe_layer_desc_t* desc, const moe_weights
   st = check_weights(desc, weights);
   if (st != MOE_OK) return st;
   if (N < 1) return MOE_ERR_INVALID_ARG;
-  if ((long long)N * desc->top_k > moe::kMaxSlots) return MOE_ERR_UNSUPPORTED;
   if (!x || !aligned16(x) || !out || !aligned16(out)) return MOE_ERR_INVALID_ARG;
-  if (ws_layout(*desc, N).total > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_total(*desc, N) > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
   void* ws = nullptr;
   st = noalloc_scratch(&ws);
   if (st != MOE_OK) return st;

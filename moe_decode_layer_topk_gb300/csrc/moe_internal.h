@@ -97,6 +97,62 @@ struct Params {
   unsigned long long timeout_ns;
 };
 
+// ------------------------------------------------------------ grouped path
+// Many-token forward (N * top_k beyond kMaxSlots): per-expert token groups on
+// the tensor cores (grouped_kernel.cu).
+constexpr int kGTileTok = 64;   // positions per token tile (MMA N <= 64)
+
+struct GroupedParams {
+  int N, H, inter, E, k, scoring, norm;
+  float rsf;
+  int fmt;
+  int route_only;
+  const uint16_t* x;        // [N, H] bf16
+  const uint16_t* router;   // [E, H] bf16
+  const float* bias;        // [E] or null
+  int32_t* topk_idx;        // [N, k] or null
+  float* topk_w;
+  uint16_t* out;            // [N, H] bf16
+  // workspace
+  float* logits;            // [N, E]
+  int* xexp;                // [N]   x = xg * 2^xexp
+  int* sel_e;               // [S]   per (token, slot)
+  float* sel_w;
+  int* tiles;               // [T][3] expert, first position, positions
+  int* ntiles;              // [1]
+  int* pos_of;              // [S]   expert-sorted position of slot s
+  int* tok_of;              // [S]   token of position
+  float* w_of;              // [S]   routing weight of position
+  int* bexp;                // [S]   exponent of xg rows
+  int* hexp;                // [S]   exponent of h16 rows
+  uint16_t* xg;             // [S, H] f16
+  float* hbuf;              // [S, max(inter, H)] FP32: h, later y
+  uint16_t* h16;            // [S, inter] f16
+};
+
+struct GemmParams {
+  CUtensorMap tmA[2];       // FP4 rows [E*rows, K/2] bytes: box 64 B x 128 rows, 64-byte swizzle
+  CUtensorMap tmB;          // f16 rows [S, 2K] bytes: box 128 B x 64 rows, 128-byte swizzle
+  const uint8_t* sc[2];     // block scales [E, rows, K/gs]
+  const float* s2[2];       // per-expert scale2 (NVFP4) or null
+  const int* tiles;
+  const int* ntiles;
+  const int* bexp;          // per position: exponent of the B row
+  const float* wpos;        // per position routing weight (one-projection GEMM)
+  float* out;               // [S, rows] FP32
+  uint32_t* err;            // workspace error word
+  int rows, K, sr;
+  int nstages, nscbuf, stage_bytes, sc_bytes, off_sc, off_bar;
+  unsigned long long timeout_ns;
+};
+
+// Ring and scale-buffer layout of a grouped GEMM; returns its shared-memory
+// bytes (0 if it does not fit in `smem_budget`).
+int grouped_plan_gemm(GemmParams& g, int nproj, int smem_budget);
+cudaError_t grouped_set_smem(int smem_bytes);
+cudaError_t launch_grouped(const GroupedParams& gp, GemmParams gu, GemmParams gd, int grid,
+                           int smem_gu, int smem_gd, cudaStream_t st);
+
 // Fills p.geo / ring / smem layout from the layer shape; returns false if
 // the shape does not fit the kernel's shared-memory budget.
 bool plan_decode(Params& p, int smem_budget);

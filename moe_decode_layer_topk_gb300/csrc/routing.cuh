@@ -1,0 +1,90 @@
+// Warp-level top-k routing of one token, shared by the decode and grouped
+// kernels.  Scoring follows the gating step of the forward chain: softmax
+// (selection by logit, weights softmax over all E, optionally renormalised
+// over the selected) or sigmoid + correction bias (selection by
+// sigmoid(l) + bias, weights sigmoid(l) without the bias, optional
+// renormalisation, then times the routed scaling factor).  Ties go to the
+// lower expert index.
+#pragma once
+#include <math.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Selection key, order preserving as unsigned: larger key = larger score.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// lg[i] = logit of expert lane + 32*i (-inf where that index is >= E).  The k
+// selections are k rounds of a warp arg-max; lane j < k returns selection j
+// (expert and weight) in *e_out / *w_out, in selection order.
+template <int PER>
+__device__ __forceinline__ void topk_warp(int E, int k, int scoring, int norm, float rsf,
+                                          const float* bias, const float (&lg)[PER], int lane,
+                                          int* e_out, float* w_out) {
+  uint32_t key[PER];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = 0u;
+    if (e < E) {
+      const float l = lg[i];
+      mx = fmaxf(mx, l);
+      key[i] = order_key(scoring == 1 ? 1.0f / (1.0f + expf(-l)) + bias[e] : l);
+    }
+  }
+  uint32_t bk = 0u, be = 0xFFFFFFFFu;   // lane-local best, lowest index among equals
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    if (key[i] > bk) { bk = key[i]; be = lane + 32 * i; }
+  uint32_t mine = 0u;                   // lane j: expert of selection j
+  for (int j = 0; j < k; ++j) {
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+    uint32_t we = __reduce_min_sync(0xffffffffu, (bk == m) ? be : 0xFFFFFFFFu);
+    if (we >= (uint32_t)E) we = 0;      // only if fewer than k valid keys (k <= E is checked)
+    if (lane == j) mine = we;
+    if ((we & 31u) == (uint32_t)lane) {
+#pragma unroll
+      for (int i = 0; i < PER; ++i)
+        if (lane + 32 * i == (int)we) key[i] = 0u;
+      bk = 0u;
+      be = 0xFFFFFFFFu;
+#pragma unroll
+      for (int i = 0; i < PER; ++i)
+        if (key[i] > bk) { bk = key[i]; be = lane + 32 * i; }
+    }
+  }
+  float den = 0.f;
+  if (scoring == 0) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      if (lane + 32 * i < E) den += expf(lg[i] - mx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  }
+  // logit of this lane's selection, from the lane that holds it
+  float l = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const float v = __shfl_sync(0xffffffffu, lg[i], mine & 31u);
+    if ((int)(mine >> 5) == i) l = v;
+  }
+  float w = 0.f;
+  if (lane < k) w = (scoring == 0) ? expf(l - mx) / den : 1.0f / (1.0f + expf(-l));
+  float wsum = w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+  if (lane < k) {
+    if (norm) w = w / wsum;
+    if (scoring == 1) w *= rsf;
+    *e_out = (int)mine;
+    *w_out = w;
+  }
+}
+
+}  // namespace moe

@@ -86,7 +86,11 @@ def test_argument_refusals_happen_before_any_cuda_call(lib):
     """Every case below is refused by the host checks (no GPU needed)."""
     d, w = _desc(), _fake_weights()
     assert _forward(lib, d, w, N=0) == _lib.MOE_ERR_INVALID_ARG
-    assert _forward(lib, d, w, N=300) == _lib.MOE_ERR_UNSUPPORTED      # N*k > 256
+    # N*k > 256 takes the grouped path: its own workspace check, and no shared expert yet
+    assert _forward(lib, d, w, N=300, ws_bytes=1 << 20) == _lib.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert _lib.moe_workspace_size(d, 300) > _lib.moe_workspace_size(d, 128)
+    assert _forward(lib, _desc(shared_inter=64), _fake_weights(shared=True), N=300) == \
+        _lib.MOE_ERR_UNSUPPORTED
     assert _forward(lib, d, w, x=(1 << 24) + 8) == _lib.MOE_ERR_INVALID_ARG
     assert _forward(lib, d, w, out=None) == _lib.MOE_ERR_INVALID_ARG
     assert _forward(lib, d, w, ws_bytes=16) == _lib.MOE_ERR_WORKSPACE_TOO_SMALL
