@@ -7,8 +7,8 @@
 // rows)", forward_batched.rs) and the contractions run on the tcgen05 tensor
 // cores.  Stream-ordered launches:
 //
-//   router    logits[n,e] (FP32, CUDA cores), per-token power-of-two exponent
-//             of x, warp top-k per token
+//   router    logits[n,e] (FP32, CUDA cores)
+//   top-k     warp top-k per token; per-token power-of-two exponent of x
 //   plan      per-expert token counts, expert-sorted positions of the
 //             (token, slot) pairs, token tiles of <= 64 positions (one CTA)
 //   gather    xg[pos] = x[token(pos)] * 2^-xexp as f16, in expert order
@@ -18,18 +18,18 @@
 //   gemm(1)   y = w(pos) * Dq(Wd) h16^T (FP32, one row per position)
 //   combine   out[n] = bf16(sum over the k slots of n of y)
 //
-// GEMM kernel (persistent, one CTA per SM, 14 warps):
+// GEMM kernel (persistent, one CTA per SM, 23 warps):
 //   warp 0      TMA producer: FP4 weight boxes (64 bytes x 128 rows, 64-byte
 //               swizzle), activation boxes (64 f16 x 64 rows, 128-byte
 //               swizzle), the unit's block scales (1D bulk copy)
-//   warp 1      TMEM allocation; lane 0 issues tcgen05.mma kind::f16
+//   warps 1, 22 TMEM allocation (warp 1); lane 0 of each issues tcgen05.mma kind::f16
 //               (A from tensor memory, B from shared memory, FP32 accumulators
 //               in tensor memory, M = 128 weight rows, N = tokens rounded to 16)
-//   warps 2-9   dequantisation: thread = weight row; E2M1 -> f16 with
+//   warps 2-17  dequantisation: thread = weight row; E2M1 -> f16 with
 //               cvt.rn.f16x2.e2m1x2, times the block scale (E4M3 as f16:
 //               exact; E8M0 as a power of two relative to the row's largest
 //               scale), written to tensor memory with tcgen05.st
-//   warps 10-13 epilogue: tcgen05.ld of the accumulators, scale factors,
+//   warps 18-21 epilogue: tcgen05.ld of the accumulators, scale factors,
 //               SiLU(g)*u or the routing weight, FP32 stores
 //
 // The f16 A and B operands are exact images of the FP4 weights and of the
@@ -50,12 +50,12 @@ namespace moe {
 namespace {
 
 constexpr int kRtTok = 8;          // tokens per router CTA
-constexpr int kGThreads = 448;     // GEMM kernel: 14 warps
+constexpr int kGThreads = 736;     // GEMM kernel: 23 warps
 constexpr int kTileRows = 128;     // weight rows per unit (MMA M)
 constexpr int kKChunk = 128;       // K elements per stage
 constexpr int kABox = 8192;        // 128 rows x 64 bytes of FP4
 constexpr int kBBox = 8192;        // 64 positions x 128 bytes of f16
-constexpr int kNA = 4;             // A slots (64 K each) in tensor memory
+constexpr int kNA = 4;             // A slots in tensor memory
 constexpr uint32_t kTmemCols = 512;
 
 // power-of-two exponent e with max * 2^-e in [2^14, 2^15) (0 for max == 0)
@@ -74,10 +74,15 @@ __device__ __forceinline__ uint32_t f16x2_pack(float a, float b) {
 }  // namespace
 
 // ------------------------------------------------------------------ router
+// Grid (token groups of 8) x (expert groups of 16): each CTA holds its 8 x
+// rows in shared memory; each warp computes 2 experts for the 8 tokens, with
+// the router row's loads issued 8 vectors at a time (latency, not bandwidth,
+// bounds this kernel).
+constexpr int kRtExp = 16;   // experts per router CTA
+
 __global__ void __launch_bounds__(256) grouped_router_kernel(const GroupedParams p) {
   extern __shared__ __align__(1024) uint8_t rsmem[];
-  uint16_t* xs = reinterpret_cast<uint16_t*>(rsmem);                       // [8][H]
-  float* ls = reinterpret_cast<float*>(rsmem + (size_t)kRtTok * p.H * 2);  // [8][E]
+  uint16_t* xs = reinterpret_cast<uint16_t*>(rsmem);   // [8][H]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n0 = blockIdx.x * kRtTok;
   const int nt = min(kRtTok, p.N - n0);
@@ -85,33 +90,37 @@ __global__ void __launch_bounds__(256) grouped_router_kernel(const GroupedParams
   for (int i = tid * 8; i < nt * H; i += 256 * 8)
     *reinterpret_cast<uint4*>(xs + i) = ld_nc_u4(p.x + (size_t)n0 * H + i);
   __syncthreads();
-  if (warp < nt) {   // per-token exponent of the f16 image of x
-    float mx = 0.f;
-    for (int h = lane; h < H; h += 32) mx = fmaxf(mx, fabsf(__uint_as_float((uint32_t)xs[warp * H + h] << 16)));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) p.xexp[n0 + warp] = f16_exponent(mx);
-  }
-  for (int e = warp; e < E; e += 8) {
+  for (int e = blockIdx.y * kRtExp + warp; e < min(E, (int)(blockIdx.y + 1) * kRtExp); e += 8) {
     float acc[kRtTok];
 #pragma unroll
     for (int t = 0; t < kRtTok; ++t) acc[t] = 0.f;
     const uint16_t* wr = p.router + (size_t)e * H;
-    for (int h = lane * 8; h < H; h += 256) {
-      const uint4 wv = ld_nc_u4(wr + h);
-      const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w};
+    for (int hb = 0; hb < H; hb += 8 * 256) {
+      uint4 wv[8];
 #pragma unroll
-      for (int t = 0; t < kRtTok; ++t) {
-        if (t < nt) {
-          const uint4 xv = *reinterpret_cast<const uint4*>(xs + t * H + h);
-          const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w};
-          float a = acc[t];
+      for (int i = 0; i < 8; ++i) {
+        const int h = hb + (i * 32 + lane) * 8;
+        wv[i] = (h < H) ? ld_nc_u4(wr + h) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            a = fmaf(__uint_as_float(wa[q] << 16), __uint_as_float(xa[q] << 16), a);
-            a = fmaf(__uint_as_float(wa[q] & 0xFFFF0000u), __uint_as_float(xa[q] & 0xFFFF0000u), a);
+      for (int i = 0; i < 8; ++i) {
+        const int h = hb + (i * 32 + lane) * 8;
+        if (h >= H) continue;
+        const uint32_t wa[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+#pragma unroll
+        for (int t = 0; t < kRtTok; ++t) {
+          if (t < nt) {
+            const uint4 xv = *reinterpret_cast<const uint4*>(xs + t * H + h);
+            const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w};
+            float a2 = acc[t];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              a2 = fmaf(__uint_as_float(wa[q] << 16), __uint_as_float(xa[q] << 16), a2);
+              a2 = fmaf(__uint_as_float(wa[q] & 0xFFFF0000u),
+                        __uint_as_float(xa[q] & 0xFFFF0000u), a2);
+            }
+            acc[t] = a2;
           }
-          acc[t] = a;
         }
       }
     }
@@ -120,38 +129,53 @@ __global__ void __launch_bounds__(256) grouped_router_kernel(const GroupedParams
       float v = acc[t];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0 && t < nt) {
-        ls[t * E + e] = v;
-        p.logits[(size_t)(n0 + t) * E + e] = v;
-      }
+      if (lane == 0 && t < nt) p.logits[(size_t)(n0 + t) * E + e] = v;
     }
   }
-  __syncthreads();
-  if (warp < nt) {
-    const int n = n0 + warp;
-    const float* lrow = ls + warp * E;
-    int se = 0;
-    float sw = 0.f;
-#define MOE_TOPK_CASE(PER)                                                              \
-  {                                                                                     \
-    float lg[PER];                                                                      \
-    _Pragma("unroll") for (int i = 0; i < PER; ++i) {                                   \
-      const int e = lane + 32 * i;                                                      \
-      lg[i] = (e < E) ? lrow[e] : -INFINITY;                                            \
-    }                                                                                   \
-    topk_warp<PER>(E, p.k, p.scoring, p.norm, p.rsf, p.bias, lg, lane, &se, &sw);      \
+}
+
+// One warp per token: top-k over the FP32 logits, and the power-of-two
+// exponent of the token's f16 image.
+__global__ void __launch_bounds__(256) grouped_topk_kernel(const GroupedParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.x * 8 + warp;
+  if (n >= p.N) return;
+  const int E = p.E;
+  float mx = 0.f;
+  const uint16_t* xr = p.x + (size_t)n * p.H;
+  for (int h = lane * 8; h < p.H; h += 256) {
+    const uint4 v = ld_nc_u4(xr + h);
+    const uint32_t a[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(a[q] << 16)),
+                           fabsf(__uint_as_float(a[q] & 0xFFFF0000u))));
   }
-    if (E <= 128) MOE_TOPK_CASE(4)
-    else if (E <= 256) MOE_TOPK_CASE(8)
-    else if (E <= 512) MOE_TOPK_CASE(16)
-    else MOE_TOPK_CASE(32)
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) p.xexp[n] = f16_exponent(mx);
+  const float* lrow = p.logits + (size_t)n * E;
+  int se = 0;
+  float sw = 0.f;
+#define MOE_TOPK_CASE(PER)                                                         \
+  {                                                                                \
+    float lg[PER];                                                                 \
+    _Pragma("unroll") for (int i = 0; i < PER; ++i) {                              \
+      const int e = lane + 32 * i;                                                 \
+      lg[i] = (e < E) ? lrow[e] : -INFINITY;                                       \
+    }                                                                              \
+    topk_warp<PER>(E, p.k, p.scoring, p.norm, p.rsf, p.bias, lg, lane, &se, &sw); \
+  }
+  if (E <= 128) MOE_TOPK_CASE(4)
+  else if (E <= 256) MOE_TOPK_CASE(8)
+  else if (E <= 512) MOE_TOPK_CASE(16)
+  else MOE_TOPK_CASE(32)
 #undef MOE_TOPK_CASE
-    if (lane < p.k) {
-      p.sel_e[n * p.k + lane] = se;
-      p.sel_w[n * p.k + lane] = sw;
-      if (p.topk_idx) p.topk_idx[n * p.k + lane] = se;
-      if (p.topk_w) p.topk_w[n * p.k + lane] = sw;
-    }
+  if (lane < p.k) {
+    p.sel_e[n * p.k + lane] = se;
+    p.sel_w[n * p.k + lane] = sw;
+    if (p.topk_idx) p.topk_idx[n * p.k + lane] = se;
+    if (p.topk_w) p.topk_w[n * p.k + lane] = sw;
   }
 }
 
@@ -283,16 +307,27 @@ __global__ void __launch_bounds__(256) grouped_combine_kernel(const GroupedParam
 // -------------------------------------------------------------------- GEMM
 namespace {
 
+// Roles: warp 0 producer, warp 1 TMEM owner + MMA issuer 0, warps 2-17
+// dequantisation (one 32-element piece of one projection per A slot each),
+// warps 18-21 epilogue, warp 22 MMA issuer 1.  A single thread issues a
+// small-N tcgen05.mma only every ~45 cycles whatever N (<= 64), while the
+// tensor core can take more: two issuers, each with its own accumulator
+// (gate / up, or the even / odd A slots of the one-projection GEMM), double
+// the MMA rate.
+constexpr int kDeqWarps = 16;
+constexpr int kEpiWarps = 4;
+constexpr int kDeq0 = 2, kEpi0 = kDeq0 + kDeqWarps, kMma1 = kEpi0 + kEpiWarps;
+
 struct GBars {
   uint64_t* full;     // [8]   stage ring: TMA -> dequant + MMA
-  uint64_t* empty;    // [8]   8 dequant warps + MMA commit -> producer
+  uint64_t* empty;    // [8]   16 dequant warps + MMA commit -> producer
   uint64_t* afull;    // [4]   dequant -> MMA (tensor-memory A slot written)
-  uint64_t* aempty;   // [4]   MMA commit -> dequant
-  uint64_t* dfull;    // [2]   MMA commit -> epilogue (accumulator ready)
+  uint64_t* aempty;   // [4]   MMA commits of the issuers that read the slot -> dequant
+  uint64_t* dfull;    // [2]   both issuers' commits -> epilogue (accumulators ready)
   uint64_t* dempty;   // [2]   epilogue -> MMA
   uint64_t* scfull;   // [2]   unit scales landed
   uint64_t* scempty;  // [2]   dequant + epilogue done with the unit's scales
-  uint64_t* fin;      // final MMA commit
+  uint64_t* fin;      // [2]   final MMA commit of each issuer
   uint32_t* tslot;
   int* abort;
 };
@@ -304,15 +339,16 @@ struct GUnit {
 __device__ __forceinline__ GUnit gunit(const GemmParams& p, int u, int RT) {
   const int t = u / RT;
   GUnit r;
-  r.e = p.tiles[3 * t];
-  r.p0 = p.tiles[3 * t + 1];
-  r.nt = p.tiles[3 * t + 2];
+  r.e = __ldg(p.tiles + 3 * t);
+  r.p0 = __ldg(p.tiles + 3 * t + 1);
+  r.nt = __ldg(p.tiles + 3 * t + 2);
   r.rt = u - t * RT;
   return r;
 }
 
 __device__ __forceinline__ bool gwait(const GemmParams& p, const GBars& b, uint64_t* bar,
                                       uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
   if (*reinterpret_cast<volatile int*>(b.abort)) return false;
   if (mbar_wait_bounded(bar, parity, p.timeout_ns)) return true;
   atomicExch(b.abort, 1);
@@ -332,9 +368,15 @@ __device__ __forceinline__ uint8_t* gstage(uint8_t* smem, const GemmParams& p, i
 __device__ __forceinline__ uint8_t* gscbuf(uint8_t* smem, const GemmParams& p, int ub) {
   return smem + p.off_sc + (size_t)ub * p.sc_bytes;
 }
-// tensor-memory columns: accumulators [2 buffers][2 proj][64], A slots [4][2 proj][32]
+// Tensor-memory columns: accumulators [2 buffers][2 proj][64 tokens], then
+// 4 A slots of 64 columns: [2 proj][32 columns = 64 K] (two projections) or
+// [64 columns = 128 K] (one projection).
 __device__ __forceinline__ int dcol(int b, int pj) { return b * 128 + pj * 64; }
 __device__ __forceinline__ int acol(int a, int pj) { return 256 + a * 64 + pj * 32; }
+// K elements of one A slot: 16 MMA K-steps' worth of dequantisation work
+// (16 warps x one 32-element piece) whatever the projection count.
+template <int NPROJ>
+__host__ __device__ constexpr int slot_k() { return 128 / NPROJ; }
 
 // largest non-NaN E8M0 code of a row's scales (0 if none)
 __device__ __forceinline__ int row_max_e8m0(const uint8_t* s, int n) {
@@ -371,12 +413,12 @@ __device__ void g_producer(const GemmParams& p, uint8_t* smem, const GBars& b, i
       const int s = sctr % p.nstages;
       const uint32_t r = (uint32_t)(sctr / p.nstages);
       if (!gwait(p, b, b.empty + s, (r & 1u) ^ 1u)) { ok = false; break; }
-      const int nsub = min(2, (p.K - c * kKChunk + 63) / 64);
-      mbar_arrive_expect_tx(b.full + s, (uint32_t)(NPROJ * kABox + nsub * kBBox));
+      const int nb = min(2, (p.K - c * kKChunk + 63) / 64);
+      mbar_arrive_expect_tx(b.full + s, (uint32_t)(NPROJ * kABox + nb * kBBox));
       uint8_t* st = gstage(smem, p, s);
       for (int pj = 0; pj < NPROJ; ++pj)
         tma_load_2d(st + pj * kABox, &p.tmA[pj], c * (kKChunk / 2), arow, b.full + s);
-      for (int j = 0; j < nsub; ++j)
+      for (int j = 0; j < nb; ++j)
         tma_load_2d(st + NPROJ * kABox + j * kBBox, &p.tmB, (c * kKChunk + j * 64) * 2, un.p0,
                     b.full + s);
     }
@@ -391,15 +433,18 @@ __device__ void g_producer(const GemmParams& p, uint8_t* smem, const GBars& b, i
   }
 }
 
+// One dequantisation warp: rows q*32 .. q*32+31 of the tile (its tensor-memory
+// lane quarter), one projection, one 32-element piece of every A slot.
 template <int NPROJ, int FMT>
 __device__ void g_dequant(const GemmParams& p, uint8_t* smem, const GBars& b, uint32_t tbase,
                           int RT, int nunits) {
+  constexpr int SK = slot_k<NPROJ>();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = (warp - 2) >> 2;   // 0: warps 2-5, 1: warps 6-9
-  const int q = warp & 3;            // tensor-memory lane quarter
-  const int m = q * 32 + lane;       // weight row within the tile
-  const int pj = (NPROJ == 2) ? grp : 0;
-  const int pc0 = (NPROJ == 2) ? 0 : grp, pcs = (NPROJ == 2) ? 1 : 2;   // pieces handled
+  const int role = (warp - kDeq0) >> 2;   // 0..3
+  const int q = warp & 3;                 // tensor-memory lane quarter
+  const int m = q * 32 + lane;            // weight row within the tile
+  const int pj = (NPROJ == 2) ? (role >> 1) : 0;
+  const int pc = (NPROJ == 2) ? (role & 1) : role;   // piece within the slot
   const int nch = (p.K + kKChunk - 1) / kKChunk;
   int sctr = 0, actr = 0, it = 0;
   for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++it) {
@@ -415,17 +460,16 @@ __device__ void g_dequant(const GemmParams& p, uint8_t* smem, const GBars& b, ui
       const int s = sctr % p.nstages;
       if (!gwait_warp(p, b, b.full + s, (uint32_t)(sctr / p.nstages) & 1u)) return;
       const uint8_t* at = gstage(smem, p, s) + pj * kABox + m * 64;
-      const int nsub = min(2, (p.K - c * kKChunk + 63) / 64);
-      for (int j = 0; j < nsub; ++j, ++actr) {
+      const int nslot = min(NPROJ, (p.K - c * kKChunk + SK - 1) / SK);
+      for (int j = 0; j < nslot; ++j, ++actr) {
         const int a = actr % kNA;
-        if (!gwait_warp(p, b, b.aempty + a, ((uint32_t)(actr / kNA) & 1u) ^ 1u)) return;
-        tc_fence_after();
-        for (int pc = pc0; pc < 2; pc += pcs) {
-          const int k0 = c * kKChunk + j * 64 + pc * 32;
-          if (!live || k0 >= p.K) continue;
-          const int pi = j * 2 + pc;   // 16-byte piece of the 64-byte row
+        const int pi = j * (SK / 32) + pc;   // 16-byte piece of the 64-byte row
+        const int k0 = c * kKChunk + pi * 32;
+        const bool work = live && k0 < p.K;
+        // load and convert before waiting for the slot
+        uint32_t v[16];
+        if (work) {
           const uint4 w = *reinterpret_cast<const uint4*>(at + ((pi ^ ((m >> 1) & 3)) << 4));
-          uint32_t v[16];
           uint32_t o[4];
           e2m1x8_to_f16x2x4(w.x, o);
           v[0] = o[0]; v[1] = o[1]; v[2] = o[2]; v[3] = o[3];
@@ -437,7 +481,8 @@ __device__ void g_dequant(const GemmParams& p, uint8_t* smem, const GBars& b, ui
           v[12] = o[0]; v[13] = o[1]; v[14] = o[2]; v[15] = o[3];
           uint32_t s0, s1;
           if (FMT == FMT_NVFP4) {
-            const uint32_t sv = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(srow + k0 / 16));
+            const uint32_t sv =
+                e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(srow + k0 / 16));
             s0 = __byte_perm(sv, 0, 0x1010);
             s1 = __byte_perm(sv, 0, 0x3232);
           } else {
@@ -455,9 +500,13 @@ __device__ void g_dequant(const GemmParams& p, uint8_t* smem, const GBars& b, ui
           for (int i = 0; i < 8; ++i) v[i] = hmul2(v[i], s0);
 #pragma unroll
           for (int i = 8; i < 16; ++i) v[i] = hmul2(v[i], s1);
-          tmem_st16(tmem_addr(tbase, q * 32, acol(a, pj) + pc * 16), v);
         }
-        tmem_wait_st();
+        if (!gwait_warp(p, b, b.aempty + a, ((uint32_t)(actr / kNA) & 1u) ^ 1u)) return;
+        tc_fence_after();
+        if (work) {
+          tmem_st16(tmem_addr(tbase, q * 32, acol(a, pj) + pc * 16), v);
+          tmem_wait_st();
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(b.afull + a);
@@ -470,9 +519,15 @@ __device__ void g_dequant(const GemmParams& p, uint8_t* smem, const GBars& b, ui
   }
 }
 
+// MMA issuer `me` (0 or 1).  Two projections: issuer = projection, every A
+// slot.  One projection: issuer = parity of the A slot, own accumulator; the
+// epilogue adds the two.  Full slots are issued as straight-line code (a
+// branch between MMAs slows the issue).
 template <int NPROJ>
 __device__ void g_mma(const GemmParams& p, uint8_t* smem, const GBars& b, uint32_t tbase, int RT,
-                      int nunits) {
+                      int nunits, int me) {
+  constexpr int SK = slot_k<NPROJ>();
+  constexpr int KS = SK / 16;   // MMA K-steps per slot
   const int nch = (p.K + kKChunk - 1) / kKChunk;
   int sctr = 0, actr = 0, it = 0;
   for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++it) {
@@ -480,26 +535,42 @@ __device__ void g_mma(const GemmParams& p, uint8_t* smem, const GBars& b, uint32
     const int db = it & 1;
     if (!gwait(p, b, b.dempty + db, ((uint32_t)(it >> 1) & 1u) ^ 1u)) break;
     tc_fence_after();
-    const int nmma = (un.nt + 15) & ~15;
-    const uint32_t idesc = idesc_f16_f32(kTileRows, nmma);
-    bool first = true;
+    const uint32_t idesc = idesc_f16_f32(kTileRows, (un.nt + 15) & ~15);
+    const uint32_t d = tmem_addr(tbase, 0, dcol(db, me));
+    uint32_t accum = 0u;
     bool ok = true;
     for (int c = 0; c < nch && ok; ++c, ++sctr) {
       const int s = sctr % p.nstages;
+      const int kleft = p.K - c * kKChunk;
+      const int nslot = min(NPROJ, (kleft + SK - 1) / SK);
+      // one projection: a stage is one slot, used by one issuer
+      const bool mine = (NPROJ == 2) || ((actr & 1) == me);
+      if (!mine) {
+        actr += nslot;
+        continue;
+      }
       if (!gwait(p, b, b.full + s, (uint32_t)(sctr / p.nstages) & 1u)) { ok = false; break; }
-      const uint32_t bst = smem_u32(gstage(smem, p, s) + NPROJ * kABox);
-      const int nsub = min(2, (p.K - c * kKChunk + 63) / 64);
-      for (int j = 0; j < nsub; ++j, ++actr) {
+      const uint64_t bdesc = sdesc_sw128(smem_u32(gstage(smem, p, s) + NPROJ * kABox));
+      for (int j = 0; j < nslot; ++j, ++actr) {
         const int a = actr % kNA;
         if (!gwait(p, b, b.afull + a, (uint32_t)(actr / kNA) & 1u)) { ok = false; break; }
         tc_fence_after();
-        for (int ks = 0; ks < 4; ++ks) {
-          if (c * kKChunk + j * 64 + ks * 16 >= p.K) break;
-          const uint64_t bd = sdesc_sw128(bst + j * kBBox + ks * 32);
-          for (int pj = 0; pj < NPROJ; ++pj)
-            mma_f16_ts(tmem_addr(tbase, 0, dcol(db, pj)), tmem_addr(tbase, 0, acol(a, pj) + ks * 8),
-                       bd, idesc, first ? 0u : 1u);
-          first = false;
+        const uint32_t at = tmem_addr(tbase, 0, acol(a, NPROJ == 2 ? me : 0));
+        // B: box kk/64 of the stage, 32 bytes per K-step inside the 128-byte swizzled row
+        const uint64_t bd = bdesc + (uint64_t)((j * SK / 64) * (kBBox >> 4));
+        if (kleft - j * SK >= SK) {
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            mma_f16_ts(d, at + ks * 8, bd + (uint64_t)((ks >> 2) * (kBBox >> 4) + (ks & 3) * 2),
+                       idesc, accum);
+            accum = 1u;
+          }
+        } else {
+          for (int ks = 0; ks * 16 < kleft - j * SK; ++ks) {
+            mma_f16_ts(d, at + ks * 8, bd + (uint64_t)((ks >> 2) * (kBBox >> 4) + (ks & 3) * 2),
+                       idesc, accum);
+            accum = 1u;
+          }
         }
         mma_commit(b.aempty + a);
       }
@@ -508,8 +579,8 @@ __device__ void g_mma(const GemmParams& p, uint8_t* smem, const GBars& b, uint32
     if (!ok) break;
     mma_commit(b.dfull + db);
   }
-  mma_commit(b.fin);   // completes once every MMA issued above has finished
-  mbar_wait_bounded(b.fin, 0, p.timeout_ns);
+  mma_commit(b.fin + me);   // completes once every MMA issued above has finished
+  mbar_wait_bounded(b.fin + me, 0, p.timeout_ns);
 }
 
 template <int NPROJ, int FMT>
@@ -525,45 +596,56 @@ __device__ void g_epilogue(const GemmParams& p, uint8_t* smem, const GBars& b, u
     const bool live = m < rv;
     const int db = it & 1;
     const int ub = it % p.nscbuf;
-    if (!gwait_warp(p, b, b.dfull + db, (uint32_t)(it >> 1) & 1u)) return;
-    tc_fence_after();
+    // per-token factors, token t held by lane t % 32 (t < 64): 2^bexp (and weight)
+    float tf0 = 0.f, tf1 = 0.f;
+    if (lane < un.nt) {
+      tf0 = ldexpf(1.0f, __ldg(p.bexp + un.p0 + lane));
+      if (NPROJ == 1) tf0 *= __ldg(p.wpos + un.p0 + lane);
+    }
+    if (lane + 32 < un.nt) {
+      tf1 = ldexpf(1.0f, __ldg(p.bexp + un.p0 + 32 + lane));
+      if (NPROJ == 1) tf1 *= __ldg(p.wpos + un.p0 + 32 + lane);
+    }
     if (!gwait_warp(p, b, b.scfull + ub, (uint32_t)(it / p.nscbuf) & 1u)) return;
     // per-row factors: scale2 (NVFP4) or 2^(row reference exponent - 127) (MXFP4)
-    float fs[2] = {1.f, 1.f};
-    int fe[2] = {0, 0};
+    float rf[2] = {1.f, 1.f};
 #pragma unroll
     for (int pj = 0; pj < NPROJ; ++pj) {
       if (FMT == FMT_NVFP4) {
-        fs[pj] = p.s2[pj] ? __ldg(p.s2[pj] + un.e) : 1.0f;
+        rf[pj] = p.s2[pj] ? __ldg(p.s2[pj] + un.e) : 1.0f;
       } else if (live) {
         const uint8_t* srow = gscbuf(smem, p, ub) + pj * kTileRows * p.sr + m * p.sr;
-        fe[pj] = row_max_e8m0(srow, p.sr) - 13 - 127;
+        rf[pj] = ldexpf(1.0f, row_max_e8m0(srow, p.sr) - 13 - 127);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(b.scempty + ub);
+    if (!gwait_warp(p, b, b.dfull + db, (uint32_t)(it >> 1) & 1u)) return;
+    tc_fence_after();
     const int nmma = (un.nt + 15) & ~15;
-    const int r = un.rt * kTileRows + m;
+    const bool two_acc = (p.K + kKChunk - 1) / kKChunk > 1;   // issuer 1 had A slots
+    float* dst = p.out + (size_t)un.p0 * p.rows + un.rt * kTileRows + m;
     for (int cb = 0; cb < nmma; cb += 16) {
       uint32_t v0[16], v1[16];
       tmem_ld16(tmem_addr(tbase, q * 32, dcol(db, 0) + cb), v0);
-      if (NPROJ == 2) tmem_ld16(tmem_addr(tbase, q * 32, dcol(db, 1) + cb), v1);
+      if (NPROJ == 2 || two_acc) tmem_ld16(tmem_addr(tbase, q * 32, dcol(db, 1) + cb), v1);
       tmem_wait_ld();
-      if (live) {
+      if (NPROJ == 1 && two_acc) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int t = cb + i;
-          if (t >= un.nt) continue;
-          const int pos = un.p0 + t;
-          const int be = __ldg(p.bexp + pos);
-          float* dst = p.out + (size_t)pos * p.rows + r;
+        for (int i = 0; i < 16; ++i)
+          v0[i] = __float_as_uint(__uint_as_float(v0[i]) + __uint_as_float(v1[i]));
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int t = cb + i;
+        const float tf = __shfl_sync(0xffffffffu, t < 32 ? tf0 : tf1, t & 31);
+        if (live && t < un.nt) {
           if (NPROJ == 2) {
-            const float g = ldexpf(__uint_as_float(v0[i]) * fs[0], fe[0] + be);
-            const float uu = ldexpf(__uint_as_float(v1[i]) * fs[1], fe[1] + be);
-            *dst = g / (1.0f + expf(-g)) * uu;
+            const float g = __uint_as_float(v0[i]) * rf[0] * tf;
+            const float uu = __uint_as_float(v1[i]) * rf[1] * tf;
+            dst[(size_t)t * p.rows] = g / (1.0f + expf(-g)) * uu;
           } else {
-            const float y = ldexpf(__uint_as_float(v0[i]) * fs[0], fe[0] + be);
-            *dst = y * __ldg(p.wpos + pos);
+            dst[(size_t)t * p.rows] = __uint_as_float(v0[i]) * rf[0] * tf;
           }
         }
       }
@@ -591,25 +673,25 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemm_kernel(const __grid
   b.scfull = bars + 28;
   b.scempty = bars + 30;
   b.fin = bars + 32;
-  b.tslot = reinterpret_cast<uint32_t*>(bars + 33);
-  b.abort = reinterpret_cast<int*>(bars + 34);
+  b.tslot = reinterpret_cast<uint32_t*>(bars + 34);
+  b.abort = reinterpret_cast<int*>(bars + 35);
   const int tid = threadIdx.x, warp = tid >> 5;
   if (tid == 0) {
     for (int s = 0; s < p.nstages; ++s) {
       mbar_init(b.full + s, 1);
-      mbar_init(b.empty + s, 8 + 1);
+      mbar_init(b.empty + s, kDeqWarps + (NPROJ == 2 ? 2 : 1));
     }
     for (int a = 0; a < kNA; ++a) {
-      mbar_init(b.afull + a, 8);
-      mbar_init(b.aempty + a, 1);
+      mbar_init(b.afull + a, kDeqWarps);
+      mbar_init(b.aempty + a, NPROJ == 2 ? 2 : 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(b.dfull + i, 1);
-      mbar_init(b.dempty + i, 4);
+      mbar_init(b.dfull + i, 2);
+      mbar_init(b.dempty + i, kEpiWarps);
       mbar_init(b.scfull + i, 1);
-      mbar_init(b.scempty + i, 8 + 4);
+      mbar_init(b.scempty + i, kDeqWarps + kEpiWarps);
+      mbar_init(b.fin + i, 1);
     }
-    mbar_init(b.fin, 1);
     *b.abort = 0;
     fence_mbar_init();
   }
@@ -627,8 +709,10 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemm_kernel(const __grid
   if (warp == 0) {
     if ((tid & 31) == 0) g_producer<NPROJ>(p, smem, b, RT, nunits);
   } else if (warp == 1) {
-    if ((tid & 31) == 0) g_mma<NPROJ>(p, smem, b, tbase, RT, nunits);
-  } else if (warp < 10) {
+    if ((tid & 31) == 0) g_mma<NPROJ>(p, smem, b, tbase, RT, nunits, 0);
+  } else if (warp == kMma1) {
+    if ((tid & 31) == 0) g_mma<NPROJ>(p, smem, b, tbase, RT, nunits, 1);
+  } else if (warp < kEpi0) {
     g_dequant<NPROJ, FMT>(p, smem, b, tbase, RT, nunits);
   } else {
     g_epilogue<NPROJ, FMT>(p, smem, b, tbase, RT, nunits);
@@ -683,8 +767,10 @@ cudaError_t grouped_set_smem(int smem_bytes) {
 cudaError_t launch_grouped(const GroupedParams& gp, GemmParams gu, GemmParams gd, int grid,
                            int smem_gu, int smem_gd, cudaStream_t st) {
   const int S = gp.N * gp.k;
-  const int rsmem = kRtTok * gp.H * 2 + kRtTok * gp.E * 4;
-  grouped_router_kernel<<<(gp.N + kRtTok - 1) / kRtTok, 256, rsmem, st>>>(gp);
+  const int rsmem = kRtTok * gp.H * 2;
+  const dim3 rgrid((gp.N + kRtTok - 1) / kRtTok, (gp.E + kRtExp - 1) / kRtExp);
+  grouped_router_kernel<<<rgrid, 256, rsmem, st>>>(gp);
+  grouped_topk_kernel<<<(gp.N + 7) / 8, 256, 0, st>>>(gp);
   if (gp.route_only) return cudaGetLastError();
   grouped_plan_kernel<<<1, 1024, 0, st>>>(gp);
   grouped_gather_kernel<<<S, 128, 0, st>>>(gp);

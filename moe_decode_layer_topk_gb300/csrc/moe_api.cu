@@ -252,7 +252,7 @@ moe_status_t run_grouped(const moe_layer_desc_t* d, const moe_weights_t* w, cons
   int budget = 0, grid = 0;
   moe_status_t st = device_info(&budget, &grid);
   if (st != MOE_OK) return st;
-  if ((size_t)8 * d->H * 2 + (size_t)8 * d->E * 4 > (size_t)budget) return MOE_ERR_UNSUPPORTED;
+  if ((size_t)8 * d->H * 2 > (size_t)budget) return MOE_ERR_UNSUPPORTED;
 
   uint8_t* b = static_cast<uint8_t*>(ws);
   moe::GroupedParams gp;
