@@ -18,13 +18,14 @@
 //   gemm(1)   y = w(pos) * Dq(Wd) h16^T (FP32, one row per position)
 //   combine   out[n] = bf16(sum over the k slots of n of y)
 //
-// GEMM kernel (persistent, one CTA per SM, 23 warps):
+// GEMM kernel (persistent, one CTA per SM, 25 warps):
 //   warp 0      TMA producer: FP4 weight boxes (64 bytes x 128 rows, 64-byte
 //               swizzle), activation boxes (64 f16 x 64 rows, 128-byte
 //               swizzle), the unit's block scales (1D bulk copy)
-//   warps 1, 22 TMEM allocation (warp 1); lane 0 of each issues tcgen05.mma kind::f16
+//   warps 1,22-24  TMEM allocation (warp 1); lane 0 of each issues tcgen05.mma kind::f16
 //               (A from tensor memory, B from shared memory, FP32 accumulators
-//               in tensor memory, M = 128 weight rows, N = tokens rounded to 16)
+//               in tensor memory, M = 128 weight rows, N = tokens rounded to 16,
+//               one partial accumulator per issuer)
 //   warps 2-17  dequantisation: thread = weight row; E2M1 -> f16 with
 //               cvt.rn.f16x2.e2m1x2, times the block scale (E4M3 as f16:
 //               exact; E8M0 as a power of two relative to the row's largest
@@ -50,7 +51,7 @@ namespace moe {
 namespace {
 
 constexpr int kRtTok = 8;          // tokens per router CTA
-constexpr int kGThreads = 736;     // GEMM kernel: 23 warps
+constexpr int kGThreads = 800;     // GEMM kernel: 25 warps
 constexpr int kTileRows = 128;     // weight rows per unit (MMA M)
 constexpr int kKChunk = 128;       // K elements per stage
 constexpr int kABox = 8192;        // 128 rows x 64 bytes of FP4
@@ -309,13 +310,16 @@ namespace {
 
 // Roles: warp 0 producer, warp 1 TMEM owner + MMA issuer 0, warps 2-17
 // dequantisation (one 32-element piece of one projection per A slot each),
-// warps 18-21 epilogue, warp 22 MMA issuer 1.  A single thread issues a
-// small-N tcgen05.mma only every ~45 cycles whatever N (<= 64), while the
-// tensor core can take more: two issuers, each with its own accumulator
-// (gate / up, or the even / odd A slots of the one-projection GEMM), double
-// the MMA rate.
+// warps 18-21 epilogue, warps 22-24 MMA issuers 1-3.  One thread issues a
+// small-N tcgen05.mma only every ~45-60 cycles whatever N (<= 64), while the
+// tensor core takes far more; so four issuers share the MMAs, each with its
+// own accumulator, each owning whole stages (two projections: issuer =
+// projection x stage parity; one projection: issuer = stage index mod 4), so
+// that every barrier has a fixed set of arrivals.  The epilogue sums the
+// issuers' partial accumulators.
 constexpr int kDeqWarps = 16;
 constexpr int kEpiWarps = 4;
+constexpr int kIssuers = 4;
 constexpr int kDeq0 = 2, kEpi0 = kDeq0 + kDeqWarps, kMma1 = kEpi0 + kEpiWarps;
 
 struct GBars {
@@ -323,11 +327,11 @@ struct GBars {
   uint64_t* empty;    // [8]   16 dequant warps + MMA commit -> producer
   uint64_t* afull;    // [4]   dequant -> MMA (tensor-memory A slot written)
   uint64_t* aempty;   // [4]   MMA commits of the issuers that read the slot -> dequant
-  uint64_t* dfull;    // [2]   both issuers' commits -> epilogue (accumulators ready)
+  uint64_t* dfull;    // [2]   all issuers' commits -> epilogue (accumulators ready)
   uint64_t* dempty;   // [2]   epilogue -> MMA
   uint64_t* scfull;   // [2]   unit scales landed
   uint64_t* scempty;  // [2]   dequant + epilogue done with the unit's scales
-  uint64_t* fin;      // [2]   final MMA commit of each issuer
+  uint64_t* fin;      // [4]   final MMA commit of each issuer
   uint32_t* tslot;
   int* abort;
 };
@@ -368,10 +372,10 @@ __device__ __forceinline__ uint8_t* gstage(uint8_t* smem, const GemmParams& p, i
 __device__ __forceinline__ uint8_t* gscbuf(uint8_t* smem, const GemmParams& p, int ub) {
   return smem + p.off_sc + (size_t)ub * p.sc_bytes;
 }
-// Tensor-memory columns: accumulators [2 buffers][2 proj][64 tokens], then
+// Tensor-memory columns: accumulators [2 buffers][4 issuers][32 tokens], then
 // 4 A slots of 64 columns: [2 proj][32 columns = 64 K] (two projections) or
 // [64 columns = 128 K] (one projection).
-__device__ __forceinline__ int dcol(int b, int pj) { return b * 128 + pj * 64; }
+__device__ __forceinline__ int dcol(int b, int i) { return b * 128 + i * 32; }
 __device__ __forceinline__ int acol(int a, int pj) { return 256 + a * 64 + pj * 32; }
 // K elements of one A slot: 16 MMA K-steps' worth of dequantisation work
 // (16 warps x one 32-element piece) whatever the projection count.
@@ -519,15 +523,22 @@ __device__ void g_dequant(const GemmParams& p, uint8_t* smem, const GBars& b, ui
   }
 }
 
-// MMA issuer `me` (0 or 1).  Two projections: issuer = projection, every A
-// slot.  One projection: issuer = parity of the A slot, own accumulator; the
-// epilogue adds the two.  Full slots are issued as straight-line code (a
-// branch between MMAs slows the issue).
+// Does issuer `i` own stage `sctr`?  Two projections: stage parity = i & 1
+// (the projection is i >> 1); one projection: stage index mod 4 = i.
+template <int NPROJ>
+__device__ __forceinline__ bool owns_stage(int i, int sctr) {
+  return NPROJ == 2 ? ((sctr & 1) == (i & 1)) : ((sctr & 3) == i);
+}
+
+// MMA issuer `me` (0..3): every A slot of the stages it owns, into its own
+// partial accumulator.  Full slots are issued as straight-line code (a branch
+// between MMAs slows the issue).
 template <int NPROJ>
 __device__ void g_mma(const GemmParams& p, uint8_t* smem, const GBars& b, uint32_t tbase, int RT,
                       int nunits, int me) {
   constexpr int SK = slot_k<NPROJ>();
   constexpr int KS = SK / 16;   // MMA K-steps per slot
+  const int pj = (NPROJ == 2) ? (me >> 1) : 0;
   const int nch = (p.K + kKChunk - 1) / kKChunk;
   int sctr = 0, actr = 0, it = 0;
   for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++it) {
@@ -543,9 +554,7 @@ __device__ void g_mma(const GemmParams& p, uint8_t* smem, const GBars& b, uint32
       const int s = sctr % p.nstages;
       const int kleft = p.K - c * kKChunk;
       const int nslot = min(NPROJ, (kleft + SK - 1) / SK);
-      // one projection: a stage is one slot, used by one issuer
-      const bool mine = (NPROJ == 2) || ((actr & 1) == me);
-      if (!mine) {
+      if (!owns_stage<NPROJ>(me, sctr)) {
         actr += nslot;
         continue;
       }
@@ -555,7 +564,7 @@ __device__ void g_mma(const GemmParams& p, uint8_t* smem, const GBars& b, uint32
         const int a = actr % kNA;
         if (!gwait(p, b, b.afull + a, (uint32_t)(actr / kNA) & 1u)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t at = tmem_addr(tbase, 0, acol(a, NPROJ == 2 ? me : 0));
+        const uint32_t at = tmem_addr(tbase, 0, acol(a, pj));
         // B: box kk/64 of the stage, 32 bytes per K-step inside the 128-byte swizzled row
         const uint64_t bd = bdesc + (uint64_t)((j * SK / 64) * (kBBox >> 4));
         if (kleft - j * SK >= SK) {
@@ -623,17 +632,32 @@ __device__ void g_epilogue(const GemmParams& p, uint8_t* smem, const GBars& b, u
     if (!gwait_warp(p, b, b.dfull + db, (uint32_t)(it >> 1) & 1u)) return;
     tc_fence_after();
     const int nmma = (un.nt + 15) & ~15;
-    const bool two_acc = (p.K + kKChunk - 1) / kKChunk > 1;   // issuer 1 had A slots
+    // issuers that owned a stage of this unit (its stages are it*nch .. +nch-1)
+    const int nch = (p.K + kKChunk - 1) / kKChunk;
+    uint32_t used = 0u;
+    for (int c = 0; c < nch && c < 4; ++c)
+#pragma unroll
+      for (int is = 0; is < kIssuers; ++is)
+        if (owns_stage<NPROJ>(is, it * nch + c)) used |= 1u << is;
     float* dst = p.out + (size_t)un.p0 * p.rows + un.rt * kTileRows + m;
     for (int cb = 0; cb < nmma; cb += 16) {
-      uint32_t v0[16], v1[16];
-      tmem_ld16(tmem_addr(tbase, q * 32, dcol(db, 0) + cb), v0);
-      if (NPROJ == 2 || two_acc) tmem_ld16(tmem_addr(tbase, q * 32, dcol(db, 1) + cb), v1);
-      tmem_wait_ld();
-      if (NPROJ == 1 && two_acc) {
+      // partial accumulators of the issuers that owned at least one stage
+      float v0[16], v1[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          v0[i] = __float_as_uint(__uint_as_float(v0[i]) + __uint_as_float(v1[i]));
+      for (int i = 0; i < 16; ++i) v0[i] = v1[i] = 0.f;
+#pragma unroll
+      for (int is = 0; is < kIssuers; ++is) {
+        if (!(used >> is & 1)) continue;
+        uint32_t r[16];
+        tmem_ld16(tmem_addr(tbase, q * 32, dcol(db, is) + cb), r);
+        tmem_wait_ld();
+        if (NPROJ == 2 && is >= 2) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v1[i] += __uint_as_float(r[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v0[i] += __uint_as_float(r[i]);
+        }
       }
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -641,11 +665,11 @@ __device__ void g_epilogue(const GemmParams& p, uint8_t* smem, const GBars& b, u
         const float tf = __shfl_sync(0xffffffffu, t < 32 ? tf0 : tf1, t & 31);
         if (live && t < un.nt) {
           if (NPROJ == 2) {
-            const float g = __uint_as_float(v0[i]) * rf[0] * tf;
-            const float uu = __uint_as_float(v1[i]) * rf[1] * tf;
+            const float g = v0[i] * rf[0] * tf;
+            const float uu = v1[i] * rf[1] * tf;
             dst[(size_t)t * p.rows] = g / (1.0f + expf(-g)) * uu;
           } else {
-            dst[(size_t)t * p.rows] = __uint_as_float(v0[i]) * rf[0] * tf;
+            dst[(size_t)t * p.rows] = v0[i] * rf[0] * tf;
           }
         }
       }
@@ -673,8 +697,8 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemm_kernel(const __grid
   b.scfull = bars + 28;
   b.scempty = bars + 30;
   b.fin = bars + 32;
-  b.tslot = reinterpret_cast<uint32_t*>(bars + 34);
-  b.abort = reinterpret_cast<int*>(bars + 35);
+  b.tslot = reinterpret_cast<uint32_t*>(bars + 36);
+  b.abort = reinterpret_cast<int*>(bars + 37);
   const int tid = threadIdx.x, warp = tid >> 5;
   if (tid == 0) {
     for (int s = 0; s < p.nstages; ++s) {
@@ -683,15 +707,15 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemm_kernel(const __grid
     }
     for (int a = 0; a < kNA; ++a) {
       mbar_init(b.afull + a, kDeqWarps);
-      mbar_init(b.aempty + a, NPROJ == 2 ? 2 : 1);
+      mbar_init(b.aempty + a, NPROJ == 2 ? 2 : 1);   // issuers reading the slot
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(b.dfull + i, 2);
+      mbar_init(b.dfull + i, kIssuers);
       mbar_init(b.dempty + i, kEpiWarps);
       mbar_init(b.scfull + i, 1);
       mbar_init(b.scempty + i, kDeqWarps + kEpiWarps);
-      mbar_init(b.fin + i, 1);
     }
+    for (int i = 0; i < kIssuers; ++i) mbar_init(b.fin + i, 1);
     *b.abort = 0;
     fence_mbar_init();
   }
@@ -710,8 +734,8 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemm_kernel(const __grid
     if ((tid & 31) == 0) g_producer<NPROJ>(p, smem, b, RT, nunits);
   } else if (warp == 1) {
     if ((tid & 31) == 0) g_mma<NPROJ>(p, smem, b, tbase, RT, nunits, 0);
-  } else if (warp == kMma1) {
-    if ((tid & 31) == 0) g_mma<NPROJ>(p, smem, b, tbase, RT, nunits, 1);
+  } else if (warp >= kMma1) {
+    if ((tid & 31) == 0) g_mma<NPROJ>(p, smem, b, tbase, RT, nunits, warp - kMma1 + 1);
   } else if (warp < kEpi0) {
     g_dequant<NPROJ, FMT>(p, smem, b, tbase, RT, nunits);
   } else {

@@ -100,7 +100,7 @@ struct Params {
 // ------------------------------------------------------------ grouped path
 // Many-token forward (N * top_k beyond kMaxSlots): per-expert token groups on
 // the tensor cores (grouped_kernel.cu).
-constexpr int kGTileTok = 64;   // positions per token tile (MMA N <= 64)
+constexpr int kGTileTok = 32;   // positions per token tile (MMA N <= 32)
 
 struct GroupedParams {
   int N, H, inter, E, k, scoring, norm;
