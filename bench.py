@@ -12,7 +12,9 @@ back from the routing outputs before timing).  value = sum of bytes / time.
 
 Timed region: K steps replayed from a captured CUDA graph, bracketed by a
 barrier and torch.cuda.synchronize(), CUDA events on the launch stream; the
-maximum over ranks is taken.  --impl reference times the FP64 CPU oracle on a
+maximum over ranks is taken.  The line also carries "grouped": the many-token
+path (gpt-oss-shaped MXFP4 layer at N = 512, tcgen05 GEMMs) timed on the same
+GPU after the main measurement.  --impl reference times the FP64 CPU oracle on a
 bounded sample of the same workload instead.
 """
 from __future__ import annotations
@@ -114,6 +116,87 @@ def algorithmic_bytes(spec, idx: np.ndarray, N: int) -> dict:
     return {"U": U, "routed": routed, "total": routed + other}
 
 
+def decode_traffic(calls, launches_per_cycle: int):
+    """DRAM bytes per decode-kernel launch from the committed ncu record
+    (profiles/traffic.json), or None when the kernel source changed since the
+    counters were taken.  Token counts without their own capture are scaled
+    from the captured ones by algorithmic bytes (traffic/algorithmic ratio)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "moe_decode_layer_topk_gb300", "csrc", "decode_kernel.cu")
+    try:
+        rec = json.load(open(path))
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except (OSError, ValueError):
+        return None, "no record"
+    if rec.get("decode_kernel_cu_sha256") != h:
+        return None, "kernel changed since the ncu capture"
+    meas, alg = rec["dram_bytes_per_launch"], rec["algorithmic_bytes_per_launch"]
+    ratio = float(np.mean([meas[k] / alg[k] for k in meas]))
+    tot, scaled = 0.0, False
+    for c in calls:
+        key = str(c[1])
+        if key in meas:
+            tot += meas[key]
+        else:
+            tot += ratio * c[5]["total"]
+            scaled = True
+    note = rec["source"] + ("; other token counts scaled by algorithmic bytes" if scaled else "")
+    return tot / len(calls), note
+
+
+def kernels_per_call(spec, N: int) -> int:
+    """Kernels one moe_forward enqueues: the fused decode kernel, or the
+    grouped chain (router, top-k, plan, gather, gate/up GEMM, pack, down GEMM,
+    combine) once N * top_k exceeds the decode slot table (256)."""
+    return 1 if N * spec.top_k <= 256 else 8
+
+
+def measure_grouped(stream, name: str = "gpt_oss_120b", N: int = 512, reps: int = 10) -> dict:
+    """The grouped many-token path (tcgen05 GEMMs) on its headline workload:
+    one layer (1.69 GB of MXFP4 experts, far above L2, so every call streams
+    the weights from HBM), N tokens, CUDA-graph replays timed with events."""
+    import torch
+    from moe_decode_layer_topk_gb300 import _lib, synth
+    from moe_decode_layer_topk_gb300.device import DeviceLayer, bf16_tensor, workspace
+    spec = synth.CONFIGS[name]
+    dev = DeviceLayer.upload(synth.make_layer(spec))
+    x = bf16_tensor(synth.make_tokens(spec, N, seed=90512))
+    out = torch.empty_like(x)
+    ws = workspace(spec, N)
+    idx = torch.empty((N, spec.top_k), dtype=torch.int32, device="cuda")
+    _lib.moe_forward(dev.desc, dev.weights, x, out, ws, idx)
+    torch.cuda.synchronize()
+    b = algorithmic_bytes(spec, idx.cpu().numpy(), N)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            _lib.moe_forward(dev.desc, dev.weights, x, out, ws, stream=stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        _lib.moe_forward(dev.desc, dev.weights, x, out, ws, stream=stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    assert _lib.moe_get_error(ws) == _lib.MOE_OK
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    flops = 2.0 * N * spec.top_k * 3 * spec.H * spec.inter
+    peak, _ = _peaks()
+    del dev, ws
+    torch.cuda.empty_cache()
+    return {"workload": f"{name} layer at N={N} (grouped tcgen05 path)", "us_per_layer": round(us, 2),
+            "tokens_per_s": round(N / us * 1e6, 1), "U": b["U"], "bytes": int(b["total"]),
+            "GBps": round(b["total"] / us / 1e3, 1),
+            "hbm_frac_of_measured": round(b["total"] / us / 1e3 / peak, 4),
+            "tensor_tflops": round(flops / us / 1e6, 2), "launches_per_call": kernels_per_call(spec, N),
+            "reps": reps}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -150,6 +233,7 @@ def run_gpu(args):
     for c in calls:
         assert _lib.moe_get_error(c[4]) == _lib.MOE_OK
     launches_per_cycle = len(calls)
+    kernels_per_cycle = sum(kernels_per_call(spec, c[1]) for c in calls)
 
     def enqueue_cycle():
         for dev, N, x, out, ws, _ in calls:
@@ -259,6 +343,8 @@ def run_gpu(args):
                "h2d_bytes_per_step": io, "d2h_bytes_per_step": io}
 
     peak, peak_kind = _peaks()
+    traffic, traffic_note = (args.traffic, "--traffic") if args.traffic else \
+        decode_traffic(calls[:launches_per_cycle], launches_per_cycle)
     result = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -284,12 +370,16 @@ def run_gpu(args):
         "us_per_layer_mean": round(avg_launch_us, 3),
         "per_n": per_n,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": args.traffic,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": None if traffic is None else int(traffic),
+                     "traffic_source": traffic_note,
                      "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
                      "kernel": "moe::moe_decode_kernel"},
-        "gpu_launches": launches,
+        "gpu_launches": cycles * kernels_per_cycle,
         "e2e": e2e,
     }
+    if rank == 0 and not args.no_grouped:
+        result["grouped"] = measure_grouped(stream)
     if rank == 0:
         result["clocks"] = clk.summary()
         if not args.no_cpu_baseline:
@@ -377,6 +467,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-grouped", action="store_true",
+                    help="skip the grouped-path (gpt-oss N=512) measurement")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -114,11 +114,13 @@ typedef struct {
   const void* sh_gate_w;         /* bf16 [H] or NULL (ungated) */
 } moe_weights_t;
 
-/* Bytes of device workspace moe_forward needs for up to max_tokens rows.
+/* Bytes of device workspace moe_forward needs for any 1 <= N <= max_tokens.
  * Returns 0 if the descriptor is invalid.  The workspace holds the router
  * logits, the routing table, the gate/up activations, the FP32 output
  * accumulator and the grid-barrier words (the scratch the pages carve out of
- * ctx.buffers.scratch() in forward_atomic_c4.rs). */
+ * ctx.buffers.scratch() in forward_atomic_c4.rs); when max_tokens * top_k >
+ * 256 it also covers the grouped path's expert-sorted activation copies
+ * (about S * (2H + 4 max(H, inter) + 2 inter) bytes, S = max_tokens * top_k). */
 MOE_API size_t moe_workspace_size(const moe_layer_desc_t* desc, int32_t max_tokens);
 
 /* Zero a workspace before its first use (and after MOE_ERR_TIMEOUT).  Enqueues
@@ -134,10 +136,14 @@ MOE_API moe_status_t moe_workspace_init(void* workspace, size_t ws_bytes, void* 
  *   topk_w    f32 [N, top_k] device or NULL: their routing weights
  *   workspace device, >= moe_workspace_size(desc, N) bytes, zeroed once by
  *             moe_workspace_init; one workspace per concurrently running call
- * Supports 1 <= N and N*top_k <= 256.  Asynchronous on `stream`; no host
- * synchronisation, no allocation, so it may be captured in a CUDA graph.
- * Argument errors are returned before anything is enqueued; device-side
- * timeouts are reported by moe_get_error. */
+ * N*top_k <= 256 runs one fused decode kernel; larger N runs the grouped
+ * path (per-expert token groups on the tcgen05 tensor cores, the pages'
+ * "grouped GEMM (more than 64 rows)" of forward_batched.rs), which does not
+ * take a shared expert yet: N*top_k > 256 with shared_inter > 0 returns
+ * MOE_ERR_UNSUPPORTED.  Asynchronous on `stream`; no host synchronisation,
+ * no allocation, so it may be captured in a CUDA graph.  Argument errors are
+ * returned before anything is enqueued; device-side timeouts are reported by
+ * moe_get_error. */
 MOE_API moe_status_t moe_forward(const moe_layer_desc_t* desc, const moe_weights_t* weights,
                          const void* x, int32_t N, void* out,
                          int32_t* topk_idx, float* topk_w,
