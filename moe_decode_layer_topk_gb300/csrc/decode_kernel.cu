@@ -2,50 +2,54 @@
 //
 // Computes, for N token rows, the chain of forward_k3.rs (doc comment of
 // MoeLayer::forward_k3: gate GEMV -> batched top-k -> expert gate+up ->
-// SiLU+down -> weighted sum + shared blend) with the routed experts
-// accumulated as routing-weighted FP32 sums and cast to BF16 once at the end
+// SiLU+down -> weighted sum + shared blend) with the routed experts summed as
+// routing-weighted FP32 partials and cast to BF16 once at the end
 // (forward_atomic_c4.rs, doc comment of forward_atomic_c4_decode).
 //
 // Execution model: a persistent grid, one CTA per SM, every CTA resident at
 // once (cooperative launch).  Each CTA has 8 compute ("consumer") warps and
-// one producer thread that streams weights into a ring of shared-memory
-// stages with TMA (2D tensor-map boxes of 32 rows x 128 bytes, 128-byte
-// swizzle), completion tracked by mbarriers.
+// 4 producer threads (lane 0 of 4 warps, stage k issued by producer k mod 4:
+// a TMA instruction from DRAM holds its thread for a few hundred cycles) that
+// stream weights into a ring of shared-memory stages with TMA (2D tensor-map
+// boxes of 16 or 32 rows x 128 bytes, 128-byte swizzle), completion tracked
+// by mbarriers.
 //
 // Phases of one call (per CTA):
 //   P0  router GEMV for rows e = cta, cta+G, ... (128-bit loads); token prep
 //       (f16 copy of x scaled by a power of two, shared-expert gate) on the
-//       last CTAs; zero the FP32 accumulator and the row-block counters.
+//       last CTAs; zero the per-unit readiness counters.
 //   --  grid barrier B1 (arrive).  Shared-expert gate/up row groups need only
 //       x, so they are streamed and computed before waiting on B1.
 //   P1  every CTA computes the same top-k for all N tokens and the same table
-//       of unique experts (ascending id), per-expert token lists and
-//       (expert, token batch) units: each routed expert's weights are then read
-//       once for all its tokens (forward_batched.rs: "streams its weights once
-//       for all rows").
-//   P2  routed gate/up row groups -> h = SiLU(g)*u (FP32, workspace).
-//   --  grid barrier B2 (the producer keeps prefetching down weights).
-//   P3  down row groups (routed, then shared) -> routing-weighted FP32 red.add
-//       into acc[N,H]; at the end each CTA bumps the completion counters of the
-//       32-row output blocks it touched, and the CTA that completes a block
-//       casts it to BF16 into out (no third grid barrier).
+//       of unique experts, per-expert token lists and (expert, token batch)
+//       units: each routed expert's weights are then read once for all its
+//       tokens (forward_batched.rs: "streams its weights once for all rows").
+//   P2  routed gate/up row groups of 16 rows (gate rows and up rows stacked
+//       as one 32-row tile, lane j < 16 gate, lane j >= 16 up): h = SiLU(g)*u
+//       stored as f16 with one power-of-two exponent per 16 rows; each row
+//       group bumps its unit's readiness counter.
+//   P3  down: each CTA owns whole 16-row blocks of the output.  Every unit
+//       (and shared-expert token batch) is one job for one warp (half-warps
+//       split K); the producer prefetches the down weights during P2 and adds
+//       a job's activations to its stage once the unit's counter says its h
+//       is complete.  Jobs add their routing-weighted rows into shared
+//       memory; the block is cast to BF16 and written once: no second grid
+//       barrier, no global atomics, no accumulator in global memory.
 //
-// Work split: a row group (RG) is 32 consecutive weight rows of one
-// (expert, token batch) unit; each kind's RG list is split evenly over the
-// CTAs.  Inside a CTA, lane j of every consumer warp owns row j of the RG and
-// the 8 warps split the K range; partial sums meet in shared memory at the
-// end of the RG.  The 128-byte swizzle of the boxes makes the lane-per-row
-// 128-bit shared loads conflict free; activations are read as broadcasts.
+// Inside a row group, lane j owns weight row j and the 8 warps split the K
+// range; partial sums meet in shared memory at the end of the group.  The
+// 128-byte swizzle makes the lane-per-row 128-bit shared loads conflict free;
+// activations are read as broadcasts.
 //
 // FP4 arithmetic: E2M1 codes become f16x2 with cvt.rn.f16x2.e2m1x2; each
-// 16-element (NVFP4) or 32-element (MXFP4) block is summed with f16x2 FMAs
-// against x (or h) held as f16 scaled by a per-row power of two that keeps
-// every partial below 2^14; each block partial is then multiplied by its
-// E4M3/E8M0 scale and accumulated in FP32.  The shared expert (BF16) uses
-// fma.rn.f32.bf16 (BF16 products, FP32 accumulation).
+// 16-element block is summed with f16x2 FMAs against x or h held as f16
+// scaled by a power of two that keeps every partial below 2^14; each block
+// partial is then multiplied by its E4M3/E8M0 scale (times the h exponent in
+// the down projection) and accumulated in FP32.  The shared expert (BF16)
+// uses fma.rn.f32.bf16 (BF16 products, FP32 accumulation).
 //
-// Every wait (grid barrier, stage, routing-ready) is bounded by a time budget;
-// on expiry the kernel records an error bit in the workspace and drains.
+// Every wait (grid barrier, stage, readiness) is bounded by a time budget; on
+// expiry the kernel records an error bit in the workspace and drains.
 
 #include <algorithm>
 
@@ -61,21 +65,18 @@ namespace moe {
 struct Tables {
   int16_t sel_e[kMaxSlots];    // routing per slot s = n*k + j
   float sel_w[kMaxSlots];
-  uint32_t cnt[kMaxE];         // per expert: count, then unique index
-  int16_t uexp[kMaxSlots];     // unique experts, ascending id
+  uint32_t cnt[kMaxE];         // per expert: first slot, then unique index
+  int16_t uexp[kMaxSlots];     // unique experts
   uint16_t ucnt[kMaxSlots];    // tokens routed to unique expert u
   uint16_t hoff[kMaxSlots];    // first slot of u in the (expert, token) order
   uint8_t utok[kMaxSlots];     // token of (expert, position) slot
   float uw[kMaxSlots];         // routing weight of that slot
   uint16_t unit_u[kMaxSlots];  // units = (unique expert, token batch)
   uint8_t unit_tb[kMaxSlots];
-  uint16_t brg[kMaxRgList];    // output row blocks this CTA added to (pending)
-  uint8_t bfin[kMaxRgList];    // ... and whether this CTA completed them
-  int nbrg;
+  int16_t xe[kMaxSlots];       // power-of-two exponent of each token's f16 x
+  float s2[3][kMaxSlots];      // gate / up / down scale2 of unique expert u
   int U, n_units;
   int abort;                   // set when a bounded wait expired
-  int hb_kind, hb_unit;        // unit whose activations sit in hbuf
-  int hexp[kTB];               // power-of-two exponents of hbuf rows
   float rscratch[kConsumerWarps * 8];
   uint32_t uscratch[kConsumerWarps * 2];
 };
@@ -152,10 +153,10 @@ __device__ __forceinline__ int scale_exponent(float amax) {
 
 // ------------------------------------------------------------ grid barrier
 // The workspace keeps one monotonic 64-bit arrival counter.  Every CTA
-// arrives exactly twice per call, so at kernel start the counter lies in
-// [base, base + G) with base a multiple of 2G (no CTA can pass B1 before all
-// have arrived).  Arrivals are fire-and-forget release reductions; a waiter
-// polls with acquire loads until the counter reaches base + G*(b+1).
+// arrives exactly once per call, so at kernel start the counter is a multiple
+// of G (no CTA can pass B1 before all have arrived).  Arrivals are
+// fire-and-forget release reductions; a waiter polls with acquire loads until
+// the counter reaches base + G.
 __device__ __forceinline__ void grid_arrive(Ctrl* c) { red_release_add_u64(&c->arrivals, 1ull); }
 
 __device__ bool grid_wait(Ctrl* c, unsigned long long target, uint64_t budget_ns) {
@@ -417,6 +418,8 @@ __device__ __noinline__ void routing_phase(const Params& p, int write_out, Table
     else if (E <= 512) topk_token<16>(E, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
     else topk_token<32>(E, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
   }
+  if (!p.route_only && warp == kConsumerWarps - 1)
+    for (int n = lane; n < p.N; n += 32) tb.xe[n] = (int16_t)ld_cg_s32(p.xexp + n);
   consumer_sync();
   if (warp == 0) {
     const bool done = (S <= 32) && build_tables_small(k, S, tb, lane);
@@ -429,9 +432,20 @@ __device__ __noinline__ void routing_phase(const Params& p, int write_out, Table
     }
   }
   consumer_sync();
+  if (!p.route_only && warp == kConsumerWarps - 1) {
+    for (int u = lane; u < tb.U; u += 32) {
+      const int e = tb.uexp[u];
+      tb.s2[0][u] = p.g2 ? __ldg(p.g2 + e) : 1.0f;
+      tb.s2[1][u] = p.u2 ? __ldg(p.u2 + e) : 1.0f;
+      tb.s2[2][u] = p.d2 ? __ldg(p.d2 + e) : 1.0f;
+    }
+  }
+  consumer_sync();
 }
 
 // ------------------------------------------------------- row-group plumbing
+// Gate/up row groups (AS: 32 shared-expert rows; AR: 16 routed rows of gate
+// and of up).
 
 struct RG {
   int unit, rg;   // unit index within the kind, row group within the unit
@@ -442,14 +456,14 @@ struct RG {
 
 template <int KIND>
 __device__ __forceinline__ int kind_units(const Params& p, const Tables& tb) {
-  if (KIND == KIND_AS || KIND == KIND_BS) return p.Is > 0 ? (p.N + kTB - 1) / kTB : 0;
+  if (KIND == KIND_AS) return p.Is > 0 ? (p.N + kTB - 1) / kTB : 0;
   return tb.n_units;
 }
 
 template <int KIND>
 __device__ __forceinline__ void kind_range(const Params& p, const Tables& tb, int cta, int G,
                                            int& lo, int& hi) {
-  const uint32_t rpu = (uint32_t)(p.geo[KIND].rows_total / kRows);
+  const uint32_t rpu = (uint32_t)(p.geo[KIND].rows_total / p.geo[KIND].rg_rows);
   const uint32_t T = (uint32_t)kind_units<KIND>(p, tb) * rpu;   // < 2^22: products fit 32 bits
   lo = (int)(T * (uint32_t)cta / (uint32_t)G);
   hi = (int)(T * (uint32_t)(cta + 1) / (uint32_t)G);
@@ -459,29 +473,30 @@ template <int KIND>
 __device__ __forceinline__ RG decode_rg(const Params& p, const Tables& tb, int g) {
   RG r;
   const int rows = p.geo[KIND].rows_total;
-  const int rpu = rows / kRows;
+  const int rr = p.geo[KIND].rg_rows;
+  const int rpu = rows / rr;
   r.unit = g / rpu;
   r.rg = g % rpu;
-  if (KIND == KIND_AS || KIND == KIND_BS) {
+  if (KIND == KIND_AS) {
     r.u = 0;
     r.e = 0;
     r.tb = r.unit;
     r.nt = min(kTB, p.N - r.tb * kTB);
-    r.row0 = r.rg * kRows;
+    r.row0 = r.rg * rr;
   } else {
     r.u = tb.unit_u[r.unit];
     r.tb = tb.unit_tb[r.unit];
     r.e = tb.uexp[r.u];
     r.nt = min(kTB, (int)tb.ucnt[r.u] - r.tb * kTB);
-    r.row0 = r.e * rows + r.rg * kRows;
+    r.row0 = r.e * rows + r.rg * rr;
   }
   return r;
 }
 
-// Token (row of x / out) of batch slot t of an RG.
+// Token (row of x / out) of batch slot t of a gate/up row group.
 template <int KIND>
 __device__ __forceinline__ int rg_token(const Tables& tb, const RG& r, int t) {
-  if (KIND == KIND_AS || KIND == KIND_BS) return r.tb * kTB + t;
+  if (KIND == KIND_AS) return r.tb * kTB + t;
   return tb.utok[tb.hoff[r.u] + r.tb * kTB + t];
 }
 
@@ -491,50 +506,97 @@ __device__ __forceinline__ int chunk_row_bytes(const Geo& g, int c) {
 }
 __device__ __forceinline__ bool swizzled(const Geo& g) { return g.kb >= kBoxBytes; }
 
+// Down jobs of a CTA: for each owned 16-row output block i (rows
+// (cta + i*G)*16 ..), the routed units 0..nr-1, then the shared-expert token
+// batches; each job is nchunks stages.
+struct DnIt {
+  int i, jb, c;
+};
+__device__ __forceinline__ void dn_next(DnIt& it, int J, int nr, int nch_r, int nch_s) {
+  ++it.c;
+  if (it.c == (it.jb < nr ? nch_r : nch_s)) {
+    it.c = 0;
+    if (++it.jb == J) {
+      it.jb = 0;
+      ++it.i;
+    }
+  }
+}
+__device__ __forceinline__ int dn_blocks(const Params& p, int cta, int G) {
+  return cta < p.nrb ? (p.nrb - cta + G - 1) / G : 0;
+}
+
 // ------------------------------------------------------------------ producer
 
+// Weight boxes (and block scales) of chunk c of one stage; `opnd_bytes` of
+// activations will complete the stage's transaction count (issued now or
+// later by produce_operand).
 template <int KIND>
-__device__ __forceinline__ void produce_stage(const Params& p, const Tables& tb, const RG& r,
-                                              int c, uint8_t* st, uint64_t* full) {
+__device__ __forceinline__ void produce_weights(const Params& p, int row0, int c, uint8_t* st,
+                                                uint64_t* full, uint32_t opnd_bytes) {
   const Geo& g = p.geo[KIND];
   const int rb = chunk_row_bytes(g, c);
   const bool sw = swizzled(g);
   const int nbox = sw ? (rb + kBoxBytes - 1) / kBoxBytes : 1;
-  const int box_bytes = sw ? kBoxTileBytes : kRows * g.kb;
-  const bool has_opnd = (KIND == KIND_AS || KIND == KIND_AR);
-  const int elems = rb * 8 / (g.fmt == FMT_BF16 ? 16 : 4);   // K elements in this chunk
-  uint32_t bytes = (uint32_t)(g.nproj * nbox * box_bytes);
-  if (g.scale_mode == SCALES_TMAP) bytes += (uint32_t)(g.nproj * kRows * g.scb);
-  if (g.scale_mode == SCALES_BLOCK) bytes += (uint32_t)(g.nproj * kRows * g.sr);
-  if (has_opnd) bytes += (uint32_t)(r.nt * elems * 2);
+  const int box_bytes = sw ? g.brows * kBoxBytes : g.brows * g.kb;
+  // projection stride inside the stage: one tile of 4 columns x brows rows
+  const int pstride = sw ? kBoxesPerChunk * g.brows * kBoxBytes : g.brows * g.kb;
+  uint32_t bytes = (uint32_t)(g.nproj * (g.use3d ? kBoxesPerChunk : nbox) * box_bytes) + opnd_bytes;
+  if (g.scale_mode == SCALES_TMAP) bytes += (uint32_t)(g.nproj * g.brows * g.scb);
+  if (g.scale_mode == SCALES_BLOCK) bytes += (uint32_t)(g.nproj * g.brows * g.sr);
   mbar_arrive_expect_tx(full, bytes);
   const int wmap0 = (KIND == KIND_AR) ? TM_GQ : (KIND == KIND_BR) ? TM_DQ
                   : (KIND == KIND_AS) ? TM_SG : TM_SD;
+  const int wmap3 = (KIND == KIND_AR) ? TM3_GQ : (KIND == KIND_BR) ? TM3_DQ
+                  : (KIND == KIND_AS) ? TM3_SG : TM3_SD;
   for (int pj = 0; pj < g.nproj; ++pj) {
-    const CUtensorMap* tm = &p.tm[wmap0 + pj];
-    for (int b = 0; b < nbox; ++b)
-      tma_load_2d(st + (sw ? (pj * kBoxesPerChunk + b) * kBoxTileBytes : pj * kRows * g.kb), tm,
-                  c * kChunkBytes + b * kBoxBytes, r.row0, full);
+    if (g.use3d) {
+      // columns 4c .. 4c+3 (beyond the row: zero fill, counted in the box bytes)
+      tma_load_3d(st + pj * pstride, &p.tm[wmap3 + pj], 0, row0, c * kBoxesPerChunk, full);
+    } else {
+      const CUtensorMap* tm = &p.tm[wmap0 + pj];
+      for (int b = 0; b < nbox; ++b)
+        tma_load_2d(st + pj * pstride + b * g.tile_bytes, tm, c * kChunkBytes + b * kBoxBytes,
+                    row0, full);
+    }
   }
   if (g.scale_mode == SCALES_TMAP) {
     const int smap0 = (KIND == KIND_AR) ? TM_GS : TM_DS;
     for (int pj = 0; pj < g.nproj; ++pj)
-      tma_load_2d(st + g.scale_off + pj * kRows * g.scb, &p.tm[smap0 + pj], c * g.scb, r.row0,
+      tma_load_2d(st + g.scale_off + pj * g.brows * g.scb, &p.tm[smap0 + pj], c * g.scb, row0,
                   full);
   } else if (g.scale_mode == SCALES_BLOCK) {
     for (int pj = 0; pj < g.nproj; ++pj) {
       const uint8_t* base = (KIND == KIND_AR) ? (pj == 0 ? p.gsc : p.usc) : p.dsc;
-      bulk_g2s(st + g.scale_off + pj * kRows * g.sr, base + (size_t)r.row0 * g.sr,
-               (uint32_t)(kRows * g.sr), full);
+      bulk_g2s(st + g.scale_off + pj * g.brows * g.sr, base + (size_t)row0 * g.sr,
+               (uint32_t)(g.brows * g.sr), full);
     }
   }
-  if (has_opnd) {
-    const uint16_t* xs = (KIND == KIND_AR) ? p.x16 : p.x;
-    for (int t = 0; t < r.nt; ++t) {
-      const int n = rg_token<KIND>(tb, r, t);
-      bulk_g2s(st + g.opnd_off + t * g.Kc * 2, xs + (size_t)n * p.H + (size_t)c * g.Kc,
-               (uint32_t)(elems * 2), full);
-    }
+}
+
+// K elements of chunk c.
+__device__ __forceinline__ int chunk_elems(const Geo& g, int c) {
+  const int rb = chunk_row_bytes(g, c);
+  return g.fmt == FMT_BF16 ? rb / 2 : rb * 2;
+}
+
+template <int KIND>
+__device__ __forceinline__ uint32_t gateup_opnd_bytes(const Geo& g, int c, int nt) {
+  return (uint32_t)(nt * chunk_elems(g, c) * 2);
+}
+
+// One stage of a gate/up row group: weights, scales and the x chunk.
+template <int KIND>
+__device__ __forceinline__ void produce_stage(const Params& p, const Tables& tb, const RG& r,
+                                              int c, uint8_t* st, uint64_t* full) {
+  const Geo& g = p.geo[KIND];
+  const int elems = chunk_elems(g, c);
+  produce_weights<KIND>(p, r.row0, c, st, full, gateup_opnd_bytes<KIND>(g, c, r.nt));
+  const uint16_t* xs = (KIND == KIND_AR) ? p.x16 : p.x;
+  for (int t = 0; t < r.nt; ++t) {
+    const int n = rg_token<KIND>(tb, r, t);
+    bulk_g2s(st + g.opnd_off + t * g.Kc * 2, xs + (size_t)n * p.H + (size_t)c * g.Kc,
+             (uint32_t)(elems * 2), full);
   }
 }
 
@@ -545,10 +607,11 @@ struct Ring {
   int nstages, stage_bytes;
 };
 
-// Streams every stage of one kind's row groups; returns false on abort.
+// Streams the stages k = pid (mod kProducers) of one gate/up kind's row
+// groups; returns false on abort.  `*ctr_io` counts all stages.
 template <int KIND>
 __device__ __noinline__ bool produce_kind(const Params& p, Tables& tb, const Ring ring, int cta,
-                                          int G, int* ctr_io) {
+                                          int G, int* ctr_io, int pid) {
   int ctr = *ctr_io;
   if (kind_units<KIND>(p, tb) == 0) return true;
   int lo, hi;
@@ -557,6 +620,10 @@ __device__ __noinline__ bool produce_kind(const Params& p, Tables& tb, const Rin
   for (int gi = lo; gi < hi; ++gi) {
     const RG r = decode_rg<KIND>(p, tb, gi);
     for (int c = 0; c < nch; ++c) {
+      if (ctr % kProducers != pid) {
+        *ctr_io = ++ctr;
+        continue;
+      }
       const int slot = ctr % ring.nstages;
       const uint32_t round = (uint32_t)(ctr / ring.nstages);
       if (aborted(tb)) return false;
@@ -573,6 +640,153 @@ __device__ __noinline__ bool produce_kind(const Params& p, Tables& tb, const Rin
   return true;
 }
 
+// Job parameters of a down stage.
+struct DnJob {
+  bool routed;
+  int row0;    // tensor-map row of the block
+  int nt;      // tokens
+  int src0;    // first activation row: h16 slot (routed) or token (shared)
+  int unit;    // routed unit (readiness counter, hexp row)
+};
+__device__ __forceinline__ DnJob dn_job(const Params& p, const Tables& tb, int cta, int G,
+                                        const DnIt& it, int nr) {
+  DnJob j;
+  const int rb = cta + it.i * G;
+  j.routed = it.jb < nr;
+  if (j.routed) {
+    const int u = tb.unit_u[it.jb], tbi = tb.unit_tb[it.jb];
+    j.unit = it.jb;
+    j.nt = min(kTB, (int)tb.ucnt[u] - tbi * kTB);
+    j.src0 = tb.hoff[u] + tbi * kTB;
+    j.row0 = tb.uexp[u] * p.H + rb * kDnRows;
+  } else {
+    const int b = it.jb - nr;
+    j.unit = -1;
+    j.nt = min(kTB, p.N - b * kTB);
+    j.src0 = b * kTB;
+    j.row0 = rb * kDnRows;
+  }
+  return j;
+}
+__device__ __forceinline__ uint32_t dn_opnd_bytes(const Params& p, const DnJob& j, int c) {
+  const Geo& g = p.geo[j.routed ? KIND_BR : KIND_BS];
+  const int elems = chunk_elems(g, c);
+  uint32_t b = (uint32_t)(j.nt * elems * 2);
+  if (j.routed) b += (uint32_t)(((elems / 16) + 15) & ~15);
+  return b;
+}
+__device__ __forceinline__ void dn_operand(const Params& p, const DnJob& j, int c, uint8_t* st,
+                                           uint64_t* full) {
+  const Geo& g = p.geo[j.routed ? KIND_BR : KIND_BS];
+  const int elems = chunk_elems(g, c);
+  if (j.routed) {
+    for (int t = 0; t < j.nt; ++t)
+      bulk_g2s(st + g.opnd_off + t * g.Kc * 2,
+               p.h16 + (size_t)(j.src0 + t) * p.inter + (size_t)c * g.Kc, (uint32_t)(elems * 2),
+               full);
+    bulk_g2s(st + g.hx_off, p.hexp + (size_t)j.unit * p.hstride + c * (g.Kc / 16),
+             (uint32_t)(((elems / 16) + 15) & ~15), full);
+  } else {
+    for (int t = 0; t < j.nt; ++t)
+      bulk_g2s(st + g.opnd_off + t * g.Kc * 2,
+               p.hs + (size_t)(j.src0 + t) * p.Is + (size_t)c * g.Kc, (uint32_t)(elems * 2), full);
+  }
+}
+
+// Down stages: weights are issued as soon as ring slots free up (prefetch
+// during the gate/up phase); a stage's activations follow once its unit's
+// gate/up row groups are all done everywhere (readiness counters, acquire).
+__device__ __noinline__ bool produce_down(const Params& p, Tables& tb, const Ring ring, int cta,
+                                          int G, int* ctr_io, int pid) {
+  const int nrbl = dn_blocks(p, cta, G);
+  const int nr = tb.n_units, nsh = p.Is > 0 ? (p.N + kTB - 1) / kTB : 0, J = nr + nsh;
+  if (nrbl == 0 || J == 0) return true;
+  const int nch_r = p.geo[KIND_BR].nchunks, nch_s = nsh ? p.geo[KIND_BS].nchunks : 1;
+  const int total = nrbl * (nr * nch_r + nsh * nch_s);
+  const uint32_t need_r = (uint32_t)(p.inter / kDnRows);
+  const uint32_t need_s = nsh ? (uint32_t)(nsh * (p.Is / kRows)) : 0u;
+  const int ctr0 = *ctr_io;
+  DnIt W{0, 0, 0}, O{0, 0, 0};
+  int kw = 0, ko = 0;
+  uint64_t idle0 = 0;
+  bool ok = true;
+  // skip the stages of the other producers (both cursors)
+  auto skip_w = [&]() {
+    while (kw < total && (ctr0 + kw) % kProducers != pid) {
+      dn_next(W, J, nr, nch_r, nch_s);
+      ++kw;
+    }
+  };
+  auto skip_o = [&]() {
+    while (ko < kw && (ctr0 + ko) % kProducers != pid) {
+      dn_next(O, J, nr, nch_r, nch_s);
+      ++ko;
+    }
+  };
+  skip_w();
+  while (ko < total) {
+    if (aborted(tb)) { ok = false; break; }
+    skip_o();
+    if (ko >= total) break;
+    bool did = false;
+    if (ko < kw) {
+      const DnJob j = dn_job(p, tb, cta, G, O, nr);
+      const uint32_t have = ld_acquire_u32(p.ready + (j.routed ? j.unit : kReadyAS));
+      if (have >= (j.routed ? need_r : need_s)) {
+        fence_proxy_async_global();   // h16 / hs were written by other CTAs
+        const int k = ctr0 + ko;
+        dn_operand(p, j, O.c, ring.base + (size_t)(k % ring.nstages) * ring.stage_bytes,
+                   ring.full + k % ring.nstages);
+        dn_next(O, J, nr, nch_r, nch_s);
+        ++ko;
+        skip_o();
+        did = true;
+      }
+    }
+    if (!did && kw < total) {
+      const int k = ctr0 + kw;
+      const int slot = k % ring.nstages;
+      if (mbar_test_wait(ring.empty + slot, ((uint32_t)(k / ring.nstages) & 1u) ^ 1u)) {
+        const DnJob j = dn_job(p, tb, cta, G, W, nr);
+        uint8_t* st = ring.base + (size_t)slot * ring.stage_bytes;
+        if (j.routed) produce_weights<KIND_BR>(p, j.row0, W.c, st, ring.full + slot, dn_opnd_bytes(p, j, W.c));
+        else produce_weights<KIND_BS>(p, j.row0, W.c, st, ring.full + slot, dn_opnd_bytes(p, j, W.c));
+        dn_next(W, J, nr, nch_r, nch_s);
+        ++kw;
+        skip_w();
+        did = true;
+      }
+    }
+    if (did) {
+      idle0 = 0;
+    } else {
+      const uint64_t now = global_timer_ns();
+      if (idle0 == 0) idle0 = now;
+      else if (now - idle0 > p.timeout_ns) {
+        set_abort(p, tb, kErrTimeoutProducer);
+        ok = false;
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  if (!ok) {
+    // complete the transaction counts of our stages whose weights are in flight
+    while (ko < kw) {
+      if ((ctr0 + ko) % kProducers == pid) {
+        const DnJob j = dn_job(p, tb, cta, G, O, nr);
+        const int k = ctr0 + ko;
+        dn_operand(p, j, O.c, ring.base + (size_t)(k % ring.nstages) * ring.stage_bytes,
+                   ring.full + k % ring.nstages);
+      }
+      dn_next(O, J, nr, nch_r, nch_s);
+      ++ko;
+    }
+  }
+  *ctr_io = ctr0 + kw;
+  return ok;
+}
+
 // ------------------------------------------------------------------ consumer
 
 struct ConsumerCtx {
@@ -580,8 +794,10 @@ struct ConsumerCtx {
   uint64_t* full;
   uint64_t* empty;
   int nstages, stage_bytes;
-  float* red;
-  uint8_t* hbuf;
+  float* red;        // two partial-sum buffers of kRedFloats
+  float* sacc;
+  uint64_t* rfull;   // [2] compute warps -> epilogue warp (buffer filled)
+  uint64_t* rempty;  // [2] epilogue warp -> compute warps (buffer free)
 };
 
 template <typename T>
@@ -591,24 +807,44 @@ __device__ __forceinline__ T lds(const uint8_t* p) {
 
 // Stage geometry of one kind, held in registers by the consumer.
 struct SG {
-  int kb, Kc, K, nchunks, scale_mode, scale_off, scb, sr, opnd_off, scale_swz;
+  int kb, Kc, K, nchunks, scale_mode, scale_off, scb, sr, opnd_off, hx_off, scale_swz;
 };
 __device__ __forceinline__ SG load_sg(const Geo& g) {
   SG r;
   r.kb = g.kb; r.Kc = g.Kc; r.K = g.K; r.nchunks = g.nchunks; r.scale_mode = g.scale_mode;
   r.scale_off = g.scale_off; r.scb = g.scb; r.sr = g.sr; r.opnd_off = g.opnd_off;
+  r.hx_off = g.hx_off;
   r.scale_swz = (g.scale_mode == SCALES_TMAP && g.scb == 64) ? 1 : 0;
   return r;
 }
 
-// Address of the 16-byte piece `piece` of weight row `lane` in a stage, for
-// projection pj: 128-byte-swizzled boxes (rows of >= 128 bytes) or plain rows.
+// Routed gate/up stage: lane j < 16 reads gate row j, lane j >= 16 up row
+// j-16; tiles [proj][128-byte column][16 rows][128 bytes] (128-byte swizzle),
+// or plain rows (gate rows then up rows) when the row is under 128 bytes.
+__device__ __forceinline__ const uint8_t* wptr_ar(const uint8_t* st, int kb, int lane,
+                                                  int piece) {
+  if (kb >= kBoxBytes)
+    return st + (lane >> 4) * (kBoxesPerChunk * kDnRows * kBoxBytes) +
+           (piece >> 3) * (kDnRows * kBoxBytes) + (lane & 15) * kBoxBytes +
+           (((piece & 7) ^ (lane & 7)) << 4);
+  return st + lane * kb + piece * 16;
+}
+
+// Address of the 16-byte piece `piece` of tile row `lane` (32-row tiles of
+// 128-byte-swizzled boxes, rows >= 128 bytes) or of plain rows.
 __device__ __forceinline__ const uint8_t* wptr(const uint8_t* st, int kb, int pj, int lane,
                                                int piece) {
   if (kb >= kBoxBytes)
     return st + (pj * kBoxesPerChunk + (piece >> 3)) * kBoxTileBytes + lane * kBoxBytes +
            (((piece & 7) ^ (lane & 7)) << 4);
   return st + pj * kRows * kb + lane * kb + piece * 16;
+}
+// Same for the 16-row tiles of the down blocks.
+__device__ __forceinline__ const uint8_t* wptr16(const uint8_t* st, int kb, int row, int piece) {
+  if (kb >= kBoxBytes)
+    return st + (piece >> 3) * (kDnRows * kBoxBytes) + row * kBoxBytes +
+           (((piece & 7) ^ (row & 7)) << 4);
+  return st + row * kb + piece * 16;
 }
 
 // Scale byte `b` of row `lane` in a tensor-map scale box (64-byte swizzle when
@@ -679,7 +915,7 @@ __device__ __forceinline__ void compute_fp4(const uint8_t* st, const SG& g, int 
       uint32_t wd[NPROJ][16];
 #pragma unroll
       for (int pj = 0; pj < NPROJ; ++pj) {
-        const uint4 w = lds<uint4>(wptr(st, g.kb, pj, lane, s));
+        const uint4 w = lds<uint4>(wptr_ar(st, g.kb, lane, s));
         uint32_t o[4];
         e2m1x8_to_f16x2x4(w.x, o);
         wd[pj][0] = o[0]; wd[pj][1] = o[1]; wd[pj][2] = o[2]; wd[pj][3] = o[3];
@@ -770,154 +1006,219 @@ __device__ __forceinline__ void compute_bf16(const uint8_t* st, const SG& g,
   }
 }
 
-// Activations of a down-projection unit into hbuf: routed h as f16 scaled
-// per token by a power of two, shared h as BF16.
-template <int KIND>
-__device__ __noinline__ void stage_hbuf(const Params& p, Tables& tb, const RG& r, uint8_t* hbuf,
-                                        int ctid) {
-  const int K = p.geo[KIND].K;
-  if (KIND == KIND_BR) {
-    float m[kTB];
-#pragma unroll
-    for (int t = 0; t < kTB; ++t) m[t] = 0.f;
-#pragma unroll
-    for (int t = 0; t < kTB; ++t) {
-      if (t < r.nt) {
-        const float* src = p.h + (size_t)(tb.hoff[r.u] + r.tb * kTB + t) * p.inter;
-        for (int kk = ctid * 4; kk < K; kk += kConsumerThreads * 4) {
-          const float4 v = ld_cg_f32x4(src + kk);
-          m[t] = fmaxf(m[t], fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-        }
-      }
-    }
-    block_reduce<kTB, true>(m, tb, ctid);
-#pragma unroll
-    for (int t = 0; t < kTB; ++t) {
-      if (t < r.nt) {
-        const int ex = scale_exponent(m[t]);
-        if (ctid == 0) tb.hexp[t] = ex;
-        const float sc = ldexpf(1.0f, -ex);
-        const float* src = p.h + (size_t)(tb.hoff[r.u] + r.tb * kTB + t) * p.inter;
-        __half* dst = reinterpret_cast<__half*>(hbuf) + (size_t)t * K;
-        for (int kk = ctid * 4; kk < K; kk += kConsumerThreads * 4) {
-          const float4 v = ld_cg_f32x4(src + kk);
-          *reinterpret_cast<__half2*>(dst + kk) = __floats2half2_rn(v.x * sc, v.y * sc);
-          *reinterpret_cast<__half2*>(dst + kk + 2) = __floats2half2_rn(v.z * sc, v.w * sc);
-        }
-      }
-    }
+// ------------------------------------------------------------- down compute
+// 2^e for e in [-126, 127].
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// One 16-byte piece s of a routed down job for NT tokens: per-token sum of
+// its two 16-element blocks, each scaled by block scale x 2^(h exponent).
+template <int FMT, int NT>
+__device__ __forceinline__ void dn_piece(const uint8_t* st, const SG& g, int c, int s, int row,
+                                         const uint8_t* ob, const int8_t* hx, float (&part)[kTB]) {
+  const uint4 w = lds<uint4>(wptr16(st, g.kb, row, s));
+  uint32_t wd[16];
+  uint32_t o[4];
+  e2m1x8_to_f16x2x4(w.x, o);
+  wd[0] = o[0]; wd[1] = o[1]; wd[2] = o[2]; wd[3] = o[3];
+  e2m1x8_to_f16x2x4(w.y, o);
+  wd[4] = o[0]; wd[5] = o[1]; wd[6] = o[2]; wd[7] = o[3];
+  e2m1x8_to_f16x2x4(w.z, o);
+  wd[8] = o[0]; wd[9] = o[1]; wd[10] = o[2]; wd[11] = o[3];
+  e2m1x8_to_f16x2x4(w.w, o);
+  wd[12] = o[0]; wd[13] = o[1]; wd[14] = o[2]; wd[15] = o[3];
+  float f0, f1;
+  if (FMT == FMT_NVFP4) {
+    const uint8_t* sa = (g.scale_mode == SCALES_TMAP)
+                            ? sptr(st, g, 0, row, 2 * s)
+                            : st + g.scale_off + row * g.sr + (c * g.Kc + s * 32) / 16;
+    const float2 sc = f16x2_to_f32x2(e4m3x2_to_f16x2(lds<uint16_t>(sa)));
+    f0 = sc.x * pow2i(hx[2 * s]);
+    f1 = sc.y * pow2i(hx[2 * s + 1]);
   } else {
+    const uint8_t* sa = (g.scale_mode == SCALES_TMAP)
+                            ? sptr(st, g, 0, row, s)
+                            : st + g.scale_off + row * g.sr + (c * g.Kc + s * 32) / 32;
+    const float sc = e8m0_to_f32(lds<uint8_t>(sa));
+    f0 = sc * pow2i(hx[2 * s]);
+    f1 = sc * pow2i(hx[2 * s + 1]);
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const uint8_t* oa = ob + t * g.Kc * 2 + s * 64;
+    uint32_t xo[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 x = lds<uint4>(oa + q * 16);
+      xo[4 * q + 0] = x.x; xo[4 * q + 1] = x.y; xo[4 * q + 2] = x.z; xo[4 * q + 3] = x.w;
+    }
+    // four independent f16x2 chains of four
+    uint32_t q0 = hmul2(wd[0], xo[0]), q1 = hmul2(wd[4], xo[4]);
+    uint32_t q2 = hmul2(wd[8], xo[8]), q3 = hmul2(wd[12], xo[12]);
+#pragma unroll
+    for (int e = 1; e < 4; ++e) {
+      q0 = hfma2(wd[e], xo[e], q0);
+      q1 = hfma2(wd[4 + e], xo[4 + e], q1);
+      q2 = hfma2(wd[8 + e], xo[8 + e], q2);
+      q3 = hfma2(wd[12 + e], xo[12 + e], q3);
+    }
+    const float2 a = f16x2_to_f32x2(q0), a1 = f16x2_to_f32x2(q1);
+    const float2 b = f16x2_to_f32x2(q2), b1 = f16x2_to_f32x2(q3);
+    part[t] = fmaf((a.x + a.y) + (a1.x + a1.y), f0, part[t]);
+    part[t] = fmaf((b.x + b.y) + (b1.x + b1.y), f1, part[t]);
+  }
+}
+
+// One chunk of a routed down job: 16 weight rows (row = lane & 15) against
+// the f16 h of NT tokens; the half-warp covers 16-byte pieces [p0, p1) of the
+// chunk, two pieces in flight (independent partial sums).
+template <int FMT, int NT>
+__device__ __forceinline__ void compute_dn_fp4(const uint8_t* st, const SG& g, int c, int p0,
+                                               int p1, int row, float (&acc)[kTB]) {
+  const uint8_t* ob = st + g.opnd_off;
+  const int8_t* hx = reinterpret_cast<const int8_t*>(st + g.hx_off);
+  float pa[kTB], pb[kTB];
+#pragma unroll
+  for (int t = 0; t < kTB; ++t) pa[t] = pb[t] = 0.f;
+  int s = p0;
+  for (; s + 1 < p1; s += 2) {
+    dn_piece<FMT, NT>(st, g, c, s, row, ob, hx, pa);
+    dn_piece<FMT, NT>(st, g, c, s + 1, row, ob, hx, pb);
+  }
+  if (s < p1) dn_piece<FMT, NT>(st, g, c, s, row, ob, hx, pa);
+#pragma unroll
+  for (int t = 0; t < kTB; ++t) acc[t] += pa[t] + pb[t];
+}
+
+// One chunk of a shared-expert down job: BF16 weights against BF16 h; a step
+// is 32 elements (64 bytes) of the row, the half-warp covers steps [p0, p1).
+template <int NT>
+__device__ __forceinline__ void compute_dn_bf16(const uint8_t* st, const SG& g, int p0, int p1,
+                                                int row, float (&acc)[kTB]) {
+  const uint8_t* ob = st + g.opnd_off;
+  for (int s = p0; s < p1; ++s) {
+    uint32_t wv[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = lds<uint4>(wptr16(st, g.kb, row, s * 4 + q));
+      wv[4 * q + 0] = w.x; wv[4 * q + 1] = w.y; wv[4 * q + 2] = w.z; wv[4 * q + 3] = w.w;
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const uint8_t* oa = ob + t * g.Kc * 2 + s * 64;
+      uint32_t xo[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 x = lds<uint4>(oa + q * 16);
+        xo[4 * q + 0] = x.x; xo[4 * q + 1] = x.y; xo[4 * q + 2] = x.z; xo[4 * q + 3] = x.w;
+      }
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; e += 2) {
+        a0 = fma2_bf16_to_f32(wv[e], xo[e], a0);
+        a1 = fma2_bf16_to_f32(wv[e + 1], xo[e + 1], a1);
+      }
+      acc[t] += a0 + a1;
+    }
+  }
+}
+
+// ---------------------------------------------------------- gate/up epilogue
+// Epilogue of one gate/up row group, by the epilogue warp: reduce the compute
+// warps' partial sums (`red`, layout [warp][proj][token][lane]) and store h.
+// Shared expert: BF16 h of 32 rows.  Routed: lanes 0-15 of the tile are gate
+// rows, 16-31 up rows; h = SiLU(g)*u for the 16 rows, stored as f16 times
+// 2^-e with e chosen from the group's largest |h| (max in [64, 128)).
+template <int KIND>
+__device__ __forceinline__ void rg_epilogue(const Params& p, const Tables& tb, const RG& r,
+                                            const float* red, int lane) {
+  if (KIND == KIND_AS) {
     for (int t = 0; t < r.nt; ++t) {
-      const int n = r.tb * kTB + t;
-      const float* src = p.hs + (size_t)n * p.Is;
-      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(hbuf) + (size_t)t * K;
-      for (int kk = ctid * 4; kk < K; kk += kConsumerThreads * 4) {
-        const float4 v = ld_cg_f32x4(src + kk);
-        *reinterpret_cast<__nv_bfloat162*>(dst + kk) = __floats2bfloat162_rn(v.x, v.y);
-        *reinterpret_cast<__nv_bfloat162*>(dst + kk + 2) = __floats2bfloat162_rn(v.z, v.w);
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        s0 += red[((w * 2 + 0) * kTB + t) * 32 + lane];
+        s1 += red[((w * 2 + 1) * kTB + t) * 32 + lane];
+      }
+      const int n = rg_token<KIND>(tb, r, t);
+      const __nv_bfloat16 hb = __float2bfloat16_rn(silu(s0) * s1);
+      p.hs[(size_t)n * p.Is + r.rg * kRows + lane] = *reinterpret_cast<const uint16_t*>(&hb);
+    }
+  } else if (lane < 16) {
+    const int j = lane;
+    const float g2 = tb.s2[0][r.u], u2 = tb.s2[1][r.u];
+    float h[kTB];
+    float m = 0.f;
+#pragma unroll
+    for (int t = 0; t < kTB; ++t) {
+      h[t] = 0.f;
+      if (t < r.nt) {
+        float g = 0.f, u = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          g += red[((w * 2) * kTB + t) * 32 + j];
+          u += red[((w * 2) * kTB + t) * 32 + 16 + j];
+        }
+        const float xs = ldexpf(1.0f, tb.xe[rg_token<KIND>(tb, r, t)]);
+        g *= xs * g2;
+        u *= xs * u2;
+        h[t] = silu(g) * u;
+        m = fmaxf(m, fabsf(h[t]));
       }
     }
-  }
-  consumer_sync();
-}
-
-// Row-block completion for the down phase: every CTA, after its last down row
-// group, publishes its red.adds (fence), bumps the counter of each 32-row
-// output block it added to, and casts the blocks it completed to BF16.
-__device__ __noinline__ void flush_row_blocks(const Params& p, Tables& tb, int ctid,
-                                              uint32_t b_units) {
-  __threadfence();
-  consumer_sync();
-  const int nb = tb.nbrg;
-  const bool ab = aborted(tb);
-  for (int i = ctid; i < nb; i += kConsumerThreads) {
-    int fin = 0;
-    if (!ab) {
-      const uint32_t old = atomicAdd(p.rbcnt + tb.brg[i], 1u);
-      fin = (old + 1u == b_units);
-      if (fin) __threadfence();
-    }
-    tb.bfin[i] = (uint8_t)fin;
-  }
-  consumer_sync();
-  for (int i = 0; i < nb; ++i) {
-    if (!tb.bfin[i]) continue;
-    const int rb = tb.brg[i];
-    for (int j = ctid; j < p.N * kRows; j += kConsumerThreads) {
-      const int n = j / kRows, row = rb * kRows + (j % kRows);
-      const float v = ld_cg_f32(p.acc + (size_t)n * p.H + row);
-      const __nv_bfloat16 b = __float2bfloat16_rn(v);
-      p.out[(size_t)n * p.H + row] = *reinterpret_cast<const uint16_t*>(&b);
-    }
-  }
-  consumer_sync();
-  if (ctid == 0) tb.nbrg = 0;
-  consumer_sync();
-}
-
-// Reduce the 8 warps' partial sums of an RG (already in `red`) and apply the
-// epilogue of its kind.
-// Per-thread epilogue factors of an RG (thread ctid < nt*32 serves token
-// ctid/32), loaded when the RG starts so their latency hides behind the
-// stage compute: gate/up scales for AR, output weight for BR/BS.
-template <int KIND>
-__device__ __forceinline__ float2 epi_factors(const Params& p, const Tables& tb, const RG& r,
-                                              int ctid) {
-  float2 f = make_float2(1.f, 1.f);
-  if (ctid >= r.nt * 32) return f;
-  const int t = ctid >> 5;
-  const int n = rg_token<KIND>(tb, r, t);
-  if (KIND == KIND_AR) {
-    const float xs = ldexpf(1.0f, ld_cg_s32(p.xexp + n));
-    f.x = xs * (p.g2 ? __ldg(p.g2 + r.e) : 1.0f);
-    f.y = xs * (p.u2 ? __ldg(p.u2 + r.e) : 1.0f);
-  } else if (KIND == KIND_BR) {
-    f.x = ldexpf(1.0f, tb.hexp[t]) * (p.d2 ? __ldg(p.d2 + r.e) : 1.0f) *
-          tb.uw[tb.hoff[r.u] + r.tb * kTB + t];
-  } else if (KIND == KIND_BS) {
-    f.x = ld_cg_f32(p.gsig + n);
-  }
-  return f;
-}
-
-template <int KIND>
-__device__ __noinline__ void rg_epilogue(const Params& p, Tables& tb, const RG& r,
-                                         const float* red, int ctid, uint32_t b_units, float2 ef) {
-  const Geo& g = p.geo[KIND];
-  if (ctid < r.nt * 32 && !aborted(tb)) {
-    const int t = ctid >> 5, j = ctid & 31;
-    float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      s0 += red[((w * 2 + 0) * kTB + t) * 32 + j];
-      if (g.nproj == 2) s1 += red[((w * 2 + 1) * kTB + t) * 32 + j];
-    }
-    const int row = r.rg * kRows + j;
-    const int n = rg_token<KIND>(tb, r, t);
-    if (KIND == KIND_AR) {
-      p.h[(size_t)(tb.hoff[r.u] + r.tb * kTB + t) * p.inter + row] = silu(s0 * ef.x) * (s1 * ef.y);
-    } else if (KIND == KIND_AS) {
-      p.hs[(size_t)n * p.Is + row] = silu(s0) * s1;
-    } else {
-      red_add_f32(p.acc + (size_t)n * p.H + row, s0 * ef.x);
-    }
-  }
-  consumer_sync();
-  if (KIND == KIND_BR || KIND == KIND_BS) {
-    if (ctid == 0) {
-      tb.brg[tb.nbrg] = (uint16_t)r.rg;
-      tb.nbrg = tb.nbrg + 1;
-    }
-    consumer_sync();
-    if (tb.nbrg == kMaxRgList) flush_row_blocks(p, tb, ctid, b_units);
+    for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0x0000ffffu, m, o));
+    const int e = min(max(scale_exponent(m), -126), 127);
+    const float sc = pow2i(-e);
+    const int slot0 = tb.hoff[r.u] + r.tb * kTB;
+#pragma unroll
+    for (int t = 0; t < kTB; ++t)
+      if (t < r.nt)
+        p.h16[(size_t)(slot0 + t) * p.inter + r.rg * kDnRows + j] =
+            __half_as_ushort(__float2half_rn(h[t] * sc));
+    if (j == 0) p.hexp[(size_t)r.unit * p.hstride + r.rg] = (int8_t)e;
   }
 }
 
-// Streams the chunks of one RG for NT tokens and leaves the 8 warps' partial
-// sums in `red` (layout [warp][proj][token][lane]).
+// The epilogue warp's loop over one gate/up kind's row groups (same order as
+// the compute warps); routed groups are then published to the units'
+// readiness counters (release: every lane's h stores, the warp barrier, lane
+// 0's fence and counts).  Returns the number of row groups, or -1 on abort.
+template <int KIND>
+__device__ __noinline__ int epilogue_kind(const Params& p, Tables& tb, const ConsumerCtx cx,
+                                          int cta, int G, int* rgk_io, int lane) {
+  if (kind_units<KIND>(p, tb) == 0) return 0;
+  int lo, hi;
+  kind_range<KIND>(p, tb, cta, G, lo, hi);
+  int kk = *rgk_io;
+  for (int gi = lo; gi < hi; ++gi, ++kk) {
+    const RG r = decode_rg<KIND>(p, tb, gi);
+    const int buf = kk & 1;
+    bool ok = !aborted(tb) && mbar_wait_bounded(cx.rfull + buf, (uint32_t)(kk >> 1) & 1u,
+                                                 p.timeout_ns);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) {
+      if (lane == 0 && !aborted(tb)) set_abort(p, tb, kErrTimeoutStage);
+      return -1;
+    }
+    rg_epilogue<KIND>(p, tb, r, cx.red + buf * kRedFloats, lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(cx.rempty + buf);
+  }
+  *rgk_io = kk;
+  if (KIND == KIND_AR && lane == 0 && lo < hi) {
+    const int rpu = p.inter / kDnRows;
+    __threadfence();
+    for (int u = lo / rpu; u <= (hi - 1) / rpu; ++u)
+      atomicAdd(p.ready + u, (uint32_t)(min(hi, (u + 1) * rpu) - max(lo, u * rpu)));
+  }
+  return hi - lo;
+}
+
+// Streams the chunks of one gate/up row group for NT tokens and leaves the 8
+// warps' partial sums in `red` (layout [warp][proj][token][lane]).
 template <int FMT, int NPROJ, int KIND, int NT>
 __device__ __forceinline__ void consume_rg(const Params& p, Tables& tb, const ConsumerCtx& cx,
-                                           const SG& g, int& ctr, int warp, int lane) {
+                                           const SG& g, int& ctr, int warp, int lane, float* red) {
   constexpr int kStepBytes = (FMT == FMT_BF16) ? 64 : 16;
   float acc[NPROJ][NT];
 #pragma unroll
@@ -936,15 +1237,8 @@ __device__ __forceinline__ void consume_rg(const Params& p, Tables& tb, const Co
       const uint8_t* st = cx.ring_base + (size_t)slot * cx.stage_bytes;
       const int ns = min(kChunkBytes, g.kb - c * kChunkBytes) / kStepBytes;
       const int s0 = warp * ns / kConsumerWarps, s1 = (warp + 1) * ns / kConsumerWarps;
-      const uint8_t* ob;
-      int ots;
-      if (KIND == KIND_AS || KIND == KIND_AR) {
-        ob = st + g.opnd_off;
-        ots = g.Kc * 2;
-      } else {
-        ob = cx.hbuf + c * g.Kc * 2;
-        ots = g.K * 2;
-      }
+      const uint8_t* ob = st + g.opnd_off;
+      const int ots = g.Kc * 2;
       if (FMT == FMT_BF16) compute_bf16<NPROJ, NT>(st, g, ob, ots, s0, s1, lane, acc);
       else compute_fp4<FMT, NPROJ, NT>(st, g, c, ob, ots, s0, s1, lane, acc);
     }
@@ -954,38 +1248,132 @@ __device__ __forceinline__ void consume_rg(const Params& p, Tables& tb, const Co
 #pragma unroll
   for (int pj = 0; pj < NPROJ; ++pj)
 #pragma unroll
-    for (int t = 0; t < NT; ++t) cx.red[((warp * 2 + pj) * kTB + t) * 32 + lane] = acc[pj][t];
+    for (int t = 0; t < NT; ++t) red[((warp * 2 + pj) * kTB + t) * 32 + lane] = acc[pj][t];
 }
 
-// Consumes every stage of one kind's row groups.
+// Compute warps: every stage of one gate/up kind's row groups; each group's
+// partial sums go to one of two buffers that the epilogue warp finishes.
 template <int FMT, int NPROJ, int KIND>
 __device__ __noinline__ void consume_kind(const Params& p, Tables& tb, const ConsumerCtx cx,
-                                          int cta, int G, int* ctr_io, int ctid, uint32_t b_units) {
+                                          int cta, int G, int* ctr_io, int* rgk_io, int ctid) {
   if (kind_units<KIND>(p, tb) == 0) return;
   const int warp = ctid >> 5, lane = ctid & 31;
   int lo, hi;
   kind_range<KIND>(p, tb, cta, G, lo, hi);
   const SG g = load_sg(p.geo[KIND]);
-  int ctr = *ctr_io;
-  for (int gi = lo; gi < hi; ++gi) {
+  int ctr = *ctr_io, kk = *rgk_io;
+  for (int gi = lo; gi < hi; ++gi, ++kk) {
     const RG r = decode_rg<KIND>(p, tb, gi);
-    if ((KIND == KIND_BR || KIND == KIND_BS) && (tb.hb_kind != KIND || tb.hb_unit != r.unit)) {
-      if (!aborted(tb)) stage_hbuf<KIND>(p, tb, r, cx.hbuf, ctid);
-      if (ctid == 0) {
-        tb.hb_kind = KIND;
-        tb.hb_unit = r.unit;
-      }
-      consumer_sync();
-    }
-    const float2 ef = epi_factors<KIND>(p, tb, r, ctid);
+    const int buf = kk & 1;
+    // the buffer's previous group (kk - 2) must be finished by the epilogue warp
+    if (!aborted(tb) &&
+        !mbar_wait_bounded(cx.rempty + buf, ((uint32_t)(kk >> 1) & 1u) ^ 1u, p.timeout_ns) &&
+        lane == 0)
+      set_abort(p, tb, kErrTimeoutStage);
+    float* red = cx.red + buf * kRedFloats;
     switch (r.nt) {
-      case 1: consume_rg<FMT, NPROJ, KIND, 1>(p, tb, cx, g, ctr, warp, lane); break;
-      case 2: consume_rg<FMT, NPROJ, KIND, 2>(p, tb, cx, g, ctr, warp, lane); break;
-      case 3: consume_rg<FMT, NPROJ, KIND, 3>(p, tb, cx, g, ctr, warp, lane); break;
-      default: consume_rg<FMT, NPROJ, KIND, 4>(p, tb, cx, g, ctr, warp, lane); break;
+      case 1: consume_rg<FMT, NPROJ, KIND, 1>(p, tb, cx, g, ctr, warp, lane, red); break;
+      case 2: consume_rg<FMT, NPROJ, KIND, 2>(p, tb, cx, g, ctr, warp, lane, red); break;
+      case 3: consume_rg<FMT, NPROJ, KIND, 3>(p, tb, cx, g, ctr, warp, lane, red); break;
+      default: consume_rg<FMT, NPROJ, KIND, 4>(p, tb, cx, g, ctr, warp, lane, red); break;
     }
-    consumer_sync();
-    rg_epilogue<KIND>(p, tb, r, cx.red, ctid, b_units, ef);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(cx.rfull + buf);
+  }
+  *ctr_io = ctr;
+  *rgk_io = kk;
+}
+
+// Down jobs of this CTA's output blocks (same order as produce_down).  With
+// J jobs per block and W consumer warps, a job belongs to S = W / J (a power
+// of two, at least 1) consecutive warps, each taking one K slice per
+// half-warp; every warp passes every stage (the ring's release count is W),
+// only the owners compute.  Each owner adds its routing-weighted partial into
+// the block accumulator in shared memory.
+template <int FMT>
+__device__ __noinline__ void consume_down(const Params& p, Tables& tb, const ConsumerCtx cx,
+                                          int cta, int G, int* ctr_io, int ctid) {
+  const int warp = ctid >> 5, lane = ctid & 31, row = lane & 15, half = lane >> 4;
+  const int nrbl = dn_blocks(p, cta, G);
+  const int nr = tb.n_units, nsh = p.Is > 0 ? (p.N + kTB - 1) / kTB : 0, J = nr + nsh;
+  if (nrbl == 0 || J == 0) return;
+  const SG gr = load_sg(p.geo[KIND_BR]);
+  const SG gsh = load_sg(p.geo[nsh ? KIND_BS : KIND_BR]);
+  int S = 1;
+  while (S * 2 * J <= kConsumerWarps) S *= 2;
+  int ctr = *ctr_io;
+  int q = 0;
+  for (int i = 0; i < nrbl; ++i) {
+    for (int jb = 0; jb < J; ++jb, ++q) {
+      const int w0 = (q * S) & (kConsumerWarps - 1);
+      const bool own = warp >= w0 && warp < w0 + S;
+      const int slice = (warp - w0) * 2 + half, nslice = 2 * S;
+      const bool routed = jb < nr;
+      const SG& g = routed ? gr : gsh;
+      int nt, src0, e = 0;
+      if (routed) {
+        const int u = tb.unit_u[jb], tbi = tb.unit_tb[jb];
+        nt = min(kTB, (int)tb.ucnt[u] - tbi * kTB);
+        src0 = tb.hoff[u] + tbi * kTB;
+        e = tb.uexp[u];
+      } else {
+        const int b = jb - nr;
+        nt = min(kTB, p.N - b * kTB);
+        src0 = b * kTB;
+      }
+      float acc[kTB];
+#pragma unroll
+      for (int t = 0; t < kTB; ++t) acc[t] = 0.f;
+      for (int c = 0; c < g.nchunks; ++c) {
+        const int slot = ctr % cx.nstages;
+        const uint32_t round = (uint32_t)(ctr / cx.nstages);
+        ++ctr;
+        bool ok = !aborted(tb);
+        if (ok) ok = mbar_wait_bounded(cx.full + slot, round & 1u, p.timeout_ns);
+        if (!ok) {
+          if (lane == 0 && !aborted(tb)) set_abort(p, tb, kErrTimeoutStage);
+        } else if (own) {
+          const uint8_t* st = cx.ring_base + (size_t)slot * cx.stage_bytes;
+          const int rb = min(kChunkBytes, g.kb - c * kChunkBytes);
+          if (routed) {
+            const int np = rb / 16;
+            const int p0 = slice * np / nslice, p1 = (slice + 1) * np / nslice;
+            switch (nt) {
+              case 1: compute_dn_fp4<FMT, 1>(st, g, c, p0, p1, row, acc); break;
+              case 2: compute_dn_fp4<FMT, 2>(st, g, c, p0, p1, row, acc); break;
+              case 3: compute_dn_fp4<FMT, 3>(st, g, c, p0, p1, row, acc); break;
+              default: compute_dn_fp4<FMT, 4>(st, g, c, p0, p1, row, acc); break;
+            }
+          } else {
+            const int np = rb / 64;
+            const int p0 = slice * np / nslice, p1 = (slice + 1) * np / nslice;
+            switch (nt) {
+              case 1: compute_dn_bf16<1>(st, g, p0, p1, row, acc); break;
+              case 2: compute_dn_bf16<2>(st, g, p0, p1, row, acc); break;
+              case 3: compute_dn_bf16<3>(st, g, p0, p1, row, acc); break;
+              default: compute_dn_bf16<4>(st, g, p0, p1, row, acc); break;
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cx.empty + slot);
+      }
+      if (own && !aborted(tb)) {
+#pragma unroll
+        for (int t = 0; t < kTB; ++t) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], 16);
+        if (lane < 16) {
+          const float d2 = routed ? tb.s2[2][tb.unit_u[jb]] : 1.0f;
+#pragma unroll
+          for (int t = 0; t < kTB; ++t) {
+            if (t < nt) {
+              const int n = routed ? tb.utok[src0 + t] : src0 + t;
+              const float wgt = routed ? tb.uw[src0 + t] * d2 : ld_cg_f32(p.gsig + n);
+              atomicAdd(cx.sacc + ((size_t)i * p.N + n) * kDnRows + row, acc[t] * wgt);
+            }
+          }
+        }
+      }
+    }
   }
   *ctr_io = ctr;
 }
@@ -1002,6 +1390,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
   uint64_t* full = bars;
   uint64_t* empty = bars + kMaxStages;
   uint64_t* rr = bars + 2 * kMaxStages;  // routing tables ready (consumers -> producer)
+  uint64_t* rfull = rr + 1;
+  uint64_t* rempty = rr + 3;
   const int tid = threadIdx.x;
   const int cta = blockIdx.x, G = gridDim.x;
 
@@ -1011,24 +1401,50 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
       mbar_init(empty + s, kConsumerWarps);
     }
     mbar_init(rr, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(rfull + i, kConsumerWarps);
+      mbar_init(rempty + i, 1);
+    }
     fence_mbar_init();
     tb.abort = 0;
-    tb.hb_kind = -1;
-    tb.hb_unit = -1;
     tb.n_units = 0;
     tb.U = 0;
-    tb.nbrg = 0;
   }
   __syncthreads();
 
+  float* red = reinterpret_cast<float*>(smem + p.smem_red_off);
+  float* sacc = reinterpret_cast<float*>(smem + p.smem_sacc_off);
+  ConsumerCtx cx{smem + p.smem_ring_off, full, empty, p.nstages, p.stage_bytes, red, sacc,
+                 rfull, rempty};
+
+  if ((tid >> 5) == kEpiWarp) {
+    // ------------------------------------------------------ epilogue warp
+    if (p.route_only) return;
+    const int lane = tid & 31;
+    int kk = 0;
+    const int as_done = epilogue_kind<KIND_AS>(p, tb, cx, cta, G, &kk, lane);
+    bool ok = as_done >= 0 && mbar_wait_bounded(rr, 0, p.timeout_ns);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok || aborted(tb)) return;
+    // shared-expert h rows of this CTA are complete; the readiness counters
+    // were zeroed everywhere before B1, which the routing (rr) came after
+    __syncwarp();
+    if (lane == 0 && as_done > 0) {
+      __threadfence();
+      atomicAdd(p.ready + kReadyAS, (uint32_t)as_done);
+    }
+    epilogue_kind<KIND_AR>(p, tb, cx, cta, G, &kk, lane);
+    return;
+  }
   if (tid >= kConsumerThreads) {
-    // -------------------------------------------------- producer (one thread)
-    if (tid != kConsumerThreads || p.route_only) return;
-    for (int i = 0; i < TM_COUNT; ++i)
+    // ------------------------------- producers (lane 0 of each producer warp)
+    if ((tid & 31) != 0 || p.route_only) return;
+    const int pid = (tid - kConsumerThreads - 32) >> 5;
+    for (int i = pid; i < TM_COUNT; i += kProducers)
       if (p.tm_valid & (1u << i)) prefetch_tensormap(&p.tm[i]);
     Ring ring{smem + p.smem_ring_off, full, empty, p.nstages, p.stage_bytes};
     int ctr = 0;
-    bool ok = produce_kind<KIND_AS>(p, tb, ring, cta, G, &ctr);
+    bool ok = produce_kind<KIND_AS>(p, tb, ring, cta, G, &ctr, pid);
     if (ok && !mbar_wait_bounded(rr, 0, p.timeout_ns)) {
       set_abort(p, tb, kErrTimeoutProducer);
       ok = false;
@@ -1036,40 +1452,35 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
     if (ok && aborted(tb)) ok = false;
     if (ok) {
       fence_proxy_async_global();   // x16 was written by other CTAs before B1
-      ok = produce_kind<KIND_AR>(p, tb, ring, cta, G, &ctr) &&
-           produce_kind<KIND_BR>(p, tb, ring, cta, G, &ctr) &&
-           produce_kind<KIND_BS>(p, tb, ring, cta, G, &ctr);
+      ok = produce_kind<KIND_AR>(p, tb, ring, cta, G, &ctr, pid) &&
+           produce_down(p, tb, ring, cta, G, &ctr, pid);
     }
     if (!ok) {
       // drain: wait (bounded) for copies still in flight into our stages
       const int first = ctr > p.nstages ? ctr - p.nstages : 0;
       for (int i = first; i < ctr; ++i)
-        mbar_wait_bounded(full + (i % p.nstages), (uint32_t)(i / p.nstages) & 1u, p.timeout_ns);
+        if (i % kProducers == pid)
+          mbar_wait_bounded(full + (i % p.nstages), (uint32_t)(i / p.nstages) & 1u, p.timeout_ns);
     }
     return;
   }
 
   // -------------------------------------------------------------- consumers
   const int ctid = tid;
-  float* red = reinterpret_cast<float*>(smem + p.smem_red_off);
-  ConsumerCtx cx{smem + p.smem_ring_off, full, empty, p.nstages, p.stage_bytes, red,
-                 smem + p.smem_hbuf_off};
   unsigned long long base = 0;
   if (ctid == 0) {
     const unsigned long long c0 = ld_relaxed_u64(&p.ctrl->arrivals);
-    base = c0 - c0 % (2ull * (unsigned long long)G);
+    base = c0 - c0 % (unsigned long long)G;
   }
 
-  // P0: router, token prep, zero the accumulator
+  // P0: router, token prep, zero the readiness counters and the block accumulator
   router_phase(p, cta, G, tb, ctid);
+  const int nrbl = p.route_only ? 0 : dn_blocks(p, cta, G);
   if (!p.route_only) {
     token_prep(p, cta, G, tb, ctid);
-    const size_t nacc = (size_t)p.N * p.H;
-    for (size_t i = (size_t)cta * kConsumerThreads + ctid; i < nacc;
-         i += (size_t)G * kConsumerThreads)
-      p.acc[i] = 0.f;
-    for (int i = cta * kConsumerThreads + ctid; i < p.H / kRows; i += G * kConsumerThreads)
-      p.rbcnt[i] = 0u;
+    for (int i = cta * kConsumerThreads + ctid; i <= kReadyAS; i += G * kConsumerThreads)
+      p.ready[i] = 0u;
+    for (int i = ctid; i < nrbl * p.N * kDnRows; i += kConsumerThreads) sacc[i] = 0.f;
   }
   consumer_sync();
   if (ctid == 0) {
@@ -1077,61 +1488,68 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
     grid_arrive(p.ctrl);    // B1
   }
 
-  int ctr = 0;
-  if (!p.route_only) consume_kind<FMT_BF16, 2, KIND_AS>(p, tb, cx, cta, G, &ctr, ctid, 0);
+  int ctr = 0, kk = 0;
+  if (!p.route_only) consume_kind<FMT_BF16, 2, KIND_AS>(p, tb, cx, cta, G, &ctr, &kk, ctid);
 
   if (ctid == 0 && !grid_wait(p.ctrl, base + (unsigned long long)G, p.timeout_ns))
     set_abort(p, tb, kErrTimeoutBarrier);
   consumer_sync();
   if (aborted(tb)) {
-    if (ctid == 0) {
-      grid_arrive(p.ctrl);  // keep two arrivals per call
-      mbar_arrive(rr);
-    }
+    if (ctid == 0) mbar_arrive(rr);
     return;   // the producer sees the abort and drains
   }
 
   // P1: routing
   routing_phase(p, cta == 0, tb, ctid);
-  if (p.route_only) {
-    if (ctid == 0) grid_arrive(p.ctrl);   // B2 arrival, nothing waits on it
-    return;
-  }
+  if (p.route_only) return;
   if (ctid == 0) mbar_arrive(rr);
 
-  const uint32_t b_units = (uint32_t)tb.n_units + ((p.Is > 0) ? (uint32_t)((p.N + kTB - 1) / kTB) : 0u);
-
-  // P2: routed gate/up
-  consume_kind<WF, 2, KIND_AR>(p, tb, cx, cta, G, &ctr, ctid, b_units);
-  __threadfence();
+  // P2: routed gate/up; P3: down jobs of the owned output blocks
+  consume_kind<WF, 1, KIND_AR>(p, tb, cx, cta, G, &ctr, &kk, ctid);
+  consume_down<WF>(p, tb, cx, cta, G, &ctr, ctid);
   consumer_sync();
-  if (ctid == 0) {
-    grid_arrive(p.ctrl);    // B2
-    if (!aborted(tb) && !grid_wait(p.ctrl, base + 2ull * (unsigned long long)G, p.timeout_ns))
-      set_abort(p, tb, kErrTimeoutBarrier);
+  if (aborted(tb)) return;
+  for (int idx = ctid; idx < nrbl * p.N * kDnRows; idx += kConsumerThreads) {
+    const int i = idx / (p.N * kDnRows), rem = idx - i * p.N * kDnRows;
+    const int n = rem / kDnRows, j = rem - n * kDnRows;
+    const __nv_bfloat16 b = __float2bfloat16_rn(sacc[idx]);
+    p.out[(size_t)n * p.H + (size_t)(cta + i * G) * kDnRows + j] =
+        *reinterpret_cast<const uint16_t*>(&b);
   }
-  consumer_sync();
-
-  // P3: down projections (routed, then shared) + row-block completion
-  consume_kind<WF, 1, KIND_BR>(p, tb, cx, cta, G, &ctr, ctid, b_units);
-  consume_kind<FMT_BF16, 1, KIND_BS>(p, tb, cx, cta, G, &ctr, ctid, b_units);
-  flush_row_blocks(p, tb, ctid, b_units);
 }
 
 // ------------------------------------------------------------------- host
 
-static bool plan_kind(Geo& g, int fmt, int nproj, int K, int rows, bool with_operand) {
+// Stage geometry of one kind: weight tiles, block scales, activation chunk.
+static bool plan_kind(Geo& g, int kind, int fmt, int K, int rows, int ntok) {
+  const int nproj = (kind == KIND_AS || kind == KIND_AR) ? 2 : 1;
   g.fmt = fmt;
   g.nproj = nproj;
+  g.brows = (kind == KIND_AS) ? kRows : kDnRows;
+  g.rg_rows = g.brows;
   g.K = K;
   g.rows_total = rows;
   g.opnd_off = -1;
-  if (K % 32 != 0 || rows % kRows != 0 || K <= 0 || rows <= 0) return false;
+  if (K % 32 != 0 || rows % g.rg_rows != 0 || K <= 0 || rows <= 0) return false;
   g.kb = (fmt == FMT_BF16) ? K * 2 : K / 2;
   g.Kc = (fmt == FMT_BF16) ? kChunkBytes / 2 : kChunkBytes * 2;
   g.nchunks = (g.kb + kChunkBytes - 1) / kChunkBytes;
-  int off = (g.kb >= kBoxBytes) ? nproj * kBoxesPerChunk * kBoxTileBytes : nproj * kRows * g.kb;
-  off = (off + 1023) / 1024 * 1024;
+  const bool sw = g.kb >= kBoxBytes;
+  // AS: one 32-row tile per projection; AR: gate and up 16-row boxes stacked
+  // into one 32-row tile; BR/BS: one 16-row tile
+  int wbytes;
+  if (kind == KIND_AS) {
+    g.tile_bytes = kBoxTileBytes;
+    wbytes = sw ? nproj * kBoxesPerChunk * kBoxTileBytes : nproj * kRows * g.kb;
+  } else if (kind == KIND_AR) {
+    g.tile_bytes = kDnRows * kBoxBytes;
+    wbytes = sw ? 2 * kBoxesPerChunk * kDnRows * kBoxBytes : kRows * g.kb;
+  } else {
+    g.tile_bytes = kDnRows * kBoxBytes;
+    wbytes = sw ? kBoxesPerChunk * kDnRows * kBoxBytes : kDnRows * g.kb;
+  }
+  g.use3d = (g.kb % kBoxBytes == 0) ? 1 : 0;   // whole 128-byte columns only
+  int off = (wbytes + 1023) / 1024 * 1024;
   g.scale_off = off;
   g.sr = g.scb = 0;
   g.scale_mode = SCALES_NONE;
@@ -1141,53 +1559,52 @@ static bool plan_kind(Geo& g, int fmt, int nproj, int K, int rows, bool with_ope
     if (g.sr % 16 == 0) {
       g.scale_mode = SCALES_TMAP;
       g.scb = std::min(g.Kc / gs, g.sr);
-      off += nproj * kRows * g.scb;
+      off += nproj * g.brows * g.scb;
     } else {
       g.scale_mode = SCALES_BLOCK;
-      off += nproj * kRows * g.sr;
+      off += nproj * g.brows * g.sr;
     }
     off = (off + 127) / 128 * 128;
   }
-  if (with_operand) {
-    g.opnd_off = off;
-    off += kTB * g.Kc * 2;
-  }
+  g.opnd_off = off;
+  off += ntok * g.Kc * 2;                  // activation chunk of up to ntok tokens
+  g.hx_off = off;
+  if (kind == KIND_BR) off += g.Kc / 16;   // h exponents of the chunk
   g.stage_bytes = (off + 1023) / 1024 * 1024;
   return true;
 }
 
-// Tables plus the reduction scratch; the ring needs 1024-byte alignment.
-bool plan_decode(Params& p, int smem_budget) {
+bool plan_decode(Params& p, int smem_budget, int grid) {
   const int wf = (p.fmt == 0) ? FMT_NVFP4 : FMT_MXFP4;
-  if (!plan_kind(p.geo[KIND_AR], wf, 2, p.H, p.inter, true)) return false;
-  if (!plan_kind(p.geo[KIND_BR], wf, 1, p.inter, p.H, false)) return false;
+  const int ntok = std::min(p.N, kTB);   // tokens per activation chunk
+  if (!plan_kind(p.geo[KIND_AR], KIND_AR, wf, p.H, p.inter, ntok)) return false;
+  if (!plan_kind(p.geo[KIND_BR], KIND_BR, wf, p.inter, p.H, ntok)) return false;
   int stage = std::max(p.geo[KIND_AR].stage_bytes, p.geo[KIND_BR].stage_bytes);
-  int hb = kTB * p.inter * 2;
   if (p.Is > 0) {
-    if (!plan_kind(p.geo[KIND_AS], FMT_BF16, 2, p.H, p.Is, true)) return false;
-    if (!plan_kind(p.geo[KIND_BS], FMT_BF16, 1, p.Is, p.H, false)) return false;
+    if (!plan_kind(p.geo[KIND_AS], KIND_AS, FMT_BF16, p.H, p.Is, ntok)) return false;
+    if (!plan_kind(p.geo[KIND_BS], KIND_BS, FMT_BF16, p.Is, p.H, ntok)) return false;
     stage = std::max(stage, std::max(p.geo[KIND_AS].stage_bytes, p.geo[KIND_BS].stage_bytes));
-    hb = std::max(hb, kTB * p.Is * 2);
   } else {
     p.geo[KIND_AS] = p.geo[KIND_AR];
     p.geo[KIND_BS] = p.geo[KIND_BR];
-    p.geo[KIND_AS].rows_total = kRows;
-    p.geo[KIND_BS].rows_total = kRows;
   }
-  const int red = kConsumerWarps * 2 * kTB * 32 * 4;
+  p.hstride = ((p.inter / kDnRows) + 15) / 16 * 16;
+  p.nrb = p.H / kDnRows;
+  p.nrb_cta = (p.nrb + grid - 1) / grid;
+  const int red = 2 * kRedFloats * 4;
+  const int sacc = ((p.nrb_cta * p.N * kDnRows * 4) + 127) / 128 * 128;
   const int tab = ((int)sizeof(Tables) + 127) / 128 * 128;
-  const int bars = (2 * kMaxStages + 1) * 8;
-  const int fixed = red + ((hb + 127) / 128 * 128) + tab + ((bars + 127) / 128 * 128);
+  const int bars = (2 * kMaxStages + 5) * 8;
+  const int fixed = red + sacc + tab + ((bars + 127) / 128 * 128);
   int ns = (smem_budget - fixed) / stage;
   if (ns > kMaxStages) ns = kMaxStages;
   if (ns < 2) return false;
   p.nstages = ns;
   p.stage_bytes = stage;
-  p.hbuf_bytes = hb;
   p.smem_ring_off = 0;
   p.smem_red_off = ns * stage;
-  p.smem_hbuf_off = p.smem_red_off + red;
-  p.smem_tab_off = p.smem_hbuf_off + (hb + 127) / 128 * 128;
+  p.smem_sacc_off = p.smem_red_off + red;
+  p.smem_tab_off = p.smem_sacc_off + sacc;
   p.smem_bar_off = p.smem_tab_off + tab;
   p.smem_total = p.smem_bar_off + (bars + 127) / 128 * 128;
   return p.smem_total <= smem_budget;

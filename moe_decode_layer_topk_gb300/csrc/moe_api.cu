@@ -27,7 +27,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct WsLayout {
-  size_t ctrl, logits, x16, xexp, gsig, h, hs, acc, rbcnt, total;
+  size_t ctrl, logits, x16, xexp, gsig, h16, hexp, hs, ready, total;
 };
 
 WsLayout ws_layout(const moe_layer_desc_t& d, int32_t N) {
@@ -43,10 +43,11 @@ WsLayout ws_layout(const moe_layer_desc_t& d, int32_t N) {
   L.x16 = take((size_t)N * d.H * 2);
   L.xexp = take((size_t)N * 4);
   L.gsig = take((size_t)N * 4);
-  L.h = take((size_t)N * d.top_k * d.inter * 4);
-  L.hs = take((size_t)N * std::max(d.shared_inter, 0) * 4);
-  L.acc = take((size_t)N * d.H * 4);
-  L.rbcnt = take((size_t)(d.H / 32) * 4);
+  const size_t S = (size_t)N * d.top_k;
+  L.h16 = take(S * d.inter * 2);
+  L.hexp = take(S * (size_t)(((d.inter / 16) + 15) / 16 * 16));   // units <= S
+  L.hs = take((size_t)N * std::max(d.shared_inter, 0) * 2);
+  L.ready = take((size_t)(moe::kMaxSlots + 1) * 4);
   L.total = off;
   return L;
 }
@@ -221,13 +222,52 @@ bool encode_2d(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t rows,
   return true;
 }
 
-// Weight-row map of one projection (packed FP4 or BF16 bytes).
+// 3D view of weight rows: [column of 128 bytes][row][byte], boxes of 4
+// columns x brows rows x 128 bytes (128-byte swizzle); rows must be whole
+// columns (kb % 128 == 0) so no box reaches past a row or the tensor.
+bool encode_3d(CUtensorMap* out, const void* ptr, uint64_t kb, uint64_t rows, uint32_t brows) {
+  constexpr uint32_t kKey3d = 0x3D3Du;   // cache key marker of the 3D views
+  const TmKey key{ptr, kb, rows, kKey3d, brows, 128};
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& e : g_tm_cache)
+    if (e.used && e.key == key) {
+      *out = e.map;
+      return true;
+    }
+  if (!g_encode) return false;
+  cuuint64_t dims[3] = {128, rows, kb / 128};
+  cuuint64_t strides[2] = {kb, 128};
+  cuuint32_t boxd[3] = {128, brows, (cuuint32_t)moe::kBoxesPerChunk};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUtensorMap m;
+  if (g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, boxd,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  TmEntry& e = g_tm_cache[g_tm_next];
+  g_tm_next = (g_tm_next + 1) % kTmCache;
+  e.key = key;
+  e.map = m;
+  e.used = true;
+  *out = m;
+  return true;
+}
+
+// Weight-row map of one projection (packed FP4 or BF16 bytes), boxes of
+// g.brows rows; plus its 3D view when the stage loads whole chunks.
 bool encode_rows(moe::Params& p, int slot, const void* ptr, const moe::Geo& g, uint64_t rows) {
   const bool sw = g.kb >= moe::kBoxBytes;
   if (!encode_2d(&p.tm[slot], ptr, (uint64_t)g.kb, rows, sw ? moe::kBoxBytes : (uint32_t)g.kb,
-                 sw ? 128 : 0))
+                 sw ? 128 : 0, (uint32_t)g.brows))
     return false;
   p.tm_valid |= 1u << slot;
+  if (g.use3d) {
+    const int s3 = slot == moe::TM_GQ ? moe::TM3_GQ : slot == moe::TM_UQ ? moe::TM3_UQ
+                 : slot == moe::TM_DQ ? moe::TM3_DQ : slot == moe::TM_SG ? moe::TM3_SG
+                 : slot == moe::TM_SU ? moe::TM3_SU : moe::TM3_SD;
+    if (!encode_3d(&p.tm[s3], ptr, (uint64_t)g.kb, rows, (uint32_t)g.brows)) return false;
+    p.tm_valid |= 1u << s3;
+  }
   return true;
 }
 
@@ -235,7 +275,8 @@ bool encode_rows(moe::Params& p, int slot, const void* ptr, const moe::Geo& g, u
 // rows are swizzled so the kernel's per-lane scale loads avoid bank conflicts.
 bool encode_scales(moe::Params& p, int slot, const void* ptr, const moe::Geo& g, uint64_t rows) {
   if (g.scale_mode != moe::SCALES_TMAP) return true;
-  if (!encode_2d(&p.tm[slot], ptr, (uint64_t)g.sr, rows, (uint32_t)g.scb, g.scb == 64 ? 64 : 0))
+  if (!encode_2d(&p.tm[slot], ptr, (uint64_t)g.sr, rows, (uint32_t)g.scb, g.scb == 64 ? 64 : 0,
+                 (uint32_t)g.brows))
     return false;
   p.tm_valid |= 1u << slot;
   return true;
@@ -393,12 +434,12 @@ moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* 
   p.x16 = reinterpret_cast<uint16_t*>(b + L.x16);
   p.xexp = reinterpret_cast<int*>(b + L.xexp);
   p.gsig = reinterpret_cast<float*>(b + L.gsig);
-  p.h = reinterpret_cast<float*>(b + L.h);
-  p.hs = reinterpret_cast<float*>(b + L.hs);
-  p.acc = reinterpret_cast<float*>(b + L.acc);
-  p.rbcnt = reinterpret_cast<uint32_t*>(b + L.rbcnt);
+  p.h16 = reinterpret_cast<uint16_t*>(b + L.h16);
+  p.hexp = reinterpret_cast<int8_t*>(b + L.hexp);
+  p.hs = reinterpret_cast<uint16_t*>(b + L.hs);
+  p.ready = reinterpret_cast<uint32_t*>(b + L.ready);
   p.timeout_ns = g_timeout_ns;
-  if (!moe::plan_decode(p, budget)) return MOE_ERR_UNSUPPORTED;
+  if (!moe::plan_decode(p, budget, grid)) return MOE_ERR_UNSUPPORTED;
   if (!route_only) {
     const uint64_t ER = (uint64_t)d->E;
     const moe::Geo& ga = p.geo[moe::KIND_AR];

@@ -10,8 +10,16 @@ namespace moe {
 
 constexpr int kConsumerWarps = 8;                 // compute warps per CTA
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;   // + one producer (TMA) warp
+// A TMA copy instruction from DRAM keeps its issuing thread busy for a few
+// hundred cycles whatever its size, so one thread cannot feed an SM at HBM
+// speed: several producer warps (lane 0 each) issue alternate stages.
+constexpr int kProducers = 4;
+// + one epilogue warp that finishes each gate/up row group (reduction over the
+// compute warps, SiLU(g)*u, h stores) while the compute warps go on
+constexpr int kEpiWarp = kConsumerWarps;
+constexpr int kThreads = kConsumerThreads + 32 + 32 * kProducers;
 constexpr int kTB = 4;                            // token rows per weight pass
+constexpr int kRedFloats = kConsumerWarps * 2 * kTB * 32;   // one partial-sum buffer
 constexpr int kRows = 32;                         // weight rows per row group
 constexpr int kMaxSlots = 256;                    // N * top_k per call
 constexpr int kMaxE = 1024;
@@ -20,14 +28,22 @@ constexpr int kMaxStages = 8;
 constexpr int kBoxBytes = 128;                    // inner extent of a weight box
 constexpr int kBoxesPerChunk = 4;                 // chunk = 512 bytes of each row
 constexpr int kChunkBytes = kBoxBytes * kBoxesPerChunk;
-constexpr int kBoxTileBytes = kRows * kBoxBytes;  // 4 KB: one 32-row box in smem
-constexpr int kMaxRgList = 512;                   // down row groups tracked per CTA
+constexpr int kBoxTileBytes = kRows * kBoxBytes;  // 4 KB: one 32-row tile in smem
+constexpr int kDnRows = 16;                       // output rows per down block
+constexpr int kReadyAS = kMaxSlots;               // ready[] index of the shared expert
 
+// AS shared gate/up (32-row groups), AR routed gate/up (16 gate + 16 up rows
+// stacked as one 32-row tile), BR routed down / BS shared down (16-row blocks).
 enum Kind { KIND_AS = 0, KIND_AR = 1, KIND_BR = 2, KIND_BS = 3 };
 enum Fmt { FMT_NVFP4 = 0, FMT_MXFP4 = 1, FMT_BF16 = 2 };
 enum ScaleMode { SCALES_NONE = 0, SCALES_TMAP = 1, SCALES_BLOCK = 2 };
 // tensor map slots
-enum TMap { TM_GQ = 0, TM_UQ, TM_DQ, TM_GS, TM_US, TM_DS, TM_SG, TM_SU, TM_SD, TM_COUNT };
+// 2D maps of weight rows (boxes of 128 bytes x brows), of scales, and 3D
+// maps of the weight rows viewed as [128-byte column][row][byte] (boxes of 4
+// columns: a whole 512-byte chunk of brows rows in one copy) where the row
+// length is a multiple of 128 bytes.
+enum TMap { TM_GQ = 0, TM_UQ, TM_DQ, TM_GS, TM_US, TM_DS, TM_SG, TM_SU, TM_SD,
+            TM3_GQ, TM3_UQ, TM3_DQ, TM3_SG, TM3_SU, TM3_SD, TM_COUNT };
 
 // Device-side error word bits (workspace control block).
 constexpr uint32_t kErrTimeoutBarrier = 1u;
@@ -36,7 +52,7 @@ constexpr uint32_t kErrTimeoutProducer = 4u;
 
 // Workspace control block (first 256 bytes of the workspace).
 struct Ctrl {
-  unsigned long long arrivals;   // grid-barrier arrivals, monotonic (2 per CTA per call)
+  unsigned long long arrivals;   // grid-barrier arrivals, monotonic (1 per CTA per call)
   uint32_t error;                // sticky error bits
   uint32_t pad[61];
 };
@@ -45,6 +61,8 @@ struct Ctrl {
 struct Geo {
   int fmt;          // Fmt
   int nproj;        // weight matrices streamed together (2 = gate+up, 1 = down)
+  int brows;        // rows per TMA box (32 shared gate/up, 16 routed gate/up and down)
+  int rg_rows;      // output rows per row group / down block
   int K;            // reduction length (input dim of the projection)
   int kb;           // bytes of one full weight row
   int Kc;           // K elements per full chunk (512 bytes of row)
@@ -53,13 +71,16 @@ struct Geo {
   int sr;           // scale bytes per full weight row (K / gs); 0 for bf16
   int scb;          // scale bytes per row per chunk (TMAP mode)
   int scale_off;    // offset of the scale region in the stage
-  int opnd_off;     // offset of the activation chunk region (-1: from hbuf)
+  int opnd_off;     // offset of the activation chunk region
+  int hx_off;       // offset of the chunk's h exponents (routed down stages)
   int stage_bytes;  // bytes used in a stage
   int rows_total;   // weight rows of one projection (inter, H or Is)
+  int tile_bytes;   // bytes between 128-byte box columns of one projection
+  int use3d;        // weight chunks by one 3D copy per projection
 };
 
 struct Params {
-  CUtensorMap tm[TM_COUNT];   // 2D maps: packed/bf16 weights (swizzle 128B), scales
+  CUtensorMap tm[TM_COUNT];   // weight (swizzle 128B) and scale maps
   uint32_t tm_valid;          // bit i set when tm[i] is encoded
   // layer
   int H, inter, E, k, scoring, norm;
@@ -85,15 +106,16 @@ struct Params {
   uint16_t* x16;     // [N, H] f16, x * 2^-xexp[n]
   int* xexp;         // [N]
   float* gsig;       // [N] shared-expert gate
-  float* h;          // [N*k, inter] routed SiLU(g)*u, by (expert, token) slot
-  float* hs;         // [N, Is] shared expert SiLU(g)*u
-  float* acc;        // [N, H] routed + shared FP32 accumulator
-  uint32_t* rbcnt;   // [H/32] completion counters of output row blocks
+  uint16_t* h16;     // [N*k, inter] f16 SiLU(g)*u by (expert, token) slot, x 2^-hexp
+  int8_t* hexp;      // [units][hstride] power-of-two exponent per 16 rows of h16
+  uint16_t* hs;      // [N, Is] bf16 shared expert SiLU(g)*u
+  uint32_t* ready;   // [kMaxSlots + 1] finished gate/up row groups per unit (+ shared)
+  int hstride;       // bytes per unit row of hexp (inter/16 rounded up to 16)
   // geometry
   Geo geo[4];
   int nstages, stage_bytes;
-  int smem_ring_off, smem_red_off, smem_hbuf_off, smem_tab_off, smem_bar_off, smem_total;
-  int hbuf_bytes;
+  int smem_ring_off, smem_red_off, smem_sacc_off, smem_tab_off, smem_bar_off, smem_total;
+  int nrb, nrb_cta;  // down blocks (H/16) and at most this many per CTA
   unsigned long long timeout_ns;
 };
 
@@ -155,7 +177,7 @@ cudaError_t launch_grouped(const GroupedParams& gp, GemmParams gu, GemmParams gd
 
 // Fills p.geo / ring / smem layout from the layer shape; returns false if
 // the shape does not fit the kernel's shared-memory budget.
-bool plan_decode(Params& p, int smem_budget);
+bool plan_decode(Params& p, int smem_budget, int grid);
 
 // Shared memory the decode kernel may use on this device.
 int decode_smem_budget(int device);

@@ -21,9 +21,9 @@ def lib():
 
 def test_noalloc_refuses_shapes_beyond_its_scratch(lib):
     """Host-side refusal, before any CUDA call: 64 tokens of a layer with
-    H 7168, inter 8192, top-4 need more than the 8 MiB built-in scratch."""
+    H 7168, inter 16384, top-4 need more than the 8 MiB built-in scratch."""
     d = _lib.LayerDesc()
-    d.H, d.inter, d.E, d.top_k = 7168, 8192, 256, 4
+    d.H, d.inter, d.E, d.top_k = 7168, 16384, 256, 4
     d.scoring, d.norm_topk_prob, d.routed_scaling_factor = 0, 1, 1.0
     d.wfmt, d.shared_inter = 0, 0
     assert _lib.moe_workspace_size(d, 64) > 8 << 20
