@@ -74,7 +74,7 @@ struct Tables {
   uint16_t unit_u[kMaxSlots];  // units = (unique expert, token batch)
   uint8_t unit_tb[kMaxSlots];
   int16_t xe[kMaxSlots];       // power-of-two exponent of each token's f16 x
-  float s2[3][kMaxSlots];      // gate / up / down scale2 of unique expert u
+  float s2[2][kMaxSlots];      // gate / up scale2 of unique expert u
   int U, n_units;
   int abort;                   // set when a bounded wait expired
   float rscratch[kConsumerWarps * 8];
@@ -432,15 +432,17 @@ __device__ __noinline__ void routing_phase(const Params& p, int write_out, Table
     }
   }
   consumer_sync();
-  if (!p.route_only && warp == kConsumerWarps - 1) {
-    for (int u = lane; u < tb.U; u += 32) {
-      const int e = tb.uexp[u];
-      tb.s2[0][u] = p.g2 ? __ldg(p.g2 + e) : 1.0f;
-      tb.s2[1][u] = p.u2 ? __ldg(p.u2 + e) : 1.0f;
-      tb.s2[2][u] = p.d2 ? __ldg(p.d2 + e) : 1.0f;
-    }
+}
+
+// Per-unique-expert gate/up scale2 factors into shared memory (the epilogue
+// warp, off the compute warps' path; read only by its own epilogues).
+__device__ __forceinline__ void load_scale2(const Params& p, Tables& tb, int lane) {
+  for (int u = lane; u < tb.U; u += 32) {
+    const int e = tb.uexp[u];
+    tb.s2[0][u] = p.g2 ? __ldg(p.g2 + e) : 1.0f;
+    tb.s2[1][u] = p.u2 ? __ldg(p.u2 + e) : 1.0f;
   }
-  consumer_sync();
+  __syncwarp();
 }
 
 // ------------------------------------------------------- row-group plumbing
@@ -710,6 +712,19 @@ __device__ __noinline__ bool produce_down(const Params& p, Tables& tb, const Rin
   int kw = 0, ko = 0;
   uint64_t idle0 = 0;
   bool ok = true;
+  // units already seen complete (units beyond 64 are re-checked each time)
+  unsigned long long seen = 0ull;
+  bool as_seen = false;
+  auto unit_ready = [&](const DnJob& j) -> bool {
+    if (!j.routed) {
+      if (!as_seen) as_seen = ld_acquire_u32(p.ready + kReadyAS) >= need_s;
+      return as_seen;
+    }
+    if (j.unit < 64 && (seen >> j.unit & 1ull)) return true;
+    const bool r = ld_acquire_u32(p.ready + j.unit) >= need_r;
+    if (r && j.unit < 64) seen |= 1ull << j.unit;
+    return r;
+  };
   // skip the stages of the other producers (both cursors)
   auto skip_w = [&]() {
     while (kw < total && (ctr0 + kw) % kProducers != pid) {
@@ -731,8 +746,7 @@ __device__ __noinline__ bool produce_down(const Params& p, Tables& tb, const Rin
     bool did = false;
     if (ko < kw) {
       const DnJob j = dn_job(p, tb, cta, G, O, nr);
-      const uint32_t have = ld_acquire_u32(p.ready + (j.routed ? j.unit : kReadyAS));
-      if (have >= (j.routed ? need_r : need_s)) {
+      if (unit_ready(j)) {
         fence_proxy_async_global();   // h16 / hs were written by other CTAs
         const int k = ctr0 + ko;
         dn_operand(p, j, O.c, ring.base + (size_t)(k % ring.nstages) * ring.stage_bytes,
@@ -1310,12 +1324,13 @@ __device__ __noinline__ void consume_down(const Params& p, Tables& tb, const Con
       const int slice = (warp - w0) * 2 + half, nslice = 2 * S;
       const bool routed = jb < nr;
       const SG& g = routed ? gr : gsh;
-      int nt, src0, e = 0;
+      int nt, src0;
+      float d2 = 1.0f;   // down scale2, loaded at job start (latency hidden by the compute)
       if (routed) {
         const int u = tb.unit_u[jb], tbi = tb.unit_tb[jb];
         nt = min(kTB, (int)tb.ucnt[u] - tbi * kTB);
         src0 = tb.hoff[u] + tbi * kTB;
-        e = tb.uexp[u];
+        if (own && p.d2) d2 = __ldg(p.d2 + tb.uexp[u]);
       } else {
         const int b = jb - nr;
         nt = min(kTB, p.N - b * kTB);
@@ -1362,7 +1377,6 @@ __device__ __noinline__ void consume_down(const Params& p, Tables& tb, const Con
 #pragma unroll
         for (int t = 0; t < kTB; ++t) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], 16);
         if (lane < 16) {
-          const float d2 = routed ? tb.s2[2][tb.unit_u[jb]] : 1.0f;
 #pragma unroll
           for (int t = 0; t < kTB; ++t) {
             if (t < nt) {
@@ -1433,6 +1447,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
       __threadfence();
       atomicAdd(p.ready + kReadyAS, (uint32_t)as_done);
     }
+    load_scale2(p, tb, lane);
     epilogue_kind<KIND_AR>(p, tb, cx, cta, G, &kk, lane);
     return;
   }
