@@ -85,12 +85,24 @@ struct Tables {
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+// SiLU with the fast exponential and divide (h is rounded to f16 afterwards).
+__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+// 2^e for e in [-252, 254] (two normal factors; 0 or inf outside the float range).
+__device__ __forceinline__ float exp2i(int e) {
+  const int e1 = e >> 1;
+  return __int_as_float((e1 + 127) << 23) * __int_as_float((e - e1 + 127) << 23);
+}
+// floor(log2(m)) of a positive finite float, subnormals included.
+__device__ __forceinline__ int ilog2_pos(float m) {
+  const uint32_t b = __float_as_uint(m);
+  const int ex = (int)((b >> 23) & 0xFFu);
+  return ex ? ex - 127 : -118 - __clz(b & 0x7FFFFFu);
+}
 __device__ __forceinline__ void consumer_sync() { named_bar_sync(1, kConsumerThreads); }
 __device__ __forceinline__ bool aborted(const Tables& tb) {
   return *(volatile const int*)&tb.abort != 0;
 }
-__device__ __forceinline__ void set_abort(const Params& p, Tables& tb, uint32_t bit) {
+__device__ __noinline__ void set_abort(const Params& p, Tables& tb, uint32_t bit) {
   atomicOr(&p.ctrl->error, bit);
   *(volatile int*)&tb.abort = 1;
 }
@@ -148,7 +160,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, Tables& tb, int 
 // Power-of-two exponent e such that max|v| * 2^-e lies in [64, 128).
 __device__ __forceinline__ int scale_exponent(float amax) {
   if (!(amax > 0.f) || !isfinite(amax)) return 0;
-  return ilogbf(amax) - 6;
+  return ilog2_pos(amax) - 6;
 }
 
 // ------------------------------------------------------------ grid barrier
@@ -235,7 +247,7 @@ __device__ __noinline__ void token_prep(const Params& p, int cta, int G, Tables&
     block_reduce<1, true>(m1, tb, ctid);
     block_reduce<1, false>(d, tb, ctid);
     const int ex = scale_exponent(m1[0]);
-    const float sc = ldexpf(1.0f, -ex);
+    const float sc = exp2i(-ex);
     for (int kk = ctid * 8; kk < H; kk += kConsumerThreads * 8) {
       const uint4 xv = ld_nc_u4(xr + kk);
       const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w};
@@ -814,9 +826,26 @@ struct ConsumerCtx {
   uint64_t* rempty;  // [2] epilogue warp -> compute warps (buffer free)
 };
 
+// Loads from the stage ring and tables in shared memory.  The pointers reach
+// the consumer through structures, so the address space is stated explicitly
+// (a generic load would take the slower generic-address path).
 template <typename T>
 __device__ __forceinline__ T lds(const uint8_t* p) {
-  return *reinterpret_cast<const T*>(p);
+  const uint32_t a = smem_u32(p);
+  if constexpr (sizeof(T) == 16) {
+    const uint4 v = lds128(a);
+    return *reinterpret_cast<const T*>(&v);
+  } else if constexpr (sizeof(T) == 8) {
+    const uint2 v = lds64(a);
+    return *reinterpret_cast<const T*>(&v);
+  } else if constexpr (sizeof(T) == 4) {
+    const uint32_t v = lds32(a);
+    return *reinterpret_cast<const T*>(&v);
+  } else if constexpr (sizeof(T) == 2) {
+    return (T)lds_u16(a);
+  } else {
+    return (T)lds_u8(a);
+  }
 }
 
 // Stage geometry of one kind, held in registers by the consumer.
@@ -1046,15 +1075,15 @@ __device__ __forceinline__ void dn_piece(const uint8_t* st, const SG& g, int c, 
                             ? sptr(st, g, 0, row, 2 * s)
                             : st + g.scale_off + row * g.sr + (c * g.Kc + s * 32) / 16;
     const float2 sc = f16x2_to_f32x2(e4m3x2_to_f16x2(lds<uint16_t>(sa)));
-    f0 = sc.x * pow2i(hx[2 * s]);
-    f1 = sc.y * pow2i(hx[2 * s + 1]);
+    f0 = sc.x * pow2i((int8_t)lds<uint8_t>(reinterpret_cast<const uint8_t*>(hx + 2 * s)));
+    f1 = sc.y * pow2i((int8_t)lds<uint8_t>(reinterpret_cast<const uint8_t*>(hx + 2 * s + 1)));
   } else {
     const uint8_t* sa = (g.scale_mode == SCALES_TMAP)
                             ? sptr(st, g, 0, row, s)
                             : st + g.scale_off + row * g.sr + (c * g.Kc + s * 32) / 32;
     const float sc = e8m0_to_f32(lds<uint8_t>(sa));
-    f0 = sc * pow2i(hx[2 * s]);
-    f1 = sc * pow2i(hx[2 * s + 1]);
+    f0 = sc * pow2i((int8_t)lds<uint8_t>(reinterpret_cast<const uint8_t*>(hx + 2 * s)));
+    f1 = sc * pow2i((int8_t)lds<uint8_t>(reinterpret_cast<const uint8_t*>(hx + 2 * s + 1)));
   }
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
@@ -1172,7 +1201,7 @@ __device__ __forceinline__ void rg_epilogue(const Params& p, const Tables& tb, c
           g += red[((w * 2) * kTB + t) * 32 + j];
           u += red[((w * 2) * kTB + t) * 32 + 16 + j];
         }
-        const float xs = ldexpf(1.0f, tb.xe[rg_token<KIND>(tb, r, t)]);
+        const float xs = exp2i(tb.xe[rg_token<KIND>(tb, r, t)]);
         g *= xs * g2;
         u *= xs * u2;
         h[t] = silu(g) * u;
@@ -1262,7 +1291,8 @@ __device__ __forceinline__ void consume_rg(const Params& p, Tables& tb, const Co
 #pragma unroll
   for (int pj = 0; pj < NPROJ; ++pj)
 #pragma unroll
-    for (int t = 0; t < NT; ++t) red[((warp * 2 + pj) * kTB + t) * 32 + lane] = acc[pj][t];
+    for (int t = 0; t < NT; ++t)
+      sts32(smem_u32(red + ((warp * 2 + pj) * kTB + t) * 32 + lane), __float_as_uint(acc[pj][t]));
 }
 
 // Compute warps: every stage of one gate/up kind's row groups; each group's
@@ -1382,7 +1412,8 @@ __device__ __noinline__ void consume_down(const Params& p, Tables& tb, const Con
             if (t < nt) {
               const int n = routed ? tb.utok[src0 + t] : src0 + t;
               const float wgt = routed ? tb.uw[src0 + t] * d2 : ld_cg_f32(p.gsig + n);
-              atomicAdd(cx.sacc + ((size_t)i * p.N + n) * kDnRows + row, acc[t] * wgt);
+              red_add_shared_f32(smem_u32(cx.sacc + ((size_t)i * p.N + n) * kDnRows + row),
+                                 acc[t] * wgt);
             }
           }
         }
