@@ -11,7 +11,7 @@ import numpy as np
 import torch
 
 from . import _lib
-from .synth import HostLayer, LayerSpec, NVFP4, SOFTMAX
+from .synth import BF16, HostLayer, LayerSpec, MXFP4, NVFP4, SOFTMAX
 
 
 def layer_desc(spec: LayerSpec) -> _lib.LayerDesc:
@@ -20,7 +20,7 @@ def layer_desc(spec: LayerSpec) -> _lib.LayerDesc:
     d.scoring = _lib.MOE_SCORE_SOFTMAX if spec.scoring == SOFTMAX else _lib.MOE_SCORE_SIGMOID_BIAS
     d.norm_topk_prob = int(spec.norm_topk_prob)
     d.routed_scaling_factor = float(spec.routed_scaling_factor)
-    d.wfmt = _lib.MOE_W_NVFP4 if spec.wfmt == NVFP4 else _lib.MOE_W_MXFP4
+    d.wfmt = {NVFP4: _lib.MOE_W_NVFP4, MXFP4: _lib.MOE_W_MXFP4, BF16: _lib.MOE_W_BF16}[spec.wfmt]
     d.shared_inter = spec.shared_inter
     return d
 

@@ -31,6 +31,7 @@ import numpy as np
 
 NVFP4 = "nvfp4"
 MXFP4 = "mxfp4"
+BF16 = "bf16"
 SOFTMAX = "softmax"
 SIGMOID_BIAS = "sigmoid_bias"
 
@@ -45,7 +46,7 @@ class LayerSpec:
     scoring: str            # SOFTMAX | SIGMOID_BIAS
     norm_topk_prob: bool
     routed_scaling_factor: float
-    wfmt: str               # NVFP4 | MXFP4
+    wfmt: str               # NVFP4 | MXFP4 | BF16
     shared_inter: int       # 0 = no shared expert
     shared_gated: bool      # sigmoid(w_s . x) gate on the shared expert
     x_rms_norm: bool        # x rows RMS-normalised before the BF16 cast
@@ -54,10 +55,14 @@ class LayerSpec:
 
     @property
     def gs(self) -> int:
-        return 16 if self.wfmt == NVFP4 else 32
+        """Block-scale group size (0 for BF16 experts, which have no scales)."""
+        return {NVFP4: 16, MXFP4: 32, BF16: 0}[self.wfmt]
 
     def expert_bytes(self) -> int:
-        """Bytes of one routed expert (gate+up+down packed codes + block scales)."""
+        """Bytes of one routed expert (gate+up+down packed codes + block scales,
+        or BF16 words)."""
+        if self.wfmt == BF16:
+            return 3 * self.inter * self.H * 2
         return 3 * self.inter * self.H // 2 + 3 * self.inter * self.H // self.gs
 
     def router_bytes(self) -> int:
@@ -80,9 +85,12 @@ CONFIGS = {
     # "softmax over the selected top-k" == softmax over E then renormalise.
     "gpt_oss_120b": LayerSpec("gpt_oss_120b", 2880, 2880, 128, 4, SOFTMAX, True, 1.0,
                               MXFP4, 0, False, False, (1, 2, 3, 4, 8, 16, 32, 64, 512), 8),
+    # BF16 routed experts (the pages' third expert format) on the Qwen3 shape.
+    "qwen3_30b_a3b_bf16": LayerSpec("qwen3_30b_a3b_bf16", 2048, 768, 128, 8, SOFTMAX, True,
+                                    1.0, BF16, 0, False, True, (1, 2, 3, 4), 16),
 }
 CONFIG_INDEX = {"tiny": 0, "qwen3_30b_a3b": 1, "mtp_verify": 2, "deepseek_v3": 3,
-                "gpt_oss_120b": 4}
+                "gpt_oss_120b": 4, "qwen3_30b_a3b_bf16": 5}
 
 
 def base_seed(spec: LayerSpec) -> int:
@@ -198,12 +206,12 @@ class HostLayer:
     spec: LayerSpec
     router: np.ndarray            # uint16 [E, H] BF16 bits
     bias: Optional[np.ndarray]    # float32 [E] or None
-    gate_q: np.ndarray            # uint8 [E, inter, H/2]
+    gate_q: np.ndarray            # uint8 [E, inter, H/2] (BF16 experts: uint16 [E, inter, H])
     up_q: np.ndarray
-    down_q: np.ndarray            # uint8 [E, H, inter/2]
-    gate_s: np.ndarray            # uint8 [E, inter, H/gs]
-    up_s: np.ndarray
-    down_s: np.ndarray            # uint8 [E, H, inter/gs]
+    down_q: np.ndarray            # uint8 [E, H, inter/2] (BF16 experts: uint16 [E, H, inter])
+    gate_s: Optional[np.ndarray]  # uint8 [E, inter, H/gs] (None for BF16 experts)
+    up_s: Optional[np.ndarray]
+    down_s: Optional[np.ndarray]  # uint8 [E, H, inter/gs]
     gate_s2: Optional[np.ndarray]  # float32 [E] (NVFP4) or None (MXFP4)
     up_s2: Optional[np.ndarray]
     down_s2: Optional[np.ndarray]
@@ -219,27 +227,34 @@ class HostLayer:
 
 
 def _quantize(spec: LayerSpec, w: np.ndarray):
+    if spec.wfmt == BF16:
+        return f32_to_bf16_bits(w), None
     return quantize_nvfp4(w) if spec.wfmt == NVFP4 else quantize_mxfp4(w)
 
 
 def _expert_projection(spec, rng, rows, K, pool, E):
-    """Draw `pool` experts [rows, K] ~ N(0, 0.02), quantise, and fill E slots."""
+    """Draw `pool` experts [rows, K] ~ N(0, 0.02), quantise (or round to BF16),
+    and fill E slots."""
     qs, ss = [], []
     for _ in range(pool):
         w = rng.standard_normal((rows, K), dtype=np.float32) * np.float32(0.02)
         q, s = _quantize(spec, w)
         qs.append(q)
         ss.append(s)
-    qp, sp = np.stack(qs), np.stack(ss)
+    qp = np.stack(qs)
+    sp = None if ss[0] is None else np.stack(ss)
     if pool >= E:
-        return qp[:E].copy(), sp[:E].copy()
+        return qp[:E].copy(), None if sp is None else sp[:E].copy()
     src = rng.integers(0, pool, size=E)
     src[:pool] = np.arange(pool)            # every pool entry is used
     flip = rng.random((E, rows)) < 0.5
     flip[:pool] = False
     q = qp[src]
-    q ^= (flip.astype(np.uint8) * np.uint8(0x88))[..., None]
-    return q, sp[src].copy()
+    if spec.wfmt == BF16:                    # sign bit of every BF16 word of the row
+        q ^= (flip.astype(np.uint16) * np.uint16(0x8000))[..., None]
+    else:                                    # sign bits of both E2M1 codes of each byte
+        q ^= (flip.astype(np.uint8) * np.uint8(0x88))[..., None]
+    return q, None if sp is None else sp[src].copy()
 
 
 def make_layer(spec: LayerSpec, seed: Optional[int] = None, pool: Optional[int] = None) -> HostLayer:
@@ -255,7 +270,7 @@ def make_layer(spec: LayerSpec, seed: Optional[int] = None, pool: Optional[int] 
     gate_q, gate_s = _expert_projection(spec, rng, I, H, pool, E)
     up_q, up_s = _expert_projection(spec, rng, I, H, pool, E)
     down_q, down_s = _expert_projection(spec, rng, H, I, pool, E)
-    s2 = np.ones(E, dtype=np.float32) if spec.wfmt == NVFP4 else None
+    s2 = np.ones(E, dtype=np.float32) if spec.wfmt == NVFP4 else None   # MXFP4, BF16: none
     sh_gate = sh_up = sh_down = sh_gate_w = None
     if spec.shared_inter:
         Is = spec.shared_inter

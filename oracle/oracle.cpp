@@ -16,6 +16,9 @@
 //     routed_scaling_factor;
 //   * forward_k3.rs, the E8M0 guard (GS16 vs GS32 scale groups) — NVFP4
 //     (E2M1 + per-16 E4M3) and MXFP4 (E2M1 + per-32 E8M0) expert formats;
+//   * forward_batched.rs, the BF16 expert branch (bf16_gate/up/down weight
+//     pointers, "BF16 experts, with the same kernels") — BF16 routed experts,
+//     the same chain with plain BF16 weights (no block scales);
 //   * forward_atomic_c4.rs, doc comment — routed outputs accumulated as
 //     routing-weighted sums, then cast to BF16 and blended with the shared
 //     expert;
@@ -116,11 +119,24 @@ double oracle_fp4_weight(const uint8_t* q, const uint8_t* s, double scale2,
     return oracle_e2m1(code) * bs * scale2;
 }
 
+// Value of element (r, k) of a routed projection [rows, K] in weight format
+// `fmt`: 0/1 as oracle_fp4_weight; 2 = BF16 experts, the BF16 number stored in
+// the 16-bit little-endian word r*K + k of q (no block scales: s and scale2
+// are not read).
+double oracle_weight(const uint8_t* q, const uint8_t* s, double scale2, int K, int fmt,
+                     long r, long k) {
+    if (fmt == 2) {
+        const long i = 2 * (r * (long)K + k);
+        return oracle_bf16((uint32_t)q[i] | ((uint32_t)q[i + 1] << 8));
+    }
+    return oracle_fp4_weight(q, s, scale2, K, fmt, r, k);
+}
+
 void oracle_dequant(const uint8_t* q, const uint8_t* s, double scale2, int rows, int K,
                     int fmt, double* out) {
     for (long r = 0; r < rows; ++r)
         for (long k = 0; k < K; ++k)
-            out[r * K + k] = oracle_fp4_weight(q, s, scale2, K, fmt, r, k);
+            out[r * K + k] = oracle_weight(q, s, scale2, K, fmt, r, k);
 }
 
 // ------------------------------------------------------------------- router
@@ -201,10 +217,10 @@ void oracle_route(const double* logits, const float* bias, int N, int E, int k, 
 
 static double silu(double g) { return g / (1.0 + std::exp(-g)); }
 
-// One routed expert on one token, FP4 weights:
+// One routed expert on one token (weight format fmt, see oracle_weight):
 //   g = Dq(Wg) x,  u = Dq(Wu) x,  a = SiLU(g) * u,  y = Dq(Wd) a.
 // Wg, Wu are [inter, H]; Wd is [H, inter]; x is BF16 [H]; y is [H].
-void oracle_expert_fp4(const uint8_t* gq, const uint8_t* gsc, double g2,
+void oracle_expert(const uint8_t* gq, const uint8_t* gsc, double g2,
                        const uint8_t* uq, const uint8_t* usc, double u2,
                        const uint8_t* dq, const uint8_t* dsc, double d2,
                        int H, int inter, int fmt, const uint16_t* x, double* y) {
@@ -214,8 +230,8 @@ void oracle_expert_fp4(const uint8_t* gq, const uint8_t* gsc, double g2,
     for (int i = 0; i < inter; ++i) {
         double g = 0.0, u = 0.0;
         for (int h = 0; h < H; ++h) {
-            g += oracle_fp4_weight(gq, gsc, g2, H, fmt, i, h) * xv[h];
-            u += oracle_fp4_weight(uq, usc, u2, H, fmt, i, h) * xv[h];
+            g += oracle_weight(gq, gsc, g2, H, fmt, i, h) * xv[h];
+            u += oracle_weight(uq, usc, u2, H, fmt, i, h) * xv[h];
         }
         a[i] = silu(g) * u;
     }
@@ -223,7 +239,7 @@ void oracle_expert_fp4(const uint8_t* gq, const uint8_t* gsc, double g2,
     for (int r = 0; r < H; ++r) {
         double acc = 0.0;
         for (int i = 0; i < inter; ++i)
-            acc += oracle_fp4_weight(dq, dsc, d2, inter, fmt, r, i) * a[i];
+            acc += oracle_weight(dq, dsc, d2, inter, fmt, r, i) * a[i];
         y[r] = acc;
     }
 }
@@ -258,6 +274,8 @@ void oracle_shared_expert(const uint16_t* wg, const uint16_t* wu, const uint16_t
 //   gate_q/up_q [E, inter, H/2] u8, gate_s/up_s [E, inter, H/gs] u8,
 //   down_q [E, H, inter/2] u8, down_s [E, H, inter/gs] u8,
 //   *_s2 [E] f32 or null (null = 1.0; MXFP4 has none);
+//   BF16 experts (fmt 2): gate_q/up_q [E, inter, H] and down_q [E, H, inter]
+//   hold BF16 words, the scale pointers are not read;
 //   sh_gate/sh_up [Is, H] bf16, sh_down [H, Is] bf16 (null when Is == 0);
 //   sh_gate_w [H] bf16 or null (null = ungated shared expert).
 struct oracle_weights {
@@ -280,27 +298,32 @@ int oracle_moe_forward(int H, int inter, int E, int k, int scoring, int norm, do
                        double* out_f64, uint16_t* out_bf16, int32_t* idx, double* w,
                        double* logits_out) {
     if (H <= 0 || inter <= 0 || E <= 0 || k <= 0 || k > E || N < 0) return 1;
+    if (fmt < 0 || fmt > 2) return 1;
     const int gs = (fmt == 0) ? 16 : 32;
     std::vector<double> logits((size_t)N * E);
     oracle_router_logits(x, W->router, N, E, H, logits.data());
     if (logits_out) std::copy(logits.begin(), logits.end(), logits_out);
     oracle_route(logits.data(), W->bias, N, E, k, scoring, norm, rsf, idx, w, nullptr);
 
-    const long gq_e = (long)inter * (H / 2), gs_e = (long)inter * (H / gs);
-    const long dq_e = (long)H * (inter / 2), ds_e = (long)H * (inter / gs);
+    // bytes per expert of each table (BF16: two bytes per element, no scales)
+    const bool bf = (fmt == 2);
+    const long gq_e = bf ? 2L * inter * H : (long)inter * (H / 2);
+    const long gs_e = bf ? 0 : (long)inter * (H / gs);
+    const long dq_e = bf ? 2L * H * inter : (long)H * (inter / 2);
+    const long ds_e = bf ? 0 : (long)H * (inter / gs);
     std::vector<double> y(H), sh(H);
     for (int n = 0; n < N; ++n) {
         const uint16_t* xn = x + (long)n * H;
         std::vector<double> acc(H, 0.0);
         for (int j = 0; j < k; ++j) {
             const int e = idx[(long)n * k + j];
-            const double g2 = W->gate_s2 ? W->gate_s2[e] : 1.0;
-            const double u2 = W->up_s2 ? W->up_s2[e] : 1.0;
-            const double d2 = W->down_s2 ? W->down_s2[e] : 1.0;
-            oracle_expert_fp4(W->gate_q + e * gq_e, W->gate_s + e * gs_e, g2,
-                              W->up_q + e * gq_e, W->up_s + e * gs_e, u2,
-                              W->down_q + e * dq_e, W->down_s + e * ds_e, d2,
-                              H, inter, fmt, xn, y.data());
+            const double g2 = (!bf && W->gate_s2) ? W->gate_s2[e] : 1.0;
+            const double u2 = (!bf && W->up_s2) ? W->up_s2[e] : 1.0;
+            const double d2 = (!bf && W->down_s2) ? W->down_s2[e] : 1.0;
+            oracle_expert(W->gate_q + e * gq_e, bf ? nullptr : W->gate_s + e * gs_e, g2,
+                          W->up_q + e * gq_e, bf ? nullptr : W->up_s + e * gs_e, u2,
+                          W->down_q + e * dq_e, bf ? nullptr : W->down_s + e * ds_e, d2,
+                          H, inter, fmt, xn, y.data());
             const double wj = w[(long)n * k + j];
             for (int h = 0; h < H; ++h) acc[h] += wj * y[h];
         }

@@ -65,8 +65,10 @@ def lib():
             L.oracle_router_logits.argtypes = [vp, vp, i32, i32, i32, vp]
             L.oracle_route.restype = None
             L.oracle_route.argtypes = [vp, vp, i32, i32, i32, i32, i32, d, vp, vp, vp]
-            L.oracle_expert_fp4.restype = None
-            L.oracle_expert_fp4.argtypes = [vp, vp, d, vp, vp, d, vp, vp, d, i32, i32, i32, vp, vp]
+            L.oracle_weight.restype = d
+            L.oracle_weight.argtypes = [vp, vp, d, i32, i32, ctypes.c_long, ctypes.c_long]
+            L.oracle_expert.restype = None
+            L.oracle_expert.argtypes = [vp, vp, d, vp, vp, d, vp, vp, d, i32, i32, i32, vp, vp]
             L.oracle_shared_expert.restype = None
             L.oracle_shared_expert.argtypes = [vp, vp, vp, i32, i32, vp, vp]
             L.oracle_moe_forward.restype = i32
@@ -109,7 +111,7 @@ def round_bf16(v: float) -> int:
 
 
 def fmt_code(wfmt: str) -> int:
-    return 0 if wfmt == "nvfp4" else 1
+    return {"nvfp4": 0, "mxfp4": 1, "bf16": 2}[wfmt]
 
 
 def dequant(q: np.ndarray, s: np.ndarray, scale2: float, wfmt: str) -> np.ndarray:
@@ -149,19 +151,25 @@ def route(logits: np.ndarray, k: int, scoring: str, norm: bool, rsf: float = 1.0
     return idx, w, sel
 
 
-def expert_fp4(layer, e: int, x_row: np.ndarray) -> np.ndarray:
+def weight(q: np.ndarray, s: Optional[np.ndarray], scale2: float, K: int, wfmt: str,
+           r: int, k: int) -> float:
+    """Element (r, k) of one routed projection, as the oracle decodes it."""
+    q = np.ascontiguousarray(q)
+    s = None if s is None else np.ascontiguousarray(s)
+    return lib().oracle_weight(_p(q), _p(s), float(scale2), K, fmt_code(wfmt), r, k)
+
+
+def expert(layer, e: int, x_row: np.ndarray) -> np.ndarray:
     """One routed expert of a synth.HostLayer on one BF16 token row -> float64 [H]."""
     sp = layer.spec
     y = np.empty(sp.H, dtype=np.float64)
     x_row = np.ascontiguousarray(x_row, dtype=np.uint16)
     s2 = lambda a: 1.0 if a is None else float(a[e])
-    lib().oracle_expert_fp4(
-        _p(np.ascontiguousarray(layer.gate_q[e])), _p(np.ascontiguousarray(layer.gate_s[e])),
-        s2(layer.gate_s2),
-        _p(np.ascontiguousarray(layer.up_q[e])), _p(np.ascontiguousarray(layer.up_s[e])),
-        s2(layer.up_s2),
-        _p(np.ascontiguousarray(layer.down_q[e])), _p(np.ascontiguousarray(layer.down_s[e])),
-        s2(layer.down_s2),
+    sc = lambda a: None if a is None else np.ascontiguousarray(a[e])
+    lib().oracle_expert(
+        _p(np.ascontiguousarray(layer.gate_q[e])), _p(sc(layer.gate_s)), s2(layer.gate_s2),
+        _p(np.ascontiguousarray(layer.up_q[e])), _p(sc(layer.up_s)), s2(layer.up_s2),
+        _p(np.ascontiguousarray(layer.down_q[e])), _p(sc(layer.down_s)), s2(layer.down_s2),
         sp.H, sp.inter, fmt_code(sp.wfmt), _p(x_row), _p(y))
     return y
 

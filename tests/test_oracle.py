@@ -330,6 +330,77 @@ def test_single_expert_equals_dense_swiglu(oracle_mod, wfmt):
     np.testing.assert_array_equal(r["out_bf16"], rb)
 
 
+def _bf16_layer_from_fp4(layer):
+    """The same layer with BF16 routed experts holding the FP4 experts' values
+    (test-side decode; every E2M1 x E4M3 product has at most 6 significant bits,
+    so it is a BF16 number exactly)."""
+    import dataclasses
+    sp = layer.spec
+    assert sp.wfmt == synth.NVFP4 and all(np.all(a == 1.0) for a in (layer.gate_s2, layer.up_s2, layer.down_s2))
+
+    def conv(q, s):
+        out = []
+        for e in range(q.shape[0]):
+            v = _decode_fp4_independent(q[e], s[e], sp.wfmt)
+            bits = synth.f32_to_bf16_bits(v.astype(np.float32))
+            assert np.array_equal(_bf16_arr(bits), v)          # exact
+            out.append(bits)
+        return np.stack(out)
+
+    spb = dataclasses.replace(sp, wfmt=synth.BF16)
+    return dataclasses.replace(layer, spec=spb, gate_q=conv(layer.gate_q, layer.gate_s),
+                               up_q=conv(layer.up_q, layer.up_s),
+                               down_q=conv(layer.down_q, layer.down_s),
+                               gate_s=None, up_s=None, down_s=None,
+                               gate_s2=None, up_s2=None, down_s2=None)
+
+
+def test_bf16_experts_equal_fp4_experts_with_the_same_values(oracle_mod):
+    """BF16 routed experts (the pages' BF16 expert branch: the same chain with
+    plain BF16 weights) holding exactly the values of NVFP4 experts give the
+    NVFP4 layer's result to the last bit."""
+    sp = _small_spec(E=6, top_k=3, H=96, inter=64)
+    L = synth.make_layer(sp, seed=21)
+    Lb = _bf16_layer_from_fp4(L)
+    x = synth.make_tokens(sp, 4, seed=22)
+    r, rb = oracle_mod.moe_forward(L, x), oracle_mod.moe_forward(Lb, x)
+    assert set(r["idx"].ravel()) - {0}, "routing must reach experts past the first"
+    np.testing.assert_array_equal(rb["idx"], r["idx"])
+    np.testing.assert_array_equal(rb["out_f64"], r["out_f64"])
+    np.testing.assert_array_equal(rb["out_bf16"], r["out_bf16"])
+
+
+def test_bf16_single_expert_equals_dense_swiglu(oracle_mod):
+    sp = _small_spec(E=1, top_k=1, H=96, inter=64, wfmt=synth.BF16)
+    L = synth.make_layer(sp, seed=23)
+    assert L.gate_s is None and L.gate_q.dtype == np.uint16 and L.gate_q.shape == (1, 64, 96)
+    x = synth.make_tokens(sp, 2, seed=24)
+    r = oracle_mod.moe_forward(L, x)
+    Wg, Wu, Wd = (_bf16_arr(a[0]) for a in (L.gate_q, L.up_q, L.down_q))
+    for n in range(2):
+        x64 = _bf16_arr(x[n])
+        g, u = Wg @ x64, Wu @ x64
+        ref = Wd @ (g * scipy.special.expit(g) * u)
+        np.testing.assert_allclose(r["out_f64"][n], ref, rtol=1e-12, atol=1e-15)
+    for (rr, kk) in ((0, 0), (5, 17), (63, 95)):
+        assert oracle_mod.weight(L.gate_q[0], None, 1.0, 96, synth.BF16, rr, kk) == Wg[rr, kk]
+
+
+def test_bf16_expert_pool_copies_flip_whole_rows(oracle_mod):
+    """With fewer drawn experts than slots, a BF16 slot is a pool expert with
+    some rows negated (sign bit of every word of the row)."""
+    sp = _small_spec(E=6, top_k=2, wfmt=synth.BF16, pool=2)
+    L = synth.make_layer(sp, seed=25)
+    b = _bf16_arr(L.gate_q)                       # [E, rows, K]
+    assert not np.array_equal(np.abs(b[0]), np.abs(b[1]))
+    for e in range(2, 6):
+        src = [p for p in range(2) if np.array_equal(np.abs(b[e]), np.abs(b[p]))]
+        assert len(src) == 1
+        same = np.all(b[e] == b[src[0]], axis=1)
+        neg = np.all(b[e] == -b[src[0]], axis=1)
+        assert np.all(same | neg)
+
+
 def test_scale2_scales_each_projection(oracle_mod):
     sp = _small_spec(E=1, top_k=1)
     L = synth.make_layer(sp, seed=13)

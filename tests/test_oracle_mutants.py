@@ -33,8 +33,13 @@ MUTANTS = {
     "rsf_on_softmax": ("if (scoring == 1)\n        for (int j = 0; j < k; ++j) w[j] *= rsf;",
                        "for (int j = 0; j < k; ++j) w[j] *= rsf;"),
     "softmax_denominator": ("den += std::exp(l[e] - mx);", "den += std::exp(l[e]);"),
-    "down_transposed": ("oracle_fp4_weight(dq, dsc, d2, inter, fmt, r, i)",
-                        "oracle_fp4_weight(dq, dsc, d2, inter, fmt, i % H, r % inter)"),
+    "down_transposed": ("oracle_weight(dq, dsc, d2, inter, fmt, r, i)",
+                        "oracle_weight(dq, dsc, d2, inter, fmt, i % H, r % inter)"),
+    "bf16_byte_order": ("(uint32_t)q[i] | ((uint32_t)q[i + 1] << 8)",
+                        "(uint32_t)q[i + 1] | ((uint32_t)q[i] << 8)"),
+    "bf16_adjacent_swap": ("const long i = 2 * (r * (long)K + k);",
+                           "const long i = 2 * ((r * (long)K + k) ^ 1);"),
+    "bf16_expert_stride": ("const long gq_e = bf ? 2L * inter * H", "const long gq_e = bf ? 1L * inter * H"),
     "router_transposed": ("oracle_bf16(wr[(long)e * H + h])", "oracle_bf16(wr[(long)h * E + e])"),
     "shared_gate_no_sigmoid": ("gsig = 1.0 / (1.0 + std::exp(-d));", "gsig = d;"),
     "shared_down_dropped": ("acc[h] += gsig * sh[h];", "acc[h] += gsig;"),
