@@ -13,9 +13,10 @@ back from the routing outputs before timing).  value = sum of bytes / time.
 Timed region: K steps replayed from a captured CUDA graph, bracketed by a
 barrier and torch.cuda.synchronize(), CUDA events on the launch stream; the
 maximum over ranks is taken.  The line also carries "grouped": the many-token
-path (gpt-oss-shaped MXFP4 layer at N = 512, tcgen05 GEMMs) timed on the same
-GPU after the main measurement.  --impl reference times the FP64 CPU oracle on a
-bounded sample of the same workload instead.
+path (gpt-oss-shaped MXFP4 layer at N = 512, tcgen05 GEMMs) and
+"bf16_experts": the same Qwen3 shape with BF16 routed experts at N = 1-4,
+both timed on the same GPU after the main measurement.  --impl reference
+times the FP64 CPU oracle on a bounded sample of the same workload instead.
 """
 from __future__ import annotations
 
@@ -195,6 +196,56 @@ def measure_grouped(stream, name: str = "gpt_oss_120b", N: int = 512, reps: int 
             "hbm_frac_of_measured": round(b["total"] / us / 1e3 / peak, 4),
             "tensor_tflops": round(flops / us / 1e6, 2), "launches_per_call": kernels_per_call(spec, N),
             "reps": reps}
+
+
+def measure_decode_config(stream, name: str, tokens, copies: int = 4, reps: int = 200) -> dict:
+    """Decode-kernel latency of another layer shape (e.g. BF16 routed experts)
+    at each token count: `copies` device copies of the layer, each with its
+    own token rows, replayed round-robin from one CUDA graph so consecutive
+    calls read different weight bytes (copies x touched bytes > L2)."""
+    import torch
+    from moe_decode_layer_topk_gb300 import _lib, synth
+    from moe_decode_layer_topk_gb300.device import DeviceLayer, bf16_tensor, workspace
+    spec = synth.CONFIGS[name]
+    base = DeviceLayer.upload(synth.make_layer(spec))
+    devs = [base] + [base.clone() for _ in range(copies - 1)]
+    peak, _ = _peaks()
+    res = {}
+    for N in tokens:
+        calls = []
+        for i, dev in enumerate(devs):
+            x = bf16_tensor(synth.make_tokens(spec, N, seed=77000 + 97 * N + i))
+            out, ws = torch.empty_like(x), workspace(spec, N)
+            idx = torch.empty((N, spec.top_k), dtype=torch.int32, device="cuda")
+            _lib.moe_forward(dev.desc, dev.weights, x, out, ws, idx)
+            calls.append((dev, x, out, ws, algorithmic_bytes(spec, idx.cpu().numpy(), N)))
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for dev, x, out, ws, _ in calls:
+                _lib.moe_forward(dev.desc, dev.weights, x, out, ws, stream=stream)
+        rounds = max(1, reps // len(calls))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0.record(stream)
+            for _ in range(rounds):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        for c in calls:
+            assert _lib.moe_get_error(c[3]) == _lib.MOE_OK
+        us = e0.elapsed_time(e1) * 1e3 / (rounds * len(calls))
+        b = float(np.mean([c[4]["total"] for c in calls]))
+        res[str(N)] = {"us_per_layer": round(us, 3), "tokens_per_s": round(N / us * 1e6, 1),
+                       "GBps": round(b / us / 1e3, 1),
+                       "hbm_frac_of_measured": round(b / us / 1e3 / peak, 4),
+                       "U_mean": float(np.mean([c[4]["U"] for c in calls])), "bytes_mean": int(b)}
+        del calls, g
+    del devs, base
+    torch.cuda.empty_cache()
+    return {"workload": f"{name} layer (fused decode kernel), {copies} copies round-robin",
+            "per_n": res}
 
 
 def run_gpu(args):
@@ -380,6 +431,8 @@ def run_gpu(args):
     }
     if rank == 0 and not args.no_grouped:
         result["grouped"] = measure_grouped(stream)
+    if rank == 0 and not args.no_bf16:
+        result["bf16_experts"] = measure_decode_config(stream, "qwen3_30b_a3b_bf16", (1, 2, 3, 4))
     if rank == 0:
         result["clocks"] = clk.summary()
         if not args.no_cpu_baseline:
@@ -467,6 +520,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-bf16", action="store_true",
+                    help="skip the BF16 routed-expert decode measurement")
     ap.add_argument("--no-grouped", action="store_true",
                     help="skip the grouped-path (gpt-oss N=512) measurement")
     args = ap.parse_args()

@@ -10,6 +10,7 @@
  *   3. routed experts  SwiGLU with block-scaled FP4 weights:
  *                      h = SiLU(Dq(Wg) x) * (Dq(Wu) x),  y = Dq(Wd) h,
  *                      Dq(w) = E2M1(code) * blockscale * scale2;
+ *                      or with plain BF16 weights (Dq(w) = w);
  *   4. output          out[n] = BF16( sum_j w[n,j] * y_{idx[n,j]}
  *                                     + g_s(x_n) * shared(x_n) ),
  *                      g_s = sigmoid(w_s . x_n) if a shared-expert gate vector
@@ -28,7 +29,9 @@
  *     accumulation of the routed down projections, then a BF16 cast and the
  *     shared-expert blend; the scratch carve-out and its size check;
  *   - forward_batched.rs: one router GEMM for N rows, per-token routing, and
- *     "each routed and shared expert streams its weights once for all rows".
+ *     "each routed and shared expert streams its weights once for all rows";
+ *     its BF16 expert branch (bf16 gate/up/down weight pointers, the same
+ *     kernels as the FP4 forward) for the BF16 routed-expert format.
  *
  * Memory: every pointer passed to moe_forward / moe_route is a DEVICE pointer
  * (weights, x, out, topk outputs, workspace) unless the name says _host.  The
@@ -46,6 +49,9 @@
  *   up_s       [E, inter, H/gs]   u8  gs = 16 (E4M3, NVFP4) or 32 (E8M0, MXFP4)
  *   down_s     [E, H, inter/gs]   u8
  *   gate_s2, up_s2, down_s2 [E] f32 per-expert global scale (NULL = 1.0)
+ * BF16 routed experts (wfmt MOE_W_BF16): gate_q, up_q [E, inter, H] bf16 and
+ *   down_q [E, H, inter] bf16; the scale pointers and *_s2 are not read (NULL
+ *   allowed).
  *   sh_gate, sh_up [Is, H] bf16; sh_down [H, Is] bf16  (NULL when Is == 0)
  *   sh_gate_w  [H] bf16 or NULL (NULL = ungated, always-on shared expert)
  * All weight, x, out and workspace pointers must be 16-byte aligned.
@@ -78,7 +84,9 @@ typedef enum {
 } moe_status_t;
 
 typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID_BIAS = 1 } moe_scoring_t;
-typedef enum { MOE_W_NVFP4 = 0, MOE_W_MXFP4 = 1 } moe_wfmt_t;
+/* Routed-expert weight formats: NVFP4 (E2M1 + per-16 E4M3 scale + FP32
+ * scale2), MXFP4 (E2M1 + per-32 E8M0 scale), BF16 (plain weights). */
+typedef enum { MOE_W_NVFP4 = 0, MOE_W_MXFP4 = 1, MOE_W_BF16 = 2 } moe_wfmt_t;
 
 /* Layer configuration: the config fields the pages' MoE forward reads
  * (hidden_size, moe_intermediate_size, num_experts, num_experts_per_tok,
@@ -138,9 +146,9 @@ MOE_API moe_status_t moe_workspace_init(void* workspace, size_t ws_bytes, void* 
  *             moe_workspace_init; one workspace per concurrently running call
  * N*top_k <= 256 runs one fused decode kernel; larger N runs the grouped
  * path (per-expert token groups on the tcgen05 tensor cores, the pages'
- * "grouped GEMM (more than 64 rows)" of forward_batched.rs), which does not
- * take a shared expert yet: N*top_k > 256 with shared_inter > 0 returns
- * MOE_ERR_UNSUPPORTED.  Asynchronous on `stream`; no host synchronisation,
+ * "grouped GEMM (more than 64 rows)" of forward_batched.rs), which takes
+ * neither a shared expert nor BF16 routed experts yet: N*top_k > 256 with
+ * shared_inter > 0 or wfmt MOE_W_BF16 returns MOE_ERR_UNSUPPORTED.  Asynchronous on `stream`; no host synchronisation,
  * no allocation, so it may be captured in a CUDA graph.  Argument errors are
  * returned before anything is enqueued; device-side timeouts are reported by
  * moe_get_error. */

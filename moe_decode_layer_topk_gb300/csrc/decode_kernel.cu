@@ -606,7 +606,9 @@ __device__ __forceinline__ void produce_stage(const Params& p, const Tables& tb,
   const Geo& g = p.geo[KIND];
   const int elems = chunk_elems(g, c);
   produce_weights<KIND>(p, r.row0, c, st, full, gateup_opnd_bytes<KIND>(g, c, r.nt));
-  const uint16_t* xs = (KIND == KIND_AR) ? p.x16 : p.x;
+  // FP4 experts take the scaled f16 copy of x; BF16 weights (shared expert,
+  // BF16 routed experts) take the BF16 x itself
+  const uint16_t* xs = (KIND == KIND_AR && g.fmt != FMT_BF16) ? p.x16 : p.x;
   for (int t = 0; t < r.nt; ++t) {
     const int n = rg_token<KIND>(tb, r, t);
     bulk_g2s(st + g.opnd_off + t * g.Kc * 2, xs + (size_t)n * p.H + (size_t)c * g.Kc,
@@ -1009,6 +1011,41 @@ __device__ __forceinline__ void compute_fp4(const uint8_t* st, const SG& g, int 
   }
 }
 
+// One stage of BF16 routed gate/up weights (16 gate rows over 16 up rows of
+// the stacked tile, lane = row) for NT tokens against the BF16 x chunk; a
+// step is 32 elements = 64 bytes of a row, products and sums in f32.
+template <int NT>
+__device__ __forceinline__ void compute_bf16_ar(const uint8_t* st, const SG& g,
+                                                const uint8_t* obase, int otstride, int s0,
+                                                int s1, int lane, float (&acc)[1][NT]) {
+#pragma unroll 1
+  for (int s = s0; s < s1; ++s) {
+    uint32_t wv[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = lds<uint4>(wptr_ar(st, g.kb, lane, s * 4 + q));
+      wv[4 * q + 0] = w.x; wv[4 * q + 1] = w.y; wv[4 * q + 2] = w.z; wv[4 * q + 3] = w.w;
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const uint8_t* oa = obase + t * otstride + s * 64;
+      uint32_t xo[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 x = lds<uint4>(oa + q * 16);
+        xo[4 * q + 0] = x.x; xo[4 * q + 1] = x.y; xo[4 * q + 2] = x.z; xo[4 * q + 3] = x.w;
+      }
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; e += 2) {
+        a0 = fma2_bf16_to_f32(wv[e], xo[e], a0);
+        a1 = fma2_bf16_to_f32(wv[e + 1], xo[e + 1], a1);
+      }
+      acc[0][t] += a0 + a1;
+    }
+  }
+}
+
 // One stage of BF16 weights (shared expert) for NT tokens; a step is 32
 // elements = 64 bytes of a row.
 template <int NPROJ, int NT>
@@ -1132,6 +1169,46 @@ __device__ __forceinline__ void compute_dn_fp4(const uint8_t* st, const SG& g, i
   for (int t = 0; t < kTB; ++t) acc[t] += pa[t] + pb[t];
 }
 
+// One chunk of a routed down job with BF16 weights: 16 rows (row = lane & 15)
+// against the f16 h of NT tokens; a step is 32 elements (64 bytes of a row),
+// its two 16-element halves scaled by 2^(h exponent); the half-warp covers
+// steps [p0, p1).  Products and sums in f32.
+template <int NT>
+__device__ __forceinline__ void compute_dn_bf16r(const uint8_t* st, const SG& g, int p0, int p1,
+                                                 int row, float (&acc)[kTB]) {
+  const uint8_t* ob = st + g.opnd_off;
+  const uint8_t* hx = st + g.hx_off;
+  for (int s = p0; s < p1; ++s) {
+    uint32_t wv[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = lds<uint4>(wptr16(st, g.kb, row, s * 4 + q));
+      wv[4 * q + 0] = w.x; wv[4 * q + 1] = w.y; wv[4 * q + 2] = w.z; wv[4 * q + 3] = w.w;
+    }
+    const float f0 = pow2i((int8_t)lds<uint8_t>(hx + 2 * s));
+    const float f1 = pow2i((int8_t)lds<uint8_t>(hx + 2 * s + 1));
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const uint8_t* oa = ob + t * g.Kc * 2 + s * 64;
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 x = lds<uint4>(oa + q * 16);
+        const uint32_t xv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 h = f16x2_to_f32x2(xv[i]);
+          const uint32_t w = wv[4 * q + i];
+          float& a = (q < 2) ? a0 : a1;
+          a = fmaf(bf16_lo(w), h.x, a);
+          a = fmaf(bf16_hi(w), h.y, a);
+        }
+      }
+      acc[t] = fmaf(a0, f0, fmaf(a1, f1, acc[t]));
+    }
+  }
+}
+
 // One chunk of a shared-expert down job: BF16 weights against BF16 h; a step
 // is 32 elements (64 bytes) of the row, the half-warp covers steps [p0, p1).
 template <int NT>
@@ -1201,7 +1278,8 @@ __device__ __forceinline__ void rg_epilogue(const Params& p, const Tables& tb, c
           g += red[((w * 2) * kTB + t) * 32 + j];
           u += red[((w * 2) * kTB + t) * 32 + 16 + j];
         }
-        const float xs = exp2i(tb.xe[rg_token<KIND>(tb, r, t)]);
+        // FP4 experts ran on x * 2^-xe; BF16 routed experts on x itself
+        const float xs = (p.fmt == FMT_BF16) ? 1.0f : exp2i(tb.xe[rg_token<KIND>(tb, r, t)]);
         g *= xs * g2;
         u *= xs * u2;
         h[t] = silu(g) * u;
@@ -1282,8 +1360,12 @@ __device__ __forceinline__ void consume_rg(const Params& p, Tables& tb, const Co
       const int s0 = warp * ns / kConsumerWarps, s1 = (warp + 1) * ns / kConsumerWarps;
       const uint8_t* ob = st + g.opnd_off;
       const int ots = g.Kc * 2;
-      if (FMT == FMT_BF16) compute_bf16<NPROJ, NT>(st, g, ob, ots, s0, s1, lane, acc);
-      else compute_fp4<FMT, NPROJ, NT>(st, g, c, ob, ots, s0, s1, lane, acc);
+      if constexpr (FMT == FMT_BF16 && KIND == KIND_AR)
+        compute_bf16_ar<NT>(st, g, ob, ots, s0, s1, lane, acc);
+      else if constexpr (FMT == FMT_BF16)
+        compute_bf16<NPROJ, NT>(st, g, ob, ots, s0, s1, lane, acc);
+      else
+        compute_fp4<FMT, NPROJ, NT>(st, g, c, ob, ots, s0, s1, lane, acc);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(cx.empty + slot);
@@ -1381,13 +1463,24 @@ __device__ __noinline__ void consume_down(const Params& p, Tables& tb, const Con
           const uint8_t* st = cx.ring_base + (size_t)slot * cx.stage_bytes;
           const int rb = min(kChunkBytes, g.kb - c * kChunkBytes);
           if (routed) {
-            const int np = rb / 16;
-            const int p0 = slice * np / nslice, p1 = (slice + 1) * np / nslice;
-            switch (nt) {
-              case 1: compute_dn_fp4<FMT, 1>(st, g, c, p0, p1, row, acc); break;
-              case 2: compute_dn_fp4<FMT, 2>(st, g, c, p0, p1, row, acc); break;
-              case 3: compute_dn_fp4<FMT, 3>(st, g, c, p0, p1, row, acc); break;
-              default: compute_dn_fp4<FMT, 4>(st, g, c, p0, p1, row, acc); break;
+            if constexpr (FMT == FMT_BF16) {
+              const int np = rb / 64;
+              const int p0 = slice * np / nslice, p1 = (slice + 1) * np / nslice;
+              switch (nt) {
+                case 1: compute_dn_bf16r<1>(st, g, p0, p1, row, acc); break;
+                case 2: compute_dn_bf16r<2>(st, g, p0, p1, row, acc); break;
+                case 3: compute_dn_bf16r<3>(st, g, p0, p1, row, acc); break;
+                default: compute_dn_bf16r<4>(st, g, p0, p1, row, acc); break;
+              }
+            } else {
+              const int np = rb / 16;
+              const int p0 = slice * np / nslice, p1 = (slice + 1) * np / nslice;
+              switch (nt) {
+                case 1: compute_dn_fp4<FMT, 1>(st, g, c, p0, p1, row, acc); break;
+                case 2: compute_dn_fp4<FMT, 2>(st, g, c, p0, p1, row, acc); break;
+                case 3: compute_dn_fp4<FMT, 3>(st, g, c, p0, p1, row, acc); break;
+                default: compute_dn_fp4<FMT, 4>(st, g, c, p0, p1, row, acc); break;
+              }
             }
           } else {
             const int np = rb / 64;
@@ -1621,7 +1714,7 @@ static bool plan_kind(Geo& g, int kind, int fmt, int K, int rows, int ntok) {
 }
 
 bool plan_decode(Params& p, int smem_budget, int grid) {
-  const int wf = (p.fmt == 0) ? FMT_NVFP4 : FMT_MXFP4;
+  const int wf = (p.fmt == 0) ? FMT_NVFP4 : (p.fmt == 1) ? FMT_MXFP4 : FMT_BF16;
   const int ntok = std::min(p.N, kTB);   // tokens per activation chunk
   if (!plan_kind(p.geo[KIND_AR], KIND_AR, wf, p.H, p.inter, ntok)) return false;
   if (!plan_kind(p.geo[KIND_BR], KIND_BR, wf, p.inter, p.H, ntok)) return false;
@@ -1665,19 +1758,19 @@ int decode_smem_budget(int device) {
 
 int decode_grid(int device, int smem_bytes) {
   smem_bytes += 1024;   // alignment headroom of the ring (see the kernel prologue)
-  int sms = 0, nb0 = 0, nb1 = 0;
+  int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
-  if (cudaFuncSetAttribute(moe_decode_kernel<FMT_NVFP4>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess ||
-      cudaFuncSetAttribute(moe_decode_kernel<FMT_MXFP4>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
-    return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb0, moe_decode_kernel<FMT_NVFP4>, kThreads,
-                                                    smem_bytes) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb1, moe_decode_kernel<FMT_MXFP4>, kThreads,
-                                                    smem_bytes) != cudaSuccess)
-    return 0;
-  if (nb0 < 1 || nb1 < 1) return 0;
+  const void* kernels[3] = {(const void*)moe_decode_kernel<FMT_NVFP4>,
+                            (const void*)moe_decode_kernel<FMT_MXFP4>,
+                            (const void*)moe_decode_kernel<FMT_BF16>};
+  for (const void* k : kernels) {
+    int nb = 0;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k, kThreads, smem_bytes) != cudaSuccess ||
+        nb < 1)
+      return 0;
+  }
   return sms;   // one CTA per SM
 }
 
@@ -1693,7 +1786,8 @@ cudaError_t launch_decode(const Params& p, int grid, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (p.fmt == 0) return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_NVFP4>, p);
-  return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_MXFP4>, p);
+  if (p.fmt == 1) return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_MXFP4>, p);
+  return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_BF16>, p);
 }
 
 }  // namespace moe

@@ -106,7 +106,8 @@ moe_status_t check_desc(const moe_layer_desc_t* d) {
   if (d->H <= 0 || d->inter <= 0 || d->E <= 0 || d->top_k <= 0) return MOE_ERR_INVALID_ARG;
   if (d->scoring != MOE_SCORE_SOFTMAX && d->scoring != MOE_SCORE_SIGMOID_BIAS)
     return MOE_ERR_INVALID_ARG;
-  if (d->wfmt != MOE_W_NVFP4 && d->wfmt != MOE_W_MXFP4) return MOE_ERR_INVALID_ARG;
+  if (d->wfmt != MOE_W_NVFP4 && d->wfmt != MOE_W_MXFP4 && d->wfmt != MOE_W_BF16)
+    return MOE_ERR_INVALID_ARG;
   if (d->shared_inter < 0) return MOE_ERR_INVALID_ARG;
   if (d->H % 32 || d->inter % 32 || d->shared_inter % 32) return MOE_ERR_UNSUPPORTED;
   if (d->E > moe::kMaxE || d->top_k > d->E || d->top_k > moe::kMaxTopK) return MOE_ERR_UNSUPPORTED;
@@ -115,9 +116,14 @@ moe_status_t check_desc(const moe_layer_desc_t* d) {
 
 moe_status_t check_weights(const moe_layer_desc_t* d, const moe_weights_t* w) {
   if (!w) return MOE_ERR_INVALID_ARG;
-  const void* req[] = {w->router, w->gate_q, w->up_q, w->down_q, w->gate_s, w->up_s, w->down_s};
+  const void* req[] = {w->router, w->gate_q, w->up_q, w->down_q};
   for (const void* p : req)
     if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (d->wfmt != MOE_W_BF16) {   // BF16 experts have no block scales
+    const void* sc[] = {w->gate_s, w->up_s, w->down_s};
+    for (const void* p : sc)
+      if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  }
   if (d->scoring == MOE_SCORE_SIGMOID_BIAS && !w->bias) return MOE_ERR_INVALID_ARG;
   if (d->shared_inter > 0) {
     const void* sh[] = {w->sh_gate, w->sh_up, w->sh_down};
@@ -288,6 +294,7 @@ moe_status_t run_grouped(const moe_layer_desc_t* d, const moe_weights_t* w, cons
                          int32_t N, void* out, int32_t* topk_idx, float* topk_w, void* ws,
                          size_t ws_bytes, void* stream, int route_only) {
   if (d->shared_inter > 0) return MOE_ERR_UNSUPPORTED;   // shared expert: decode sizes only
+  if (d->wfmt == MOE_W_BF16) return MOE_ERR_UNSUPPORTED;  // BF16 experts: decode sizes only
   const GWsLayout L = gws_layout(*d, N);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   int budget = 0, grid = 0;
@@ -417,12 +424,13 @@ moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* 
   p.route_only = route_only;
   p.router = static_cast<const uint16_t*>(w->router);
   p.bias = d->scoring == MOE_SCORE_SIGMOID_BIAS ? w->bias : nullptr;
-  p.gsc = w->gate_s;
-  p.usc = w->up_s;
-  p.dsc = w->down_s;
-  p.g2 = w->gate_s2;
-  p.u2 = w->up_s2;
-  p.d2 = w->down_s2;
+  const bool fp4 = d->wfmt != MOE_W_BF16;   // BF16 experts: scales are not read
+  p.gsc = fp4 ? w->gate_s : nullptr;
+  p.usc = fp4 ? w->up_s : nullptr;
+  p.dsc = fp4 ? w->down_s : nullptr;
+  p.g2 = fp4 ? w->gate_s2 : nullptr;
+  p.u2 = fp4 ? w->up_s2 : nullptr;
+  p.d2 = fp4 ? w->down_s2 : nullptr;
   p.shw = d->shared_inter > 0 ? static_cast<const uint16_t*>(w->sh_gate_w) : nullptr;
   p.x = static_cast<const uint16_t*>(x);
   p.out = static_cast<uint16_t*>(out);

@@ -85,7 +85,7 @@ struct Params {
   // layer
   int H, inter, E, k, scoring, norm;
   float rsf;
-  int fmt;   // FMT_NVFP4 / FMT_MXFP4 for the routed experts
+  int fmt;   // FMT_NVFP4 / FMT_MXFP4 / FMT_BF16 for the routed experts
   int Is;    // shared expert intermediate size (0 = none)
   int N;
   int route_only;

@@ -61,7 +61,7 @@ def test_workspace_size_grows_with_tokens(lib):
 
 
 @pytest.mark.parametrize("bad", [dict(H=100), dict(inter=48), dict(E=0), dict(top_k=9),
-                                 dict(E=2000), dict(top_k=40, E=64), dict(scoring=3), dict(wfmt=7),
+                                 dict(E=2000), dict(top_k=40, E=64), dict(scoring=3), dict(wfmt=7), dict(wfmt=3),
                                  dict(shared_inter=40)])
 def test_bad_descriptor_is_refused(lib, bad):
     assert _lib.moe_workspace_size(_desc(**bad), 1) == 0
@@ -100,6 +100,16 @@ def test_argument_refusals_happen_before_any_cuda_call(lib):
     w3 = _fake_weights()
     w3.down_s = (1 << 20) + 3
     assert _forward(lib, d, w3) == _lib.MOE_ERR_INVALID_ARG
+    w4 = _fake_weights()                                                  # FP4 experts need scales
+    w4.up_s = None
+    assert _forward(lib, d, w4) == _lib.MOE_ERR_INVALID_ARG
+    # BF16 routed experts: no grouped path yet (N*k > 256)
+    db = _desc(wfmt=_lib.MOE_W_BF16)
+    wb = _fake_weights()
+    wb.gate_s = wb.up_s = wb.down_s = wb.gate_s2 = wb.up_s2 = wb.down_s2 = None
+    assert _forward(lib, db, wb, N=300) == _lib.MOE_ERR_UNSUPPORTED
+    wb.gate_q = None
+    assert _forward(lib, db, wb) == _lib.MOE_ERR_INVALID_ARG
     ds = _desc(scoring=1)                                                 # sigmoid needs a bias
     assert _forward(lib, ds, _fake_weights()) == _lib.MOE_ERR_INVALID_ARG
     dsh = _desc(shared_inter=64)                                          # shared size, no weights

@@ -16,7 +16,7 @@ from oracle import compare, margin, oracle
 
 from .gpu_util import full_layer, run_forward, spec_from
 
-NV, MX = synth.NVFP4, synth.MXFP4
+NV, MX, BF = synth.NVFP4, synth.MXFP4, synth.BF16
 SM, SB = synth.SOFTMAX, synth.SIGMOID_BIAS
 
 SMALL = {
@@ -41,6 +41,15 @@ SMALL = {
     "n64_sweep_shape": (dict(H=128, inter=64, E=32, top_k=4), 64),
     "zero_routed_weight": (dict(H=256, inter=128, E=8, top_k=2, scoring=SB,
                                 routed_scaling_factor=0.0, shared_inter=64, shared_gated=True), 3),
+    # BF16 routed experts: 3D boxes, 2D boxes with a partial last box, several
+    # gate/up and down chunks, shared expert, sigmoid routing
+    "bf16_experts": (dict(H=256, inter=128, E=16, top_k=4, wfmt=BF), 5),
+    "bf16_experts_2d_boxes": (dict(H=160, inter=96, E=13, top_k=3, wfmt=BF), 5),
+    "bf16_experts_5_chunks_gated_shared": (dict(H=1280, inter=256, E=16, top_k=4, wfmt=BF,
+                                                shared_inter=96, shared_gated=True), 3),
+    "bf16_experts_down_3_chunks": (dict(H=256, inter=640, E=8, top_k=2, wfmt=BF), 2),
+    "bf16_experts_sigmoid_shared": (dict(H=256, inter=128, E=32, top_k=4, scoring=SB,
+                                         routed_scaling_factor=2.5, wfmt=BF, shared_inter=96), 4),
 }
 
 
@@ -99,7 +108,8 @@ def test_scale2_is_applied():
     _check(host, dev, x)
 
 
-FULL = [(name, N) for name in ("tiny", "qwen3_30b_a3b", "mtp_verify", "deepseek_v3", "gpt_oss_120b")
+FULL = [(name, N) for name in ("tiny", "qwen3_30b_a3b", "mtp_verify", "deepseek_v3", "gpt_oss_120b",
+                               "qwen3_30b_a3b_bf16")
         for N in synth.CONFIGS[name].tokens if N <= 64]
 
 
