@@ -32,6 +32,8 @@ import numpy as np
 NVFP4 = "nvfp4"
 MXFP4 = "mxfp4"
 BF16 = "bf16"
+FP8 = "fp8"
+FP8_BLOCK = 128   # FP8 experts: one FP32 scale per 128 x 128 block
 SOFTMAX = "softmax"
 SIGMOID_BIAS = "sigmoid_bias"
 
@@ -46,7 +48,7 @@ class LayerSpec:
     scoring: str            # SOFTMAX | SIGMOID_BIAS
     norm_topk_prob: bool
     routed_scaling_factor: float
-    wfmt: str               # NVFP4 | MXFP4 | BF16
+    wfmt: str               # NVFP4 | MXFP4 | BF16 | FP8
     shared_inter: int       # 0 = no shared expert
     shared_gated: bool      # sigmoid(w_s . x) gate on the shared expert
     x_rms_norm: bool        # x rows RMS-normalised before the BF16 cast
@@ -55,14 +57,18 @@ class LayerSpec:
 
     @property
     def gs(self) -> int:
-        """Block-scale group size (0 for BF16 experts, which have no scales)."""
-        return {NVFP4: 16, MXFP4: 32, BF16: 0}[self.wfmt]
+        """Block-scale group size along K (0 for BF16 experts, which have no
+        scales; FP8 blocks are 128 x 128)."""
+        return {NVFP4: 16, MXFP4: 32, BF16: 0, FP8: FP8_BLOCK}[self.wfmt]
 
     def expert_bytes(self) -> int:
         """Bytes of one routed expert (gate+up+down packed codes + block scales,
-        or BF16 words)."""
+        BF16 words, or E4M3 bytes + FP32 block scales)."""
         if self.wfmt == BF16:
             return 3 * self.inter * self.H * 2
+        if self.wfmt == FP8:
+            nb = -(-self.inter // FP8_BLOCK) * -(-self.H // FP8_BLOCK)
+            return 3 * self.inter * self.H + 3 * nb * 4
         return 3 * self.inter * self.H // 2 + 3 * self.inter * self.H // self.gs
 
     def router_bytes(self) -> int:
@@ -88,9 +94,12 @@ CONFIGS = {
     # BF16 routed experts (the pages' third expert format) on the Qwen3 shape.
     "qwen3_30b_a3b_bf16": LayerSpec("qwen3_30b_a3b_bf16", 2048, 768, 128, 8, SOFTMAX, True,
                                     1.0, BF16, 0, False, True, (1, 2, 3, 4), 16),
+    # FP8 block-scaled routed experts on the Qwen3 shape.
+    "qwen3_30b_a3b_fp8": LayerSpec("qwen3_30b_a3b_fp8", 2048, 768, 128, 8, SOFTMAX, True,
+                                   1.0, FP8, 0, False, True, (1, 2, 3, 4), 16),
 }
 CONFIG_INDEX = {"tiny": 0, "qwen3_30b_a3b": 1, "mtp_verify": 2, "deepseek_v3": 3,
-                "gpt_oss_120b": 4, "qwen3_30b_a3b_bf16": 5}
+                "gpt_oss_120b": 4, "qwen3_30b_a3b_bf16": 5, "qwen3_30b_a3b_fp8": 6}
 
 
 def base_seed(spec: LayerSpec) -> int:
@@ -178,6 +187,31 @@ def quantize_mxfp4(w: np.ndarray):
     return pack_nibbles(codes), s_code
 
 
+def quantize_fp8_block(w: np.ndarray):
+    """[rows, K] float32 -> (E4M3 bytes [rows, K], FP32 scales [ceil(rows/128),
+    ceil(K/128)]).
+
+    Per 128 x 128 block: s = amax / 448 (FP32), codes E4M3(w / s) with the
+    sign in bit 7, nearest even, saturating at 448; an all-zero block gets
+    s = 1 and zero codes."""
+    rows, K = w.shape
+    B = FP8_BLOCK
+    nr, nk = -(-rows // B), -(-K // B)
+    s = np.ones((nr, nk), dtype=np.float32)
+    q = np.zeros((rows, K), dtype=np.uint8)
+    for i in range(nr):
+        for j in range(nk):
+            blk = w[i * B:(i + 1) * B, j * B:(j + 1) * B].astype(np.float32)
+            amax = float(np.abs(blk).max()) if blk.size else 0.0
+            if amax > 0:
+                s[i, j] = np.float32(amax / 448.0)
+            r = blk.astype(np.float64) / np.float64(s[i, j])
+            code = encode_e4m3(np.abs(r))
+            neg = (r < 0) & (code != 0)
+            q[i * B:(i + 1) * B, j * B:(j + 1) * B] = code | (neg.astype(np.uint8) << np.uint8(7))
+    return q, s
+
+
 _E4M3_GRID = None
 
 
@@ -206,12 +240,12 @@ class HostLayer:
     spec: LayerSpec
     router: np.ndarray            # uint16 [E, H] BF16 bits
     bias: Optional[np.ndarray]    # float32 [E] or None
-    gate_q: np.ndarray            # uint8 [E, inter, H/2] (BF16 experts: uint16 [E, inter, H])
+    gate_q: np.ndarray            # uint8 [E, inter, H/2] (BF16: uint16 [E, inter, H]; FP8: uint8 [E, inter, H])
     up_q: np.ndarray
-    down_q: np.ndarray            # uint8 [E, H, inter/2] (BF16 experts: uint16 [E, H, inter])
-    gate_s: Optional[np.ndarray]  # uint8 [E, inter, H/gs] (None for BF16 experts)
+    down_q: np.ndarray            # uint8 [E, H, inter/2] (BF16: uint16 [E, H, inter]; FP8: uint8 [E, H, inter])
+    gate_s: Optional[np.ndarray]  # uint8 [E, inter, H/gs] (None for BF16; FP8: float32 [E, inter/128, H/128])
     up_s: Optional[np.ndarray]
-    down_s: Optional[np.ndarray]  # uint8 [E, H, inter/gs]
+    down_s: Optional[np.ndarray]  # uint8 [E, H, inter/gs] (FP8: float32 [E, H/128, inter/128])
     gate_s2: Optional[np.ndarray]  # float32 [E] (NVFP4) or None (MXFP4)
     up_s2: Optional[np.ndarray]
     down_s2: Optional[np.ndarray]
@@ -229,6 +263,8 @@ class HostLayer:
 def _quantize(spec: LayerSpec, w: np.ndarray):
     if spec.wfmt == BF16:
         return f32_to_bf16_bits(w), None
+    if spec.wfmt == FP8:
+        return quantize_fp8_block(w)
     return quantize_nvfp4(w) if spec.wfmt == NVFP4 else quantize_mxfp4(w)
 
 
@@ -252,6 +288,8 @@ def _expert_projection(spec, rng, rows, K, pool, E):
     q = qp[src]
     if spec.wfmt == BF16:                    # sign bit of every BF16 word of the row
         q ^= (flip.astype(np.uint16) * np.uint16(0x8000))[..., None]
+    elif spec.wfmt == FP8:                   # sign bit of every E4M3 byte of the row
+        q ^= (flip.astype(np.uint8) * np.uint8(0x80))[..., None]
     else:                                    # sign bits of both E2M1 codes of each byte
         q ^= (flip.astype(np.uint8) * np.uint8(0x88))[..., None]
     return q, None if sp is None else sp[src].copy()

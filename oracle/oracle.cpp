@@ -19,6 +19,11 @@
 //   * forward_batched.rs, the BF16 expert branch (bf16_gate/up/down weight
 //     pointers, "BF16 experts, with the same kernels") — BF16 routed experts,
 //     the same chain with plain BF16 weights (no block scales);
+//   * forward_k3.rs / forward_batched.rs, the FP8 expert branch (fp8 gate/up/
+//     down weight_ptrs + scale_ptrs into moe_expert_gate_up_shared_fp8 and
+//     moe_expert_silu_down_shared_fp8) — FP8 routed experts: E4M3 weights
+//     with block scales.  The pages do not give the scale granularity; the
+//     reading taken is one FP32 scale per 128 x 128 block of each projection;
 //   * forward_atomic_c4.rs, doc comment — routed outputs accumulated as
 //     routing-weighted sums, then cast to BF16 and blended with the shared
 //     expert;
@@ -123,11 +128,20 @@ double oracle_fp4_weight(const uint8_t* q, const uint8_t* s, double scale2,
 // `fmt`: 0/1 as oracle_fp4_weight; 2 = BF16 experts, the BF16 number stored in
 // the 16-bit little-endian word r*K + k of q (no block scales: s and scale2
 // are not read).
+// fmt 3 = FP8 experts: E4M3(q[r*K + k]) times the FP32 block scale
+// S[r/128][k/128] of the [ceil(rows/128), ceil(K/128)] scale table at s
+// (floats, native byte order); scale2 is not read.
 double oracle_weight(const uint8_t* q, const uint8_t* s, double scale2, int K, int fmt,
                      long r, long k) {
     if (fmt == 2) {
         const long i = 2 * (r * (long)K + k);
         return oracle_bf16((uint32_t)q[i] | ((uint32_t)q[i + 1] << 8));
+    }
+    if (fmt == 3) {
+        const long kb = (K + 127) / 128;
+        float sc;
+        std::memcpy(&sc, s + 4 * ((r / 128) * kb + k / 128), 4);
+        return oracle_e4m3(q[r * (long)K + k]) * (double)sc;
     }
     return oracle_fp4_weight(q, s, scale2, K, fmt, r, k);
 }
@@ -276,6 +290,9 @@ void oracle_shared_expert(const uint16_t* wg, const uint16_t* wu, const uint16_t
 //   *_s2 [E] f32 or null (null = 1.0; MXFP4 has none);
 //   BF16 experts (fmt 2): gate_q/up_q [E, inter, H] and down_q [E, H, inter]
 //   hold BF16 words, the scale pointers are not read;
+//   FP8 experts (fmt 3): gate_q/up_q [E, inter, H], down_q [E, H, inter] E4M3
+//   bytes; gate_s/up_s [E, ceil(inter/128), ceil(H/128)] and down_s
+//   [E, ceil(H/128), ceil(inter/128)] f32 block scales; *_s2 not read;
 //   sh_gate/sh_up [Is, H] bf16, sh_down [H, Is] bf16 (null when Is == 0);
 //   sh_gate_w [H] bf16 or null (null = ungated shared expert).
 struct oracle_weights {
@@ -298,28 +315,31 @@ int oracle_moe_forward(int H, int inter, int E, int k, int scoring, int norm, do
                        double* out_f64, uint16_t* out_bf16, int32_t* idx, double* w,
                        double* logits_out) {
     if (H <= 0 || inter <= 0 || E <= 0 || k <= 0 || k > E || N < 0) return 1;
-    if (fmt < 0 || fmt > 2) return 1;
+    if (fmt < 0 || fmt > 3) return 1;
     const int gs = (fmt == 0) ? 16 : 32;
     std::vector<double> logits((size_t)N * E);
     oracle_router_logits(x, W->router, N, E, H, logits.data());
     if (logits_out) std::copy(logits.begin(), logits.end(), logits_out);
     oracle_route(logits.data(), W->bias, N, E, k, scoring, norm, rsf, idx, w, nullptr);
 
-    // bytes per expert of each table (BF16: two bytes per element, no scales)
-    const bool bf = (fmt == 2);
-    const long gq_e = bf ? 2L * inter * H : (long)inter * (H / 2);
-    const long gs_e = bf ? 0 : (long)inter * (H / gs);
-    const long dq_e = bf ? 2L * H * inter : (long)H * (inter / 2);
-    const long ds_e = bf ? 0 : (long)H * (inter / gs);
+    // bytes per expert of each table (BF16: two bytes per element, no scales;
+    // FP8: one byte per element, 4-byte scales per 128 x 128 block)
+    const bool bf = (fmt == 2), f8 = (fmt == 3);
+    const long bi = (inter + 127) / 128, bh = (H + 127) / 128;
+    const long gq_e = bf ? 2L * inter * H : f8 ? (long)inter * H : (long)inter * (H / 2);
+    const long gs_e = bf ? 0 : f8 ? 4 * bi * bh : (long)inter * (H / gs);
+    const long dq_e = bf ? 2L * H * inter : f8 ? (long)H * inter : (long)H * (inter / 2);
+    const long ds_e = bf ? 0 : f8 ? 4 * bh * bi : (long)H * (inter / gs);
     std::vector<double> y(H), sh(H);
     for (int n = 0; n < N; ++n) {
         const uint16_t* xn = x + (long)n * H;
         std::vector<double> acc(H, 0.0);
         for (int j = 0; j < k; ++j) {
             const int e = idx[(long)n * k + j];
-            const double g2 = (!bf && W->gate_s2) ? W->gate_s2[e] : 1.0;
-            const double u2 = (!bf && W->up_s2) ? W->up_s2[e] : 1.0;
-            const double d2 = (!bf && W->down_s2) ? W->down_s2[e] : 1.0;
+            const bool fp4 = !bf && !f8;   // only the FP4 formats have scale2
+            const double g2 = (fp4 && W->gate_s2) ? W->gate_s2[e] : 1.0;
+            const double u2 = (fp4 && W->up_s2) ? W->up_s2[e] : 1.0;
+            const double d2 = (fp4 && W->down_s2) ? W->down_s2[e] : 1.0;
             oracle_expert(W->gate_q + e * gq_e, bf ? nullptr : W->gate_s + e * gs_e, g2,
                           W->up_q + e * gq_e, bf ? nullptr : W->up_s + e * gs_e, u2,
                           W->down_q + e * dq_e, bf ? nullptr : W->down_s + e * ds_e, d2,

@@ -111,7 +111,7 @@ def round_bf16(v: float) -> int:
 
 
 def fmt_code(wfmt: str) -> int:
-    return {"nvfp4": 0, "mxfp4": 1, "bf16": 2}[wfmt]
+    return {"nvfp4": 0, "mxfp4": 1, "bf16": 2, "fp8": 3}[wfmt]
 
 
 def dequant(q: np.ndarray, s: np.ndarray, scale2: float, wfmt: str) -> np.ndarray:

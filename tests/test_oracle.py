@@ -401,6 +401,82 @@ def test_bf16_expert_pool_copies_flip_whole_rows(oracle_mod):
         assert np.all(same | neg)
 
 
+def _decode_fp8_independent(q, s):
+    """Test-side FP8 decode: torch float8_e4m3fn bytes times the repeated
+    128 x 128 block scales."""
+    v = torch.from_numpy(np.ascontiguousarray(q)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    B = synth.FP8_BLOCK
+    sc = np.repeat(np.repeat(s.astype(np.float64), B, axis=0), B, axis=1)[:q.shape[0], :q.shape[1]]
+    return v * sc
+
+
+def test_fp8_quantiser_and_decode(oracle_mod):
+    """Block scale = amax/448, the block's largest element lands on +-448, and
+    every element is within half an E4M3 step of the source."""
+    rng = np.random.default_rng(31)
+    w = (rng.standard_normal((300, 200)) * 0.02).astype(np.float32)
+    w[130:140, 5:9] *= 50                                 # one loud corner
+    q, s = synth.quantize_fp8_block(w)
+    assert q.shape == (300, 200) and s.shape == (3, 2)
+    for i in range(3):
+        for j in range(2):
+            blk = w[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128]
+            assert s[i, j] == np.float32(np.abs(blk).max() / 448.0)
+    dq = _decode_fp8_independent(q, s)
+    for (r, k) in ((0, 0), (129, 7), (299, 199), (131, 6), (5, 150)):
+        assert oracle_mod.weight(q, s, 1.0, 200, synth.FP8, r, k) == dq[r, k]
+    sc = np.repeat(np.repeat(s.astype(np.float64), 128, 0), 128, 1)[:300, :200]
+    a = np.abs(w.astype(np.float64)) / sc                 # magnitude in E4M3 units
+    step = np.where(a < 2.0 ** -6, 2.0 ** -9, 2.0 ** (np.floor(np.log2(np.maximum(a, 2.0 ** -6))) - 3))
+    assert np.all(np.abs(dq - w) <= 0.5 * step * sc * (1 + 1e-9))
+    assert np.abs(_decode_fp8_independent(q, s)).max() == pytest.approx(np.abs(w).max(), rel=1e-7)
+
+
+def test_fp8_experts_equal_bf16_experts_with_the_same_values(oracle_mod):
+    """FP8 routed experts whose block scales are powers of two hold BF16
+    numbers exactly (4 significant bits); the layer then equals the BF16-expert
+    layer with those values to the last bit.  Rows > 128 give several row
+    blocks per projection."""
+    import dataclasses
+    sp = _small_spec(E=5, top_k=2, H=256, inter=160, wfmt=synth.FP8)
+    L = synth.make_layer(sp, seed=33)
+    rng = np.random.default_rng(34)
+    for a in (L.gate_s, L.up_s, L.down_s):
+        a[:] = np.ldexp(1.0, rng.integers(-13, -6, size=a.shape)).astype(np.float32)
+
+    def conv(q, s):
+        out = []
+        for e in range(q.shape[0]):
+            v = _decode_fp8_independent(q[e], s[e])
+            bits = synth.f32_to_bf16_bits(v.astype(np.float32))
+            assert np.array_equal(_bf16_arr(bits), v)
+            out.append(bits)
+        return np.stack(out)
+
+    Lb = dataclasses.replace(L, spec=dataclasses.replace(sp, wfmt=synth.BF16),
+                             gate_q=conv(L.gate_q, L.gate_s), up_q=conv(L.up_q, L.up_s),
+                             down_q=conv(L.down_q, L.down_s), gate_s=None, up_s=None, down_s=None)
+    x = synth.make_tokens(sp, 3, seed=35)
+    r, rb = oracle_mod.moe_forward(L, x), oracle_mod.moe_forward(Lb, x)
+    assert set(r["idx"].ravel()) - {0}
+    np.testing.assert_array_equal(r["out_f64"], rb["out_f64"])
+
+
+def test_fp8_single_expert_equals_dense_swiglu(oracle_mod):
+    sp = _small_spec(E=1, top_k=1, H=320, inter=192, wfmt=synth.FP8)
+    L = synth.make_layer(sp, seed=36)
+    x = synth.make_tokens(sp, 2, seed=37)
+    r = oracle_mod.moe_forward(L, x)
+    Wg = _decode_fp8_independent(L.gate_q[0], L.gate_s[0])
+    Wu = _decode_fp8_independent(L.up_q[0], L.up_s[0])
+    Wd = _decode_fp8_independent(L.down_q[0], L.down_s[0])
+    for n in range(2):
+        x64 = _bf16_arr(x[n])
+        g, u = Wg @ x64, Wu @ x64
+        np.testing.assert_allclose(r["out_f64"][n], Wd @ (g * scipy.special.expit(g) * u),
+                                   rtol=1e-12, atol=1e-15)
+
+
 def test_scale2_scales_each_projection(oracle_mod):
     sp = _small_spec(E=1, top_k=1)
     L = synth.make_layer(sp, seed=13)

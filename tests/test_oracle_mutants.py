@@ -40,6 +40,10 @@ MUTANTS = {
     "bf16_adjacent_swap": ("const long i = 2 * (r * (long)K + k);",
                            "const long i = 2 * ((r * (long)K + k) ^ 1);"),
     "bf16_expert_stride": ("const long gq_e = bf ? 2L * inter * H", "const long gq_e = bf ? 1L * inter * H"),
+    "fp8_row_block_ignored": ("s + 4 * ((r / 128) * kb + k / 128)", "s + 4 * (k / 128)"),
+    "fp8_scale_ignored": ("return oracle_e4m3(q[r * (long)K + k]) * (double)sc;",
+                          "return oracle_e4m3(q[r * (long)K + k]) * (sc > 0 ? 1.0 : 0.0);"),
+    "fp8_scale_stride": ("const long gs_e = bf ? 0 : f8 ? 4 * bi * bh", "const long gs_e = bf ? 0 : f8 ? 4 * bi"),
     "router_transposed": ("oracle_bf16(wr[(long)e * H + h])", "oracle_bf16(wr[(long)h * E + e])"),
     "shared_gate_no_sigmoid": ("gsig = 1.0 / (1.0 + std::exp(-d));", "gsig = d;"),
     "shared_down_dropped": ("acc[h] += gsig * sh[h];", "acc[h] += gsig;"),
