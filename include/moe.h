@@ -10,7 +10,9 @@
  *   3. routed experts  SwiGLU with block-scaled FP4 weights:
  *                      h = SiLU(Dq(Wg) x) * (Dq(Wu) x),  y = Dq(Wd) h,
  *                      Dq(w) = E2M1(code) * blockscale * scale2;
- *                      or with plain BF16 weights (Dq(w) = w);
+ *                      or with plain BF16 weights (Dq(w) = w), or with
+ *                      FP8 weights (Dq(w) = E4M3(code) * blockscale, one
+ *                      FP32 scale per 128 x 128 block);
  *   4. output          out[n] = BF16( sum_j w[n,j] * y_{idx[n,j]}
  *                                     + g_s(x_n) * shared(x_n) ),
  *                      g_s = sigmoid(w_s . x_n) if a shared-expert gate vector
@@ -31,7 +33,11 @@
  *   - forward_batched.rs: one router GEMM for N rows, per-token routing, and
  *     "each routed and shared expert streams its weights once for all rows";
  *     its BF16 expert branch (bf16 gate/up/down weight pointers, the same
- *     kernels as the FP4 forward) for the BF16 routed-expert format.
+ *     kernels as the FP4 forward) for the BF16 routed-expert format, and the
+ *     FP8 expert branch (weight_ptrs + scale_ptrs of moe_expert_gate_up_
+ *     shared_fp8 / moe_expert_silu_down_shared_fp8).  The pages do not give the
+ *     FP8 scale granularity; this library takes one FP32 scale per 128 x 128
+ *     block of each projection.
  *
  * Memory: every pointer passed to moe_forward / moe_route is a DEVICE pointer
  * (weights, x, out, topk outputs, workspace) unless the name says _host.  The
@@ -52,6 +58,10 @@
  * BF16 routed experts (wfmt MOE_W_BF16): gate_q, up_q [E, inter, H] bf16 and
  *   down_q [E, H, inter] bf16; the scale pointers and *_s2 are not read (NULL
  *   allowed).
+ * FP8 routed experts (wfmt MOE_W_FP8): gate_q, up_q [E, inter, H] and down_q
+ *   [E, H, inter] E4M3 bytes (OCP "fn"); gate_s, up_s point to f32
+ *   [E, ceil(inter/128), ceil(H/128)] and down_s to f32 [E, ceil(H/128),
+ *   ceil(inter/128)] block scales; *_s2 are not read.
  *   sh_gate, sh_up [Is, H] bf16; sh_down [H, Is] bf16  (NULL when Is == 0)
  *   sh_gate_w  [H] bf16 or NULL (NULL = ungated, always-on shared expert)
  * All weight, x, out and workspace pointers must be 16-byte aligned.
@@ -85,8 +95,9 @@ typedef enum {
 
 typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID_BIAS = 1 } moe_scoring_t;
 /* Routed-expert weight formats: NVFP4 (E2M1 + per-16 E4M3 scale + FP32
- * scale2), MXFP4 (E2M1 + per-32 E8M0 scale), BF16 (plain weights). */
-typedef enum { MOE_W_NVFP4 = 0, MOE_W_MXFP4 = 1, MOE_W_BF16 = 2 } moe_wfmt_t;
+ * scale2), MXFP4 (E2M1 + per-32 E8M0 scale), BF16 (plain weights), FP8 (E4M3
+ * + FP32 scale per 128 x 128 block). */
+typedef enum { MOE_W_NVFP4 = 0, MOE_W_MXFP4 = 1, MOE_W_BF16 = 2, MOE_W_FP8 = 3 } moe_wfmt_t;
 
 /* Layer configuration: the config fields the pages' MoE forward reads
  * (hidden_size, moe_intermediate_size, num_experts, num_experts_per_tok,
@@ -147,8 +158,9 @@ MOE_API moe_status_t moe_workspace_init(void* workspace, size_t ws_bytes, void* 
  * N*top_k <= 256 runs one fused decode kernel; larger N runs the grouped
  * path (per-expert token groups on the tcgen05 tensor cores, the pages'
  * "grouped GEMM (more than 64 rows)" of forward_batched.rs), which takes
- * neither a shared expert nor BF16 routed experts yet: N*top_k > 256 with
- * shared_inter > 0 or wfmt MOE_W_BF16 returns MOE_ERR_UNSUPPORTED.  Asynchronous on `stream`; no host synchronisation,
+ * neither a shared expert nor BF16 / FP8 routed experts yet: N*top_k > 256
+ * with shared_inter > 0 or wfmt MOE_W_BF16 / MOE_W_FP8 returns
+ * MOE_ERR_UNSUPPORTED.  Asynchronous on `stream`; no host synchronisation,
  * no allocation, so it may be captured in a CUDA graph.  Argument errors are
  * returned before anything is enqueued; device-side timeouts are reported by
  * moe_get_error. */

@@ -26,6 +26,7 @@ MOE_SCORE_SIGMOID_BIAS = 1
 MOE_W_NVFP4 = 0
 MOE_W_MXFP4 = 1
 MOE_W_BF16 = 2
+MOE_W_FP8 = 3
 
 EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_forward", "moe_route",
             "moe_host_staging_size", "moe_forward_host", "moe_get_error", "moe_status_string",

@@ -591,7 +591,7 @@ __device__ __forceinline__ void produce_weights(const Params& p, int row0, int c
 // K elements of chunk c.
 __device__ __forceinline__ int chunk_elems(const Geo& g, int c) {
   const int rb = chunk_row_bytes(g, c);
-  return g.fmt == FMT_BF16 ? rb / 2 : rb * 2;
+  return g.fmt == FMT_BF16 ? rb / 2 : g.fmt == FMT_FP8 ? rb : rb * 2;
 }
 
 template <int KIND>
@@ -1046,6 +1046,48 @@ __device__ __forceinline__ void compute_bf16_ar(const uint8_t* st, const SG& g,
   }
 }
 
+// One stage of FP8 routed gate/up weights (16 gate rows over 16 up rows,
+// lane = row) for NT tokens against the scaled f16 x chunk; a step is 32
+// elements = 32 bytes of a row.  E4M3 -> f16 is exact, products and sums in
+// f32; each step is scaled by its 128 x 128 block scale (srow: this lane's
+// row of block scales, indexed by K / 128).
+template <int NT>
+__device__ __forceinline__ void compute_fp8_ar(const uint8_t* st, const SG& g, int c,
+                                               const uint8_t* obase, int otstride, int s0,
+                                               int s1, int lane, const float* srow,
+                                               float (&acc)[1][NT]) {
+#pragma unroll 1
+  for (int s = s0; s < s1; ++s) {
+    const float sc = __ldg(srow + ((c * g.Kc + s * 32) >> 7));
+    const uint4 w0 = lds<uint4>(wptr_ar(st, g.kb, lane, 2 * s));
+    const uint4 w1 = lds<uint4>(wptr_ar(st, g.kb, lane, 2 * s + 1));
+    const uint32_t wb[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    uint32_t wv[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      wv[2 * i] = e4m3x2_to_f16x2(wb[i] & 0xFFFFu);
+      wv[2 * i + 1] = e4m3x2_to_f16x2(wb[i] >> 16);
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const uint8_t* oa = obase + t * otstride + s * 64;
+      uint32_t xo[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 x = lds<uint4>(oa + q * 16);
+        xo[4 * q + 0] = x.x; xo[4 * q + 1] = x.y; xo[4 * q + 2] = x.z; xo[4 * q + 3] = x.w;
+      }
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; e += 2) {
+        a0 = fma2_f16_to_f32(wv[e], xo[e], a0);
+        a1 = fma2_f16_to_f32(wv[e + 1], xo[e + 1], a1);
+      }
+      acc[0][t] = fmaf(a0 + a1, sc, acc[0][t]);
+    }
+  }
+}
+
 // One stage of BF16 weights (shared expert) for NT tokens; a step is 32
 // elements = 64 bytes of a row.
 template <int NPROJ, int NT>
@@ -1209,6 +1251,50 @@ __device__ __forceinline__ void compute_dn_bf16r(const uint8_t* st, const SG& g,
   }
 }
 
+// One chunk of a routed down job with FP8 weights: 16 rows (row = lane & 15)
+// against the f16 h of NT tokens; a step is 32 elements (32 bytes of a row),
+// its two 16-element halves scaled by 2^(h exponent) and the step by its
+// 128 x 128 block scale (srow: the 16 rows' row of block scales); the
+// half-warp covers steps [p0, p1).  Products and sums in f32.
+template <int NT>
+__device__ __forceinline__ void compute_dn_fp8(const uint8_t* st, const SG& g, int c, int p0,
+                                               int p1, int row, const float* srow,
+                                               float (&acc)[kTB]) {
+  const uint8_t* ob = st + g.opnd_off;
+  const uint8_t* hx = st + g.hx_off;
+  for (int s = p0; s < p1; ++s) {
+    const float sc = __ldg(srow + ((c * g.Kc + s * 32) >> 7));
+    const uint4 w0 = lds<uint4>(wptr16(st, g.kb, row, 2 * s));
+    const uint4 w1 = lds<uint4>(wptr16(st, g.kb, row, 2 * s + 1));
+    const uint32_t wb[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    uint32_t wv[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      wv[2 * i] = e4m3x2_to_f16x2(wb[i] & 0xFFFFu);
+      wv[2 * i + 1] = e4m3x2_to_f16x2(wb[i] >> 16);
+    }
+    const float f0 = sc * pow2i((int8_t)lds<uint8_t>(hx + 2 * s));
+    const float f1 = sc * pow2i((int8_t)lds<uint8_t>(hx + 2 * s + 1));
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const uint8_t* oa = ob + t * g.Kc * 2 + s * 64;
+      uint32_t xo[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 x = lds<uint4>(oa + q * 16);
+        xo[4 * q + 0] = x.x; xo[4 * q + 1] = x.y; xo[4 * q + 2] = x.z; xo[4 * q + 3] = x.w;
+      }
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        a0 = fma2_f16_to_f32(wv[e], xo[e], a0);
+        a1 = fma2_f16_to_f32(wv[8 + e], xo[8 + e], a1);
+      }
+      acc[t] = fmaf(a0, f0, fmaf(a1, f1, acc[t]));
+    }
+  }
+}
+
 // One chunk of a shared-expert down job: BF16 weights against BF16 h; a step
 // is 32 elements (64 bytes) of the row, the half-warp covers steps [p0, p1).
 template <int NT>
@@ -1339,8 +1425,9 @@ __device__ __noinline__ int epilogue_kind(const Params& p, Tables& tb, const Con
 // warps' partial sums in `red` (layout [warp][proj][token][lane]).
 template <int FMT, int NPROJ, int KIND, int NT>
 __device__ __forceinline__ void consume_rg(const Params& p, Tables& tb, const ConsumerCtx& cx,
-                                           const SG& g, int& ctr, int warp, int lane, float* red) {
-  constexpr int kStepBytes = (FMT == FMT_BF16) ? 64 : 16;
+                                           const SG& g, int& ctr, int warp, int lane, float* red,
+                                           const float* srow) {
+  constexpr int kStepBytes = (FMT == FMT_BF16) ? 64 : (FMT == FMT_FP8) ? 32 : 16;
   float acc[NPROJ][NT];
 #pragma unroll
   for (int a = 0; a < NPROJ; ++a)
@@ -1362,6 +1449,8 @@ __device__ __forceinline__ void consume_rg(const Params& p, Tables& tb, const Co
       const int ots = g.Kc * 2;
       if constexpr (FMT == FMT_BF16 && KIND == KIND_AR)
         compute_bf16_ar<NT>(st, g, ob, ots, s0, s1, lane, acc);
+      else if constexpr (FMT == FMT_FP8)
+        compute_fp8_ar<NT>(st, g, c, ob, ots, s0, s1, lane, srow, acc);
       else if constexpr (FMT == FMT_BF16)
         compute_bf16<NPROJ, NT>(st, g, ob, ots, s0, s1, lane, acc);
       else
@@ -1397,11 +1486,18 @@ __device__ __noinline__ void consume_kind(const Params& p, Tables& tb, const Con
         lane == 0)
       set_abort(p, tb, kErrTimeoutStage);
     float* red = cx.red + buf * kRedFloats;
+    const float* srow = nullptr;   // FP8: this lane's row of 128 x 128 block scales
+    if constexpr (FMT == FMT_FP8) {
+      const int nkb = (p.H + kFp8Block - 1) / kFp8Block;
+      const int nrb = (p.inter + kFp8Block - 1) / kFp8Block;
+      const float* tab = reinterpret_cast<const float*>(lane < 16 ? p.gsc : p.usc);
+      srow = tab + ((size_t)r.e * nrb + (r.rg * kDnRows) / kFp8Block) * nkb;
+    }
     switch (r.nt) {
-      case 1: consume_rg<FMT, NPROJ, KIND, 1>(p, tb, cx, g, ctr, warp, lane, red); break;
-      case 2: consume_rg<FMT, NPROJ, KIND, 2>(p, tb, cx, g, ctr, warp, lane, red); break;
-      case 3: consume_rg<FMT, NPROJ, KIND, 3>(p, tb, cx, g, ctr, warp, lane, red); break;
-      default: consume_rg<FMT, NPROJ, KIND, 4>(p, tb, cx, g, ctr, warp, lane, red); break;
+      case 1: consume_rg<FMT, NPROJ, KIND, 1>(p, tb, cx, g, ctr, warp, lane, red, srow); break;
+      case 2: consume_rg<FMT, NPROJ, KIND, 2>(p, tb, cx, g, ctr, warp, lane, red, srow); break;
+      case 3: consume_rg<FMT, NPROJ, KIND, 3>(p, tb, cx, g, ctr, warp, lane, red, srow); break;
+      default: consume_rg<FMT, NPROJ, KIND, 4>(p, tb, cx, g, ctr, warp, lane, red, srow); break;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(cx.rfull + buf);
@@ -1438,11 +1534,18 @@ __device__ __noinline__ void consume_down(const Params& p, Tables& tb, const Con
       const SG& g = routed ? gr : gsh;
       int nt, src0;
       float d2 = 1.0f;   // down scale2, loaded at job start (latency hidden by the compute)
+      const float* srow = nullptr;   // FP8: the block's row of 128 x 128 block scales
       if (routed) {
         const int u = tb.unit_u[jb], tbi = tb.unit_tb[jb];
         nt = min(kTB, (int)tb.ucnt[u] - tbi * kTB);
         src0 = tb.hoff[u] + tbi * kTB;
         if (own && p.d2) d2 = __ldg(p.d2 + tb.uexp[u]);
+        if constexpr (FMT == FMT_FP8) {
+          const int nkb = (p.inter + kFp8Block - 1) / kFp8Block;
+          const int nrb = (p.H + kFp8Block - 1) / kFp8Block;
+          srow = reinterpret_cast<const float*>(p.dsc) +
+                 ((size_t)tb.uexp[u] * nrb + ((cta + i * G) * kDnRows) / kFp8Block) * nkb;
+        }
       } else {
         const int b = jb - nr;
         nt = min(kTB, p.N - b * kTB);
@@ -1471,6 +1574,15 @@ __device__ __noinline__ void consume_down(const Params& p, Tables& tb, const Con
                 case 2: compute_dn_bf16r<2>(st, g, p0, p1, row, acc); break;
                 case 3: compute_dn_bf16r<3>(st, g, p0, p1, row, acc); break;
                 default: compute_dn_bf16r<4>(st, g, p0, p1, row, acc); break;
+              }
+            } else if constexpr (FMT == FMT_FP8) {
+              const int np = rb / 32;
+              const int p0 = slice * np / nslice, p1 = (slice + 1) * np / nslice;
+              switch (nt) {
+                case 1: compute_dn_fp8<1>(st, g, c, p0, p1, row, srow, acc); break;
+                case 2: compute_dn_fp8<2>(st, g, c, p0, p1, row, srow, acc); break;
+                case 3: compute_dn_fp8<3>(st, g, c, p0, p1, row, srow, acc); break;
+                default: compute_dn_fp8<4>(st, g, c, p0, p1, row, srow, acc); break;
               }
             } else {
               const int np = rb / 16;
@@ -1670,8 +1782,8 @@ static bool plan_kind(Geo& g, int kind, int fmt, int K, int rows, int ntok) {
   g.rows_total = rows;
   g.opnd_off = -1;
   if (K % 32 != 0 || rows % g.rg_rows != 0 || K <= 0 || rows <= 0) return false;
-  g.kb = (fmt == FMT_BF16) ? K * 2 : K / 2;
-  g.Kc = (fmt == FMT_BF16) ? kChunkBytes / 2 : kChunkBytes * 2;
+  g.kb = (fmt == FMT_BF16) ? K * 2 : (fmt == FMT_FP8) ? K : K / 2;
+  g.Kc = (fmt == FMT_BF16) ? kChunkBytes / 2 : (fmt == FMT_FP8) ? kChunkBytes : kChunkBytes * 2;
   g.nchunks = (g.kb + kChunkBytes - 1) / kChunkBytes;
   const bool sw = g.kb >= kBoxBytes;
   // AS: one 32-row tile per projection; AR: gate and up 16-row boxes stacked
@@ -1692,7 +1804,7 @@ static bool plan_kind(Geo& g, int kind, int fmt, int K, int rows, int ntok) {
   g.scale_off = off;
   g.sr = g.scb = 0;
   g.scale_mode = SCALES_NONE;
-  if (fmt != FMT_BF16) {
+  if (fmt == FMT_NVFP4 || fmt == FMT_MXFP4) {   // FP8 block scales are read from global
     const int gs = (fmt == FMT_NVFP4) ? 16 : 32;
     g.sr = K / gs;
     if (g.sr % 16 == 0) {
@@ -1714,7 +1826,8 @@ static bool plan_kind(Geo& g, int kind, int fmt, int K, int rows, int ntok) {
 }
 
 bool plan_decode(Params& p, int smem_budget, int grid) {
-  const int wf = (p.fmt == 0) ? FMT_NVFP4 : (p.fmt == 1) ? FMT_MXFP4 : FMT_BF16;
+  const int wf = (p.fmt == 0) ? FMT_NVFP4 : (p.fmt == 1) ? FMT_MXFP4
+               : (p.fmt == 2) ? FMT_BF16 : FMT_FP8;
   const int ntok = std::min(p.N, kTB);   // tokens per activation chunk
   if (!plan_kind(p.geo[KIND_AR], KIND_AR, wf, p.H, p.inter, ntok)) return false;
   if (!plan_kind(p.geo[KIND_BR], KIND_BR, wf, p.inter, p.H, ntok)) return false;
@@ -1760,9 +1873,10 @@ int decode_grid(int device, int smem_bytes) {
   smem_bytes += 1024;   // alignment headroom of the ring (see the kernel prologue)
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
-  const void* kernels[3] = {(const void*)moe_decode_kernel<FMT_NVFP4>,
+  const void* kernels[4] = {(const void*)moe_decode_kernel<FMT_NVFP4>,
                             (const void*)moe_decode_kernel<FMT_MXFP4>,
-                            (const void*)moe_decode_kernel<FMT_BF16>};
+                            (const void*)moe_decode_kernel<FMT_BF16>,
+                            (const void*)moe_decode_kernel<FMT_FP8>};
   for (const void* k : kernels) {
     int nb = 0;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
@@ -1787,7 +1901,8 @@ cudaError_t launch_decode(const Params& p, int grid, cudaStream_t stream) {
   cfg.numAttrs = 1;
   if (p.fmt == 0) return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_NVFP4>, p);
   if (p.fmt == 1) return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_MXFP4>, p);
-  return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_BF16>, p);
+  if (p.fmt == 2) return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_BF16>, p);
+  return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_FP8>, p);
 }
 
 }  // namespace moe

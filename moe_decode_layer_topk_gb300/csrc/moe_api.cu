@@ -106,7 +106,8 @@ moe_status_t check_desc(const moe_layer_desc_t* d) {
   if (d->H <= 0 || d->inter <= 0 || d->E <= 0 || d->top_k <= 0) return MOE_ERR_INVALID_ARG;
   if (d->scoring != MOE_SCORE_SOFTMAX && d->scoring != MOE_SCORE_SIGMOID_BIAS)
     return MOE_ERR_INVALID_ARG;
-  if (d->wfmt != MOE_W_NVFP4 && d->wfmt != MOE_W_MXFP4 && d->wfmt != MOE_W_BF16)
+  if (d->wfmt != MOE_W_NVFP4 && d->wfmt != MOE_W_MXFP4 && d->wfmt != MOE_W_BF16 &&
+      d->wfmt != MOE_W_FP8)
     return MOE_ERR_INVALID_ARG;
   if (d->shared_inter < 0) return MOE_ERR_INVALID_ARG;
   if (d->H % 32 || d->inter % 32 || d->shared_inter % 32) return MOE_ERR_UNSUPPORTED;
@@ -294,7 +295,8 @@ moe_status_t run_grouped(const moe_layer_desc_t* d, const moe_weights_t* w, cons
                          int32_t N, void* out, int32_t* topk_idx, float* topk_w, void* ws,
                          size_t ws_bytes, void* stream, int route_only) {
   if (d->shared_inter > 0) return MOE_ERR_UNSUPPORTED;   // shared expert: decode sizes only
-  if (d->wfmt == MOE_W_BF16) return MOE_ERR_UNSUPPORTED;  // BF16 experts: decode sizes only
+  if (d->wfmt == MOE_W_BF16 || d->wfmt == MOE_W_FP8)
+    return MOE_ERR_UNSUPPORTED;   // BF16 / FP8 experts: decode sizes only
   const GWsLayout L = gws_layout(*d, N);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   int budget = 0, grid = 0;
@@ -424,10 +426,13 @@ moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* 
   p.route_only = route_only;
   p.router = static_cast<const uint16_t*>(w->router);
   p.bias = d->scoring == MOE_SCORE_SIGMOID_BIAS ? w->bias : nullptr;
-  const bool fp4 = d->wfmt != MOE_W_BF16;   // BF16 experts: scales are not read
-  p.gsc = fp4 ? w->gate_s : nullptr;
-  p.usc = fp4 ? w->up_s : nullptr;
-  p.dsc = fp4 ? w->down_s : nullptr;
+  // BF16 experts read no scales; FP8 experts their f32 block scales; only
+  // the FP4 formats have scale2
+  const bool scales = d->wfmt != MOE_W_BF16;
+  const bool fp4 = d->wfmt == MOE_W_NVFP4 || d->wfmt == MOE_W_MXFP4;
+  p.gsc = scales ? w->gate_s : nullptr;
+  p.usc = scales ? w->up_s : nullptr;
+  p.dsc = scales ? w->down_s : nullptr;
   p.g2 = fp4 ? w->gate_s2 : nullptr;
   p.u2 = fp4 ? w->up_s2 : nullptr;
   p.d2 = fp4 ? w->down_s2 : nullptr;

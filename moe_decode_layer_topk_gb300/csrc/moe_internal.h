@@ -35,7 +35,8 @@ constexpr int kReadyAS = kMaxSlots;               // ready[] index of the shared
 // AS shared gate/up (32-row groups), AR routed gate/up (16 gate + 16 up rows
 // stacked as one 32-row tile), BR routed down / BS shared down (16-row blocks).
 enum Kind { KIND_AS = 0, KIND_AR = 1, KIND_BR = 2, KIND_BS = 3 };
-enum Fmt { FMT_NVFP4 = 0, FMT_MXFP4 = 1, FMT_BF16 = 2 };
+enum Fmt { FMT_NVFP4 = 0, FMT_MXFP4 = 1, FMT_BF16 = 2, FMT_FP8 = 3 };
+constexpr int kFp8Block = 128;   // FP8 experts: one FP32 scale per 128 x 128 block
 enum ScaleMode { SCALES_NONE = 0, SCALES_TMAP = 1, SCALES_BLOCK = 2 };
 // tensor map slots
 // 2D maps of weight rows (boxes of 128 bytes x brows), of scales, and 3D
@@ -85,14 +86,14 @@ struct Params {
   // layer
   int H, inter, E, k, scoring, norm;
   float rsf;
-  int fmt;   // FMT_NVFP4 / FMT_MXFP4 / FMT_BF16 for the routed experts
+  int fmt;   // FMT_NVFP4 / FMT_MXFP4 / FMT_BF16 / FMT_FP8 for the routed experts
   int Is;    // shared expert intermediate size (0 = none)
   int N;
   int route_only;
   // weights (device)
   const uint16_t* router;
   const float* bias;
-  const uint8_t *gsc, *usc, *dsc;   // scales, for 1D block copies
+  const uint8_t *gsc, *usc, *dsc;   // FP4 scales (1D block copies); FP8: f32 block scales
   const float *g2, *u2, *d2;
   const uint16_t* shw;
   // activations / outputs (device)

@@ -11,7 +11,7 @@ import numpy as np
 import torch
 
 from . import _lib
-from .synth import BF16, HostLayer, LayerSpec, MXFP4, NVFP4, SOFTMAX
+from .synth import BF16, FP8, HostLayer, LayerSpec, MXFP4, NVFP4, SOFTMAX
 
 
 def layer_desc(spec: LayerSpec) -> _lib.LayerDesc:
@@ -20,7 +20,8 @@ def layer_desc(spec: LayerSpec) -> _lib.LayerDesc:
     d.scoring = _lib.MOE_SCORE_SOFTMAX if spec.scoring == SOFTMAX else _lib.MOE_SCORE_SIGMOID_BIAS
     d.norm_topk_prob = int(spec.norm_topk_prob)
     d.routed_scaling_factor = float(spec.routed_scaling_factor)
-    d.wfmt = {NVFP4: _lib.MOE_W_NVFP4, MXFP4: _lib.MOE_W_MXFP4, BF16: _lib.MOE_W_BF16}[spec.wfmt]
+    d.wfmt = {NVFP4: _lib.MOE_W_NVFP4, MXFP4: _lib.MOE_W_MXFP4, BF16: _lib.MOE_W_BF16,
+              FP8: _lib.MOE_W_FP8}[spec.wfmt]
     d.shared_inter = spec.shared_inter
     return d
 

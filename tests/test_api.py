@@ -61,7 +61,7 @@ def test_workspace_size_grows_with_tokens(lib):
 
 
 @pytest.mark.parametrize("bad", [dict(H=100), dict(inter=48), dict(E=0), dict(top_k=9),
-                                 dict(E=2000), dict(top_k=40, E=64), dict(scoring=3), dict(wfmt=7), dict(wfmt=3),
+                                 dict(E=2000), dict(top_k=40, E=64), dict(scoring=3), dict(wfmt=7), dict(wfmt=4),
                                  dict(shared_inter=40)])
 def test_bad_descriptor_is_refused(lib, bad):
     assert _lib.moe_workspace_size(_desc(**bad), 1) == 0
@@ -110,6 +110,12 @@ def test_argument_refusals_happen_before_any_cuda_call(lib):
     assert _forward(lib, db, wb, N=300) == _lib.MOE_ERR_UNSUPPORTED
     wb.gate_q = None
     assert _forward(lib, db, wb) == _lib.MOE_ERR_INVALID_ARG
+    # FP8 routed experts: block scales required, no grouped path yet
+    d8 = _desc(wfmt=_lib.MOE_W_FP8)
+    w8 = _fake_weights()
+    assert _forward(lib, d8, w8, N=300) == _lib.MOE_ERR_UNSUPPORTED
+    w8.down_s = None
+    assert _forward(lib, d8, w8) == _lib.MOE_ERR_INVALID_ARG
     ds = _desc(scoring=1)                                                 # sigmoid needs a bias
     assert _forward(lib, ds, _fake_weights()) == _lib.MOE_ERR_INVALID_ARG
     dsh = _desc(shared_inter=64)                                          # shared size, no weights

@@ -16,7 +16,7 @@ from oracle import compare, margin, oracle
 
 from .gpu_util import full_layer, run_forward, spec_from
 
-NV, MX, BF = synth.NVFP4, synth.MXFP4, synth.BF16
+NV, MX, BF, F8 = synth.NVFP4, synth.MXFP4, synth.BF16, synth.FP8
 SM, SB = synth.SOFTMAX, synth.SIGMOID_BIAS
 
 SMALL = {
@@ -50,6 +50,15 @@ SMALL = {
     "bf16_experts_down_3_chunks": (dict(H=256, inter=640, E=8, top_k=2, wfmt=BF), 2),
     "bf16_experts_sigmoid_shared": (dict(H=256, inter=128, E=32, top_k=4, scoring=SB,
                                          routed_scaling_factor=2.5, wfmt=BF, shared_inter=96), 4),
+    # FP8 block-scaled routed experts: several 128-row and 128-column scale
+    # blocks, ragged blocks, 2D boxes, several chunks, shared expert, sigmoid
+    "fp8_experts": (dict(H=256, inter=256, E=16, top_k=4, wfmt=F8), 5),
+    "fp8_experts_ragged_blocks": (dict(H=160, inter=160, E=13, top_k=3, wfmt=F8), 5),
+    "fp8_experts_4_chunks_gated_shared": (dict(H=2048, inter=384, E=16, top_k=4, wfmt=F8,
+                                               shared_inter=96, shared_gated=True), 3),
+    "fp8_experts_down_3_chunks": (dict(H=256, inter=1152, E=8, top_k=2, wfmt=F8), 2),
+    "fp8_experts_sigmoid": (dict(H=512, inter=256, E=32, top_k=4, scoring=SB,
+                                 routed_scaling_factor=2.5, wfmt=F8), 4),
 }
 
 
@@ -109,7 +118,7 @@ def test_scale2_is_applied():
 
 
 FULL = [(name, N) for name in ("tiny", "qwen3_30b_a3b", "mtp_verify", "deepseek_v3", "gpt_oss_120b",
-                               "qwen3_30b_a3b_bf16")
+                               "qwen3_30b_a3b_bf16", "qwen3_30b_a3b_fp8")
         for N in synth.CONFIGS[name].tokens if N <= 64]
 
 
