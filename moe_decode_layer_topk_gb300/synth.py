@@ -54,6 +54,7 @@ class LayerSpec:
     x_rms_norm: bool        # x rows RMS-normalised before the BF16 cast
     tokens: tuple           # token counts the layer is run at
     pool: int               # distinct experts drawn per projection
+    router_fmt: str = BF16  # BF16 router, or NVFP4 (E2M1 + per-16 E4M3 + scale2)
 
     @property
     def gs(self) -> int:
@@ -72,6 +73,8 @@ class LayerSpec:
         return 3 * self.inter * self.H // 2 + 3 * self.inter * self.H // self.gs
 
     def router_bytes(self) -> int:
+        if self.router_fmt == NVFP4:
+            return self.E * self.H // 2 + self.E * self.H // 16
         return self.E * self.H * 2
 
     def shared_bytes(self) -> int:
@@ -97,9 +100,14 @@ CONFIGS = {
     # FP8 block-scaled routed experts on the Qwen3 shape.
     "qwen3_30b_a3b_fp8": LayerSpec("qwen3_30b_a3b_fp8", 2048, 768, 128, 8, SOFTMAX, True,
                                    1.0, FP8, 0, False, True, (1, 2, 3, 4), 16),
+    # NVFP4-quantised router on the Qwen3 shape.
+    "qwen3_30b_a3b_nvfp4_router": LayerSpec("qwen3_30b_a3b_nvfp4_router", 2048, 768, 128, 8,
+                                            SOFTMAX, True, 1.0, NVFP4, 0, False, True,
+                                            (1, 2, 3, 4), 16, NVFP4),
 }
 CONFIG_INDEX = {"tiny": 0, "qwen3_30b_a3b": 1, "mtp_verify": 2, "deepseek_v3": 3,
-                "gpt_oss_120b": 4, "qwen3_30b_a3b_bf16": 5, "qwen3_30b_a3b_fp8": 6}
+                "gpt_oss_120b": 4, "qwen3_30b_a3b_bf16": 5, "qwen3_30b_a3b_fp8": 6,
+                "qwen3_30b_a3b_nvfp4_router": 7}
 
 
 def base_seed(spec: LayerSpec) -> int:
@@ -253,11 +261,14 @@ class HostLayer:
     sh_up: Optional[np.ndarray]
     sh_down: Optional[np.ndarray]  # uint16 [H, inter_s]
     sh_gate_w: Optional[np.ndarray]  # uint16 [H] or None
+    router_s: Optional[np.ndarray] = None   # NVFP4 router: uint8 E4M3 [E, H/16] (router: uint8 [E, H/2])
+    router_s2: Optional[np.ndarray] = None  # NVFP4 router: float32 [1]
 
     def tensors(self):
         return {k: getattr(self, k) for k in (
             "router", "bias", "gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s",
-            "gate_s2", "up_s2", "down_s2", "sh_gate", "sh_up", "sh_down", "sh_gate_w")}
+            "gate_s2", "up_s2", "down_s2", "sh_gate", "sh_up", "sh_down", "sh_gate_w",
+            "router_s", "router_s2")}
 
 
 def _quantize(spec: LayerSpec, w: np.ndarray):
@@ -300,8 +311,13 @@ def make_layer(spec: LayerSpec, seed: Optional[int] = None, pool: Optional[int] 
     pool = min(spec.E, spec.pool if pool is None else pool)
     rng = np.random.default_rng(seed)
     H, I, E = spec.H, spec.inter, spec.E
-    router = f32_to_bf16_bits(rng.standard_normal((E, H), dtype=np.float32)
-                              * np.float32(1.0 / np.sqrt(H)))
+    router_w = rng.standard_normal((E, H), dtype=np.float32) * np.float32(1.0 / np.sqrt(H))
+    router_s = router_s2 = None
+    if spec.router_fmt == NVFP4:
+        router, router_s = quantize_nvfp4(router_w)
+        router_s2 = np.ones(1, dtype=np.float32)
+    else:
+        router = f32_to_bf16_bits(router_w)
     bias = None
     if spec.scoring == SIGMOID_BIAS:
         bias = (rng.standard_normal(E, dtype=np.float32) * np.float32(0.1)).astype(np.float32)
@@ -320,7 +336,7 @@ def make_layer(spec: LayerSpec, seed: Optional[int] = None, pool: Optional[int] 
                                          * np.float32(1.0 / np.sqrt(H)))
     return HostLayer(spec, router, bias, gate_q, up_q, down_q, gate_s, up_s, down_s,
                      s2, None if s2 is None else s2.copy(), None if s2 is None else s2.copy(),
-                     sh_gate, sh_up, sh_down, sh_gate_w)
+                     sh_gate, sh_up, sh_down, sh_gate_w, router_s, router_s2)
 
 
 def x_row(spec: LayerSpec, seed: int, row: int, attempt: int = 0) -> np.ndarray:

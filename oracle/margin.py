@@ -20,7 +20,7 @@ MARGIN = 1e-3
 
 def selection_keys(layer, x: np.ndarray) -> np.ndarray:
     sp = layer.spec
-    logits = oracle.router_logits(x, layer.router)
+    logits = oracle.layer_router_logits(layer, x)
     if sp.scoring == synth.SOFTMAX:
         return logits
     _, _, sel = oracle.route(logits, sp.top_k, sp.scoring, sp.norm_topk_prob,

@@ -24,6 +24,10 @@
 //     moe_expert_silu_down_shared_fp8) — FP8 routed experts: E4M3 weights
 //     with block scales.  The pages do not give the scale granularity; the
 //     reading taken is one FP32 scale per 128 x 128 block of each projection;
+//   * forward_k3.rs / forward_batched.rs / forward_ep.rs, step 1 (gate_nvfp4
+//     into w4a16_gemv_batch3 / w4a16_gemm / w4a16_decode_gemv) — the router
+//     weight may be NVFP4 (E2M1 + per-16 E4M3 scale + FP32 scale2) against the
+//     BF16 activations;
 //   * forward_atomic_c4.rs, doc comment — routed outputs accumulated as
 //     routing-weighted sums, then cast to BF16 and blended with the shared
 //     expert;
@@ -168,6 +172,29 @@ void oracle_router_logits(const uint16_t* x, const uint16_t* wr, int N, int E, i
         }
 }
 
+// Router weight (e, h): fmt 0 = BF16 router [E, H] (16-bit little-endian
+// words at wr); fmt 1 = NVFP4 router, E2M1 codes [E, H/2] at wr, E4M3 scales
+// [E, H/16] at rs, times the router's scale2 (rs2).
+double oracle_router_weight(const uint8_t* wr, const uint8_t* rs, double rs2, int H, int fmt,
+                            long e, long h) {
+    if (fmt == 1) return oracle_fp4_weight(wr, rs, rs2, H, 0, e, h);
+    const long i = 2 * (e * (long)H + h);
+    return oracle_bf16((uint32_t)wr[i] | ((uint32_t)wr[i + 1] << 8));
+}
+
+// logits[n, e] = sum_h x[n, h] * Wr[e, h] for either router format.
+void oracle_router_logits_fmt(const uint16_t* x, const uint8_t* wr, const uint8_t* rs, double rs2,
+                              int fmt, int N, int E, int H, double* logits) {
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int n = 0; n < N; ++n)
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h)
+                acc += oracle_bf16(x[(long)n * H + h]) * oracle_router_weight(wr, rs, rs2, H, fmt, e, h);
+            logits[(long)n * E + e] = acc;
+        }
+}
+
 // ------------------------------------------------------------------ routing
 
 // Routing of one token, from its logits row.
@@ -303,6 +330,8 @@ struct oracle_weights {
     const float *gate_s2, *up_s2, *down_s2;
     const uint16_t *sh_gate, *sh_up, *sh_down;
     const uint16_t* sh_gate_w;
+    const uint8_t* router_s;     // NVFP4 router: E4M3 scales [E, H/16]
+    const float* router_s2;      // NVFP4 router: scale2 (one float) or null = 1.0
 };
 
 // out_f64 [N, H] = sum_j w[n,j] * expert_{idx[n,j]}(x_n) + g_s(x_n) * shared(x_n)
@@ -310,15 +339,21 @@ struct oracle_weights {
 // shared term when Is == 0.  The routed scaling factor is not applied to the
 // shared expert.  out_bf16 is out_f64 rounded to BF16 (nearest even).
 // idx/w receive the routing ([N, k]); logits (optional) the router output.
+// router_fmt: 0 = BF16 router, 1 = NVFP4 router (router holds the codes).
 int oracle_moe_forward(int H, int inter, int E, int k, int scoring, int norm, double rsf,
                        int fmt, int Is, const oracle_weights* W, const uint16_t* x, int N,
                        double* out_f64, uint16_t* out_bf16, int32_t* idx, double* w,
-                       double* logits_out) {
+                       double* logits_out, int router_fmt) {
     if (H <= 0 || inter <= 0 || E <= 0 || k <= 0 || k > E || N < 0) return 1;
-    if (fmt < 0 || fmt > 3) return 1;
+    if (fmt < 0 || fmt > 3 || router_fmt < 0 || router_fmt > 1) return 1;
     const int gs = (fmt == 0) ? 16 : 32;
     std::vector<double> logits((size_t)N * E);
-    oracle_router_logits(x, W->router, N, E, H, logits.data());
+    if (router_fmt == 0)
+        oracle_router_logits(x, W->router, N, E, H, logits.data());
+    else
+        oracle_router_logits_fmt(x, reinterpret_cast<const uint8_t*>(W->router), W->router_s,
+                                 W->router_s2 ? (double)W->router_s2[0] : 1.0, 1, N, E, H,
+                                 logits.data());
     if (logits_out) std::copy(logits.begin(), logits.end(), logits_out);
     oracle_route(logits.data(), W->bias, N, E, k, scoring, norm, rsf, idx, w, nullptr);
 

@@ -38,7 +38,8 @@ def build(force: bool = False) -> str:
 class _Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "router", "bias", "gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s",
-        "gate_s2", "up_s2", "down_s2", "sh_gate", "sh_up", "sh_down", "sh_gate_w")]
+        "gate_s2", "up_s2", "down_s2", "sh_gate", "sh_up", "sh_down", "sh_gate_w",
+        "router_s", "router_s2")]
 
 
 def lib():
@@ -63,6 +64,8 @@ def lib():
             L.oracle_dequant.argtypes = [vp, vp, d, i32, i32, i32, vp]
             L.oracle_router_logits.restype = None
             L.oracle_router_logits.argtypes = [vp, vp, i32, i32, i32, vp]
+            L.oracle_router_logits_fmt.restype = None
+            L.oracle_router_logits_fmt.argtypes = [vp, vp, vp, d, i32, i32, i32, i32, vp]
             L.oracle_route.restype = None
             L.oracle_route.argtypes = [vp, vp, i32, i32, i32, i32, i32, d, vp, vp, vp]
             L.oracle_weight.restype = d
@@ -74,7 +77,7 @@ def lib():
             L.oracle_moe_forward.restype = i32
             L.oracle_moe_forward.argtypes = [i32, i32, i32, i32, i32, i32, d, i32, i32,
                                              ctypes.POINTER(_Weights), vp, i32,
-                                             vp, vp, vp, vp, vp]
+                                             vp, vp, vp, vp, vp, i32]
             L.oracle_num_threads.restype = i32
             L.oracle_num_threads.argtypes = []
             _lib = L
@@ -127,14 +130,28 @@ def dequant(q: np.ndarray, s: np.ndarray, scale2: float, wfmt: str) -> np.ndarra
 
 # ------------------------------------------------------------------- steps
 
-def router_logits(x: np.ndarray, router: np.ndarray) -> np.ndarray:
+def router_logits(x: np.ndarray, router: np.ndarray, router_s: Optional[np.ndarray] = None,
+                  router_s2: Optional[np.ndarray] = None) -> np.ndarray:
+    """Logits of a BF16 router [E, H] (uint16 bits), or of an NVFP4 router
+    (router = codes [E, H/2], router_s = E4M3 scales [E, H/16], router_s2 =
+    one float or None)."""
     x = np.ascontiguousarray(x, dtype=np.uint16)
-    router = np.ascontiguousarray(router, dtype=np.uint16)
     N, H = x.shape
     E = router.shape[0]
     out = np.empty((N, E), dtype=np.float64)
-    lib().oracle_router_logits(_p(x), _p(router), N, E, H, _p(out))
+    if router_s is None:
+        router = np.ascontiguousarray(router, dtype=np.uint16)
+        lib().oracle_router_logits(_p(x), _p(router), N, E, H, _p(out))
+    else:
+        router = np.ascontiguousarray(router, dtype=np.uint8)
+        rs = np.ascontiguousarray(router_s, dtype=np.uint8)
+        s2 = 1.0 if router_s2 is None else float(np.asarray(router_s2).ravel()[0])
+        lib().oracle_router_logits_fmt(_p(x), _p(router), _p(rs), s2, 1, N, E, H, _p(out))
     return out
+
+
+def layer_router_logits(layer, x: np.ndarray) -> np.ndarray:
+    return router_logits(x, layer.router, layer.router_s, layer.router_s2)
 
 
 def route(logits: np.ndarray, k: int, scoring: str, norm: bool, rsf: float = 1.0,
@@ -206,7 +223,7 @@ def moe_forward(layer, x: np.ndarray):
         sp.H, sp.inter, sp.E, sp.top_k, 0 if sp.scoring == "softmax" else 1,
         int(sp.norm_topk_prob), float(sp.routed_scaling_factor), fmt_code(sp.wfmt),
         sp.shared_inter, ctypes.byref(W), _p(x), N, _p(out), _p(outb), _p(idx), _p(w),
-        _p(logits))
+        _p(logits), 1 if sp.router_fmt == "nvfp4" else 0)
     if rc != 0:
         raise ValueError(f"oracle_moe_forward rejected its arguments (code {rc})")
     return {"out_f64": out, "out_bf16": outb, "idx": idx, "w": w, "logits": logits}

@@ -477,6 +477,30 @@ def test_fp8_single_expert_equals_dense_swiglu(oracle_mod):
                                    rtol=1e-12, atol=1e-15)
 
 
+def test_nvfp4_router_equals_bf16_router_with_the_same_values(oracle_mod):
+    """An NVFP4 router (the pages' gate_nvfp4 into the w4a16 GEMV) whose values
+    are BF16 numbers (E2M1 x E4M3 x 2) gives the BF16-router layer's routing
+    and output to the last bit; its logits match a numpy matmul on the
+    test-side decode."""
+    import dataclasses
+    sp = _small_spec(E=12, top_k=3, H=128, inter=64, router_fmt=synth.NVFP4)
+    L = synth.make_layer(sp, seed=41)
+    assert L.router.dtype == np.uint8 and L.router.shape == (12, 64) and L.router_s.shape == (12, 8)
+    L.router_s2[:] = 2.0
+    wr = _decode_fp4_independent(L.router, L.router_s, synth.NVFP4) * 2.0
+    bits = synth.f32_to_bf16_bits(wr.astype(np.float32))
+    assert np.array_equal(_bf16_arr(bits), wr)
+    Lb = dataclasses.replace(L, spec=dataclasses.replace(sp, router_fmt=synth.BF16), router=bits,
+                             router_s=None, router_s2=None)
+    x = synth.make_tokens(sp, 5, seed=42)
+    np.testing.assert_allclose(oracle_mod.layer_router_logits(L, x), _bf16_arr(x) @ wr.T,
+                               rtol=1e-13, atol=1e-13)
+    r, rb = oracle_mod.moe_forward(L, x), oracle_mod.moe_forward(Lb, x)
+    np.testing.assert_array_equal(r["logits"], rb["logits"])
+    np.testing.assert_array_equal(r["idx"], rb["idx"])
+    np.testing.assert_array_equal(r["out_f64"], rb["out_f64"])
+
+
 def test_scale2_scales_each_projection(oracle_mod):
     sp = _small_spec(E=1, top_k=1)
     L = synth.make_layer(sp, seed=13)

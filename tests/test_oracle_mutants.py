@@ -40,6 +40,9 @@ MUTANTS = {
     "bf16_adjacent_swap": ("const long i = 2 * (r * (long)K + k);",
                            "const long i = 2 * ((r * (long)K + k) ^ 1);"),
     "bf16_expert_stride": ("const long gq_e = bf ? 2L * inter * H", "const long gq_e = bf ? 1L * inter * H"),
+    "router_nvfp4_as_mxfp4": ("return oracle_fp4_weight(wr, rs, rs2, H, 0, e, h);",
+                              "return oracle_fp4_weight(wr, rs, rs2, H, 1, e, h);"),
+    "router_scale2_ignored": ("W->router_s2 ? (double)W->router_s2[0] : 1.0", "1.0"),
     "fp8_row_block_ignored": ("s + 4 * ((r / 128) * kb + k / 128)", "s + 4 * (k / 128)"),
     "fp8_scale_ignored": ("return oracle_e4m3(q[r * (long)K + k]) * (double)sc;",
                           "return oracle_e4m3(q[r * (long)K + k]) * (sc > 0 ? 1.0 : 0.0);"),
