@@ -15,8 +15,9 @@ barrier and torch.cuda.synchronize(), CUDA events on the launch stream; the
 maximum over ranks is taken.  The line also carries "grouped": the many-token
 path (gpt-oss-shaped MXFP4 layer at N = 512, tcgen05 GEMMs),
 "bf16_experts" and "fp8_experts": the same Qwen3 shape with BF16 or FP8
-(128 x 128 block-scaled) routed experts at N = 1-4, all timed on the same GPU
-after the main measurement.  --impl reference
+(128 x 128 block-scaled) routed experts at N = 1-4, and "nvfp4_router": the
+Qwen3 shape with an NVFP4-quantised router, all timed on the same GPU after
+the main measurement.  --impl reference
 times the FP64 CPU oracle on a bounded sample of the same workload instead.
 """
 from __future__ import annotations
@@ -436,6 +437,9 @@ def run_gpu(args):
         result["bf16_experts"] = measure_decode_config(stream, "qwen3_30b_a3b_bf16", (1, 2, 3, 4))
     if rank == 0 and not args.no_fp8:
         result["fp8_experts"] = measure_decode_config(stream, "qwen3_30b_a3b_fp8", (1, 2, 3, 4))
+    if rank == 0 and not args.no_nvfp4_router:
+        result["nvfp4_router"] = measure_decode_config(stream, "qwen3_30b_a3b_nvfp4_router",
+                                                       (1, 2, 3, 4))
     if rank == 0:
         result["clocks"] = clk.summary()
         if not args.no_cpu_baseline:
@@ -527,6 +531,8 @@ def main():
                     help="skip the BF16 routed-expert decode measurement")
     ap.add_argument("--no-fp8", action="store_true",
                     help="skip the FP8 routed-expert decode measurement")
+    ap.add_argument("--no-nvfp4-router", action="store_true",
+                    help="skip the NVFP4-router decode measurement")
     ap.add_argument("--no-grouped", action="store_true",
                     help="skip the grouped-path (gpt-oss N=512) measurement")
     args = ap.parse_args()

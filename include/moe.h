@@ -3,6 +3,8 @@
  *
  * One call computes, for N token rows x[N,H] (BF16):
  *   1. router logits   l[n,e] = x[n,:] . Wr[e,:]                 (FP32 accumulate)
+ *                      with a BF16 router, or an NVFP4 router
+ *                      (Wr = E2M1(code) * E4M3 scale per 16 * scale2);
  *   2. top-k routing   softmax (optionally renormalised over the selected k)
  *                      or sigmoid + correction bias for selection, sigmoid
  *                      for the weights, optional renormalisation, times the
@@ -58,6 +60,10 @@
  * BF16 routed experts (wfmt MOE_W_BF16): gate_q, up_q [E, inter, H] bf16 and
  *   down_q [E, H, inter] bf16; the scale pointers and *_s2 are not read (NULL
  *   allowed).
+ * NVFP4 router (router_fmt MOE_R_NVFP4, the pages' gate_nvfp4 into the w4a16
+ *   GEMV of forward_k3.rs step 1): router points to E2M1 codes [E, H/2] u8,
+ *   router_s to E4M3 scales [E, H/16] u8, router_s2 to one f32 scale2 (NULL =
+ *   1.0).
  * FP8 routed experts (wfmt MOE_W_FP8): gate_q, up_q [E, inter, H] and down_q
  *   [E, H, inter] E4M3 bytes (OCP "fn"); gate_s, up_s point to f32
  *   [E, ceil(inter/128), ceil(H/128)] and down_s to f32 [E, ceil(H/128),
@@ -98,6 +104,8 @@ typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID_BIAS = 1 } moe_scoring_t
  * scale2), MXFP4 (E2M1 + per-32 E8M0 scale), BF16 (plain weights), FP8 (E4M3
  * + FP32 scale per 128 x 128 block). */
 typedef enum { MOE_W_NVFP4 = 0, MOE_W_MXFP4 = 1, MOE_W_BF16 = 2, MOE_W_FP8 = 3 } moe_wfmt_t;
+/* Router weight formats. */
+typedef enum { MOE_R_BF16 = 0, MOE_R_NVFP4 = 1 } moe_rfmt_t;
 
 /* Layer configuration: the config fields the pages' MoE forward reads
  * (hidden_size, moe_intermediate_size, num_experts, num_experts_per_tok,
@@ -113,10 +121,11 @@ typedef struct {
   float routed_scaling_factor;   /* sigmoid scoring only; ignored for softmax */
   int32_t wfmt;                  /* moe_wfmt_t */
   int32_t shared_inter;          /* shared expert intermediate size; 0 = none */
+  int32_t router_fmt;            /* moe_rfmt_t (0 = BF16 router) */
 } moe_layer_desc_t;
 
 typedef struct {
-  const void* router;            /* bf16 [E, H] */
+  const void* router;            /* bf16 [E, H], or E2M1 codes [E, H/2] (NVFP4 router) */
   const float* bias;             /* f32 [E] (required iff scoring is sigmoid+bias) */
   const uint8_t* gate_q;
   const uint8_t* up_q;
@@ -131,6 +140,8 @@ typedef struct {
   const void* sh_up;
   const void* sh_down;
   const void* sh_gate_w;         /* bf16 [H] or NULL (ungated) */
+  const uint8_t* router_s;       /* NVFP4 router: E4M3 scales [E, H/16]; else NULL */
+  const float* router_s2;        /* NVFP4 router: one f32 scale2, NULL = 1.0 */
 } moe_weights_t;
 
 /* Bytes of device workspace moe_forward needs for any 1 <= N <= max_tokens.

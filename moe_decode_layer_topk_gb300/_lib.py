@@ -13,7 +13,7 @@ from typing import Optional
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = 1
@@ -27,6 +27,8 @@ MOE_W_NVFP4 = 0
 MOE_W_MXFP4 = 1
 MOE_W_BF16 = 2
 MOE_W_FP8 = 3
+MOE_R_BF16 = 0
+MOE_R_NVFP4 = 1
 
 EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_forward", "moe_route",
             "moe_host_staging_size", "moe_forward_host", "moe_get_error", "moe_status_string",
@@ -43,13 +45,15 @@ class LayerDesc(ctypes.Structure):
     _fields_ = [("H", ctypes.c_int32), ("inter", ctypes.c_int32), ("E", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("scoring", ctypes.c_int32),
                 ("norm_topk_prob", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
-                ("wfmt", ctypes.c_int32), ("shared_inter", ctypes.c_int32)]
+                ("wfmt", ctypes.c_int32), ("shared_inter", ctypes.c_int32),
+                ("router_fmt", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "router", "bias", "gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s",
-        "gate_s2", "up_s2", "down_s2", "sh_gate", "sh_up", "sh_down", "sh_gate_w")]
+        "gate_s2", "up_s2", "down_s2", "sh_gate", "sh_up", "sh_down", "sh_gate_w",
+        "router_s", "router_s2")]
 
 
 _lock = threading.Lock()

@@ -184,16 +184,16 @@ __device__ bool grid_wait(Ctrl* c, unsigned long long target, uint64_t budget_ns
 // logits[n, e] = sum_h x[n, h] * Wr[e, h], FP32 accumulation of BF16 products.
 __device__ __noinline__ void router_phase(const Params& p, int cta, int G, Tables& tb, int ctid) {
   const int H = p.H;
+  const float rs2 = (p.router_fmt == 1 && p.router_s2) ? __ldg(p.router_s2) : 1.0f;
   for (int e = cta; e < p.E; e += G) {
-    const uint16_t* wr = p.router + (size_t)e * H;
     for (int n0 = 0; n0 < p.N; n0 += 8) {
       const int nn = min(8, p.N - n0);
       float acc[8];
 #pragma unroll
       for (int t = 0; t < 8; ++t) acc[t] = 0.f;
       for (int kk = ctid * 8; kk < H; kk += kConsumerThreads * 8) {
-        const uint4 w = ld_nc_u4(wr + kk);
-        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+        float wf[8];
+        router_w8(p.router, p.router_fmt, p.router_s, rs2, H, e, kk, wf);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
           if (t < nn) {
@@ -201,8 +201,8 @@ __device__ __noinline__ void router_phase(const Params& p, int cta, int G, Table
             const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              acc[t] = fmaf(bf16_lo(wv[i]), bf16_lo(xa[i]), acc[t]);
-              acc[t] = fmaf(bf16_hi(wv[i]), bf16_hi(xa[i]), acc[t]);
+              acc[t] = fmaf(wf[2 * i], bf16_lo(xa[i]), acc[t]);
+              acc[t] = fmaf(wf[2 * i + 1], bf16_hi(xa[i]), acc[t]);
             }
           }
         }

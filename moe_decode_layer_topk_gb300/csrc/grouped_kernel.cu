@@ -91,12 +91,33 @@ __global__ void __launch_bounds__(256) grouped_router_kernel(const GroupedParams
   for (int i = tid * 8; i < nt * H; i += 256 * 8)
     *reinterpret_cast<uint4*>(xs + i) = ld_nc_u4(p.x + (size_t)n0 * H + i);
   __syncthreads();
+  const float rs2 = (p.router_fmt == 1 && p.router_s2) ? __ldg(p.router_s2) : 1.0f;
   for (int e = blockIdx.y * kRtExp + warp; e < min(E, (int)(blockIdx.y + 1) * kRtExp); e += 8) {
     float acc[kRtTok];
 #pragma unroll
     for (int t = 0; t < kRtTok; ++t) acc[t] = 0.f;
+    if (p.router_fmt == 1) {   // NVFP4 router: eight decoded weights per lane and step
+      for (int h = lane * 8; h < H; h += 32 * 8) {
+        float wf[8];
+        router_w8(p.router, 1, p.router_s, rs2, H, e, h, wf);
+#pragma unroll
+        for (int t = 0; t < kRtTok; ++t) {
+          if (t < nt) {
+            const uint4 xv = *reinterpret_cast<const uint4*>(xs + t * H + h);
+            const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w};
+            float a2 = acc[t];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              a2 = fmaf(wf[2 * q], __uint_as_float(xa[q] << 16), a2);
+              a2 = fmaf(wf[2 * q + 1], __uint_as_float(xa[q] & 0xFFFF0000u), a2);
+            }
+            acc[t] = a2;
+          }
+        }
+      }
+    }
     const uint16_t* wr = p.router + (size_t)e * H;
-    for (int hb = 0; hb < H; hb += 8 * 256) {
+    for (int hb = 0; p.router_fmt == 0 && hb < H; hb += 8 * 256) {
       uint4 wv[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {

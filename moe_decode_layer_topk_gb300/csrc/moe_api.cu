@@ -19,7 +19,7 @@
 
 namespace {
 
-constexpr int32_t kAbiVersion = 1;
+constexpr int32_t kAbiVersion = 2;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -110,6 +110,7 @@ moe_status_t check_desc(const moe_layer_desc_t* d) {
       d->wfmt != MOE_W_FP8)
     return MOE_ERR_INVALID_ARG;
   if (d->shared_inter < 0) return MOE_ERR_INVALID_ARG;
+  if (d->router_fmt != MOE_R_BF16 && d->router_fmt != MOE_R_NVFP4) return MOE_ERR_INVALID_ARG;
   if (d->H % 32 || d->inter % 32 || d->shared_inter % 32) return MOE_ERR_UNSUPPORTED;
   if (d->E > moe::kMaxE || d->top_k > d->E || d->top_k > moe::kMaxTopK) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -126,6 +127,8 @@ moe_status_t check_weights(const moe_layer_desc_t* d, const moe_weights_t* w) {
       if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
   }
   if (d->scoring == MOE_SCORE_SIGMOID_BIAS && !w->bias) return MOE_ERR_INVALID_ARG;
+  if (d->router_fmt == MOE_R_NVFP4 && (!w->router_s || !aligned16(w->router_s)))
+    return MOE_ERR_INVALID_ARG;
   if (d->shared_inter > 0) {
     const void* sh[] = {w->sh_gate, w->sh_up, w->sh_down};
     for (const void* p : sh)
@@ -319,6 +322,9 @@ moe_status_t run_grouped(const moe_layer_desc_t* d, const moe_weights_t* w, cons
   gp.route_only = route_only;
   gp.x = static_cast<const uint16_t*>(x);
   gp.router = static_cast<const uint16_t*>(w->router);
+  gp.router_fmt = d->router_fmt;
+  gp.router_s = d->router_fmt == MOE_R_NVFP4 ? w->router_s : nullptr;
+  gp.router_s2 = d->router_fmt == MOE_R_NVFP4 ? w->router_s2 : nullptr;
   gp.bias = d->scoring == MOE_SCORE_SIGMOID_BIAS ? w->bias : nullptr;
   gp.topk_idx = topk_idx;
   gp.topk_w = topk_w;
@@ -425,6 +431,9 @@ moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* 
   p.N = N;
   p.route_only = route_only;
   p.router = static_cast<const uint16_t*>(w->router);
+  p.router_fmt = d->router_fmt;
+  p.router_s = d->router_fmt == MOE_R_NVFP4 ? w->router_s : nullptr;
+  p.router_s2 = d->router_fmt == MOE_R_NVFP4 ? w->router_s2 : nullptr;
   p.bias = d->scoring == MOE_SCORE_SIGMOID_BIAS ? w->bias : nullptr;
   // BF16 experts read no scales; FP8 experts their f32 block scales; only
   // the FP4 formats have scale2

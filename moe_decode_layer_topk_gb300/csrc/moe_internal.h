@@ -91,7 +91,10 @@ struct Params {
   int N;
   int route_only;
   // weights (device)
-  const uint16_t* router;
+  const uint16_t* router;            // bf16 [E, H], or E2M1 codes [E, H/2] (router_fmt 1)
+  int router_fmt;                    // 0 = BF16 router, 1 = NVFP4 router
+  const uint8_t* router_s;           // NVFP4 router: E4M3 scales [E, H/16]
+  const float* router_s2;            // NVFP4 router: scale2 (one float) or null
   const float* bias;
   const uint8_t *gsc, *usc, *dsc;   // FP4 scales (1D block copies); FP8: f32 block scales
   const float *g2, *u2, *d2;
@@ -131,7 +134,10 @@ struct GroupedParams {
   int fmt;
   int route_only;
   const uint16_t* x;        // [N, H] bf16
-  const uint16_t* router;   // [E, H] bf16
+  const uint16_t* router;   // [E, H] bf16, or E2M1 codes [E, H/2] (router_fmt 1)
+  int router_fmt;           // 0 = BF16 router, 1 = NVFP4 router
+  const uint8_t* router_s;  // NVFP4 router: E4M3 scales [E, H/16]
+  const float* router_s2;   // NVFP4 router: scale2 (one float) or null
   const float* bias;        // [E] or null
   int32_t* topk_idx;        // [N, k] or null
   float* topk_w;

@@ -9,7 +9,39 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "ptx.cuh"
+
 namespace moe {
+
+// Eight router weights of row e, elements h .. h+7 (h a multiple of 8), as
+// FP32: a BF16 router [E, H], or an NVFP4 router (E2M1 codes [E, H/2], element
+// 2j in the low nibble; one E4M3 scale per 16 elements [E, H/16]; times the
+// router's scale2).  E2M1 x E4M3 is exact in FP32.
+__device__ __forceinline__ void router_w8(const uint16_t* router, int fmt, const uint8_t* rs,
+                                          float s2, int H, int e, int h, float (&w)[8]) {
+  if (fmt == 0) {
+    const uint4 v = ld_nc_u4(router + (size_t)e * H + h);
+    const uint32_t a[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w[2 * i] = __uint_as_float(a[i] << 16);
+      w[2 * i + 1] = __uint_as_float(a[i] & 0xFFFF0000u);
+    }
+  } else {
+    const uint8_t* q = reinterpret_cast<const uint8_t*>(router) + (size_t)e * (H / 2) + h / 2;
+    const uint32_t codes = __ldg(reinterpret_cast<const uint32_t*>(q));
+    const uint32_t sb = __ldg(rs + (size_t)e * (H / 16) + h / 16);
+    const float sc = f16x2_to_f32x2(e4m3x2_to_f16x2(sb)).x * s2;
+    uint32_t o[4];
+    e2m1x8_to_f16x2x4(codes, o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = f16x2_to_f32x2(o[i]);
+      w[2 * i] = f.x * sc;
+      w[2 * i + 1] = f.y * sc;
+    }
+  }
+}
 
 // Selection key, order preserving as unsigned: larger key = larger score.
 __device__ __forceinline__ uint32_t order_key(float f) {

@@ -23,6 +23,7 @@ def layer_desc(spec: LayerSpec) -> _lib.LayerDesc:
     d.wfmt = {NVFP4: _lib.MOE_W_NVFP4, MXFP4: _lib.MOE_W_MXFP4, BF16: _lib.MOE_W_BF16,
               FP8: _lib.MOE_W_FP8}[spec.wfmt]
     d.shared_inter = spec.shared_inter
+    d.router_fmt = _lib.MOE_R_NVFP4 if spec.router_fmt == NVFP4 else _lib.MOE_R_BF16
     return d
 
 

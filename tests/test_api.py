@@ -67,6 +67,12 @@ def test_bad_descriptor_is_refused(lib, bad):
     assert _lib.moe_workspace_size(_desc(**bad), 1) == 0
 
 
+def test_bad_router_format_is_refused(lib):
+    d = _desc()
+    d.router_fmt = 2
+    assert _lib.moe_workspace_size(d, 1) == 0
+
+
 def _fake_weights(shared=False):
     w = _lib.Weights()
     base = 1 << 20
@@ -116,6 +122,12 @@ def test_argument_refusals_happen_before_any_cuda_call(lib):
     assert _forward(lib, d8, w8, N=300) == _lib.MOE_ERR_UNSUPPORTED
     w8.down_s = None
     assert _forward(lib, d8, w8) == _lib.MOE_ERR_INVALID_ARG
+    # NVFP4 router: its scales are required
+    dr = _desc()
+    dr.router_fmt = _lib.MOE_R_NVFP4
+    wr = _fake_weights()
+    wr.router_s = None
+    assert _forward(lib, dr, wr) == _lib.MOE_ERR_INVALID_ARG
     ds = _desc(scoring=1)                                                 # sigmoid needs a bias
     assert _forward(lib, ds, _fake_weights()) == _lib.MOE_ERR_INVALID_ARG
     dsh = _desc(shared_inter=64)                                          # shared size, no weights

@@ -35,13 +35,15 @@ GROUPED = {
     "single_expert_all_tokens": (dict(H=256, inter=128, E=1, top_k=1), 300),
     "mxfp4_many_chunks": (dict(H=1024, inter=384, E=8, top_k=2, wfmt=MX), 160),
     "nvfp4_many_experts": (dict(H=512, inter=256, E=64, top_k=4), 96),
+    # NVFP4-quantised router on the grouped router kernel
+    "nvfp4_router": (dict(H=256, inter=128, E=16, top_k=4, router_fmt=NV), 100),
 }
 
 
 def _check(host, dev, x, sample=None):
     out, idx, w = run_forward(dev, x)
     sp = host.spec
-    logits = oracle.router_logits(x, host.router)
+    logits = oracle.layer_router_logits(host, x)
     ref_idx, ref_w, _ = oracle.route(logits, sp.top_k, sp.scoring, sp.norm_topk_prob,
                                      sp.routed_scaling_factor, host.bias)
     keys = margin.selection_keys(host, x)

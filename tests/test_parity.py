@@ -59,6 +59,13 @@ SMALL = {
     "fp8_experts_down_3_chunks": (dict(H=256, inter=1152, E=8, top_k=2, wfmt=F8), 2),
     "fp8_experts_sigmoid": (dict(H=512, inter=256, E=32, top_k=4, scoring=SB,
                                  routed_scaling_factor=2.5, wfmt=F8), 4),
+    # NVFP4-quantised router (softmax and sigmoid routing, with other expert formats)
+    "nvfp4_router": (dict(H=256, inter=128, E=16, top_k=4, router_fmt=NV), 5),
+    "nvfp4_router_sigmoid_shared": (dict(H=320, inter=96, E=32, top_k=3, scoring=SB,
+                                         routed_scaling_factor=2.5, shared_inter=64,
+                                         router_fmt=NV), 4),
+    "nvfp4_router_fp8_experts": (dict(H=512, inter=256, E=24, top_k=4, wfmt=F8,
+                                      router_fmt=NV), 3),
 }
 
 
@@ -118,7 +125,7 @@ def test_scale2_is_applied():
 
 
 FULL = [(name, N) for name in ("tiny", "qwen3_30b_a3b", "mtp_verify", "deepseek_v3", "gpt_oss_120b",
-                               "qwen3_30b_a3b_bf16", "qwen3_30b_a3b_fp8")
+                               "qwen3_30b_a3b_bf16", "qwen3_30b_a3b_fp8", "qwen3_30b_a3b_nvfp4_router")
         for N in synth.CONFIGS[name].tokens if N <= 64]
 
 
