@@ -55,6 +55,24 @@ def _dist():
     return rank, world, local
 
 
+def max_over_ranks(x: float, world: int, device="cuda") -> float:
+    """The largest x over all ranks of the initialised process group (the
+    timed region's length is the slowest replica's); x itself when world == 1."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbps(bytes_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: every replica moves bytes_per_rank in the timed
+    region, whose length is the maximum over ranks (ms)."""
+    return bytes_per_rank * world / (ms / 1e3) / 1e9
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
 
@@ -327,15 +345,11 @@ def run_gpu(args):
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
     for c in calls:
         assert _lib.moe_get_error(c[4]) == _lib.MOE_OK, "device-side wait expired during timing"
     steps = cycles * steps_per_cycle
-    value = cycles * per_cycle_bytes * world / (ms / 1e3) / 1e9
+    value = job_gbps(cycles * per_cycle_bytes, world, ms)
     launches = cycles * launches_per_cycle
     avg_launch_us = ms * 1e3 / launches
     achieved = per_cycle_bytes / launches_per_cycle / (avg_launch_us * 1e-6) / 1e9

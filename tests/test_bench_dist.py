@@ -1,0 +1,66 @@
+"""Multi-replica bookkeeping of bench.py on CPU: world size 2 over gloo.
+
+bench.py --gpus N runs N independent replicas (the layer forward does not
+shard); the timed region's length is the maximum over ranks and the value is
+the bytes of all replicas over that time.  The reference arm runs on rank 0
+only.  These checks need no GPU."""
+import os
+import socket
+import subprocess
+import sys
+
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, times, q):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms = bench.max_over_ranks(times[rank], world, device="cpu")
+        q.put((rank, ms, bench.job_gbps(1e9, world, ms)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_value_world_2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    times = [3.0, 5.0]
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, times, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, ms, gbps in got:
+        assert ms == 5.0                          # every rank sees the slowest replica
+        assert abs(gbps - 2 * 1e9 / 5e-3 / 1e9) < 1e-9
+
+
+def test_single_rank_is_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(7.5, 1) == 7.5
+    assert bench.job_gbps(2e9, 1, 1.0) == 2000.0
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--steps", "3", "--warmup", "3"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
