@@ -36,6 +36,7 @@ FP8 = "fp8"
 FP8_BLOCK = 128   # FP8 experts: one FP32 scale per 128 x 128 block
 SOFTMAX = "softmax"
 SIGMOID_BIAS = "sigmoid_bias"
+SOFTMAX_BIAS = "softmax_bias"   # softmax scores + correction bias for selection
 
 
 @dataclasses.dataclass(frozen=True)
@@ -45,7 +46,7 @@ class LayerSpec:
     inter: int
     E: int
     top_k: int
-    scoring: str            # SOFTMAX | SIGMOID_BIAS
+    scoring: str            # SOFTMAX | SIGMOID_BIAS | SOFTMAX_BIAS
     norm_topk_prob: bool
     routed_scaling_factor: float
     wfmt: str               # NVFP4 | MXFP4 | BF16 | FP8
@@ -55,6 +56,7 @@ class LayerSpec:
     tokens: tuple           # token counts the layer is run at
     pool: int               # distinct experts drawn per projection
     router_fmt: str = BF16  # BF16 router, or NVFP4 (E2M1 + per-16 E4M3 + scale2)
+    zero_experts: int = 0   # Z extra router outputs whose expert adds nothing
 
     @property
     def gs(self) -> int:
@@ -73,9 +75,10 @@ class LayerSpec:
         return 3 * self.inter * self.H // 2 + 3 * self.inter * self.H // self.gs
 
     def router_bytes(self) -> int:
+        R = self.E + self.zero_experts
         if self.router_fmt == NVFP4:
-            return self.E * self.H // 2 + self.E * self.H // 16
-        return self.E * self.H * 2
+            return R * self.H // 2 + R * self.H // 16
+        return R * self.H * 2
 
     def shared_bytes(self) -> int:
         return 3 * self.shared_inter * self.H * 2
@@ -100,6 +103,11 @@ CONFIGS = {
     # FP8 block-scaled routed experts on the Qwen3 shape.
     "qwen3_30b_a3b_fp8": LayerSpec("qwen3_30b_a3b_fp8", 2048, 768, 128, 8, SOFTMAX, True,
                                    1.0, FP8, 0, False, True, (1, 2, 3, 4), 16),
+    # Zero-expert routing (router of width E + Z, softmax + correction bias)
+    # on the Qwen3 shape: 128 experts and 64 zero experts.
+    "qwen3_30b_a3b_zero_experts": LayerSpec("qwen3_30b_a3b_zero_experts", 2048, 768, 128, 8,
+                                            SOFTMAX_BIAS, True, 1.0, NVFP4, 0, False, True,
+                                            (1, 2, 3, 4), 16, BF16, 64),
     # NVFP4-quantised router on the Qwen3 shape.
     "qwen3_30b_a3b_nvfp4_router": LayerSpec("qwen3_30b_a3b_nvfp4_router", 2048, 768, 128, 8,
                                             SOFTMAX, True, 1.0, NVFP4, 0, False, True,
@@ -107,7 +115,7 @@ CONFIGS = {
 }
 CONFIG_INDEX = {"tiny": 0, "qwen3_30b_a3b": 1, "mtp_verify": 2, "deepseek_v3": 3,
                 "gpt_oss_120b": 4, "qwen3_30b_a3b_bf16": 5, "qwen3_30b_a3b_fp8": 6,
-                "qwen3_30b_a3b_nvfp4_router": 7}
+                "qwen3_30b_a3b_nvfp4_router": 7, "qwen3_30b_a3b_zero_experts": 8}
 
 
 def base_seed(spec: LayerSpec) -> int:
@@ -311,7 +319,8 @@ def make_layer(spec: LayerSpec, seed: Optional[int] = None, pool: Optional[int] 
     pool = min(spec.E, spec.pool if pool is None else pool)
     rng = np.random.default_rng(seed)
     H, I, E = spec.H, spec.inter, spec.E
-    router_w = rng.standard_normal((E, H), dtype=np.float32) * np.float32(1.0 / np.sqrt(H))
+    R = E + spec.zero_experts    # router width
+    router_w = rng.standard_normal((R, H), dtype=np.float32) * np.float32(1.0 / np.sqrt(H))
     router_s = router_s2 = None
     if spec.router_fmt == NVFP4:
         router, router_s = quantize_nvfp4(router_w)
@@ -320,7 +329,10 @@ def make_layer(spec: LayerSpec, seed: Optional[int] = None, pool: Optional[int] 
         router = f32_to_bf16_bits(router_w)
     bias = None
     if spec.scoring == SIGMOID_BIAS:
-        bias = (rng.standard_normal(E, dtype=np.float32) * np.float32(0.1)).astype(np.float32)
+        bias = (rng.standard_normal(R, dtype=np.float32) * np.float32(0.1)).astype(np.float32)
+    elif spec.scoring == SOFTMAX_BIAS:
+        # on the scale of the softmax scores (about 1/R each)
+        bias = (rng.standard_normal(R, dtype=np.float32) * np.float32(0.5 / R)).astype(np.float32)
     gate_q, gate_s = _expert_projection(spec, rng, I, H, pool, E)
     up_q, up_s = _expert_projection(spec, rng, I, H, pool, E)
     down_q, down_s = _expert_projection(spec, rng, H, I, pool, E)

@@ -16,6 +16,9 @@ from moe_decode_layer_topk_gb300 import synth
 from . import oracle
 
 MARGIN = 1e-3
+# softmax + bias keys are probabilities of about 1/(E + Z): the gap is taken
+# relative to the largest key (still far above the GPU's FP32 error)
+MARGIN_REL_SOFTMAX_BIAS = 1e-3
 
 
 def selection_keys(layer, x: np.ndarray) -> np.ndarray:
@@ -26,6 +29,12 @@ def selection_keys(layer, x: np.ndarray) -> np.ndarray:
     _, _, sel = oracle.route(logits, sp.top_k, sp.scoring, sp.norm_topk_prob,
                              sp.routed_scaling_factor, layer.bias)
     return sel
+
+
+def margin_for(layer, keys_row: np.ndarray) -> float:
+    if layer.spec.scoring == synth.SOFTMAX_BIAS:
+        return MARGIN_REL_SOFTMAX_BIAS * float(np.max(np.abs(keys_row)))
+    return MARGIN
 
 
 def topk_gap(keys_row: np.ndarray, k: int) -> float:
@@ -41,7 +50,8 @@ def tokens_with_margin(layer, N: int, seed=None, max_attempts: int = 2000) -> np
     for n in range(N):
         for attempt in range(max_attempts):
             r = synth.x_row(sp, seed, n, attempt)[None, :]
-            if topk_gap(selection_keys(layer, r)[0], sp.top_k) >= MARGIN:
+            keys = selection_keys(layer, r)[0]
+            if topk_gap(keys, sp.top_k) >= margin_for(layer, keys):
                 rows.append(r[0])
                 break
         else:

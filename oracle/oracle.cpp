@@ -28,6 +28,12 @@
 //     into w4a16_gemv_batch3 / w4a16_gemm / w4a16_decode_gemv) — the router
 //     weight may be NVFP4 (E2M1 + per-16 E4M3 scale + FP32 scale2) against the
 //     BF16 activations;
+//   * forward_k3.rs / forward_batched.rs, the zero-expert guards ("LongCat
+//     zero-experts", a router of width num_experts + zero_expert_num "served
+//     only through the softmax+bias arm") — routing over E + Z router outputs
+//     with softmax scores plus a correction bias for selection; a selected
+//     zero expert runs no expert.  The pages do not say what a zero expert
+//     adds; the reading taken is nothing (its output is zero);
 //   * forward_atomic_c4.rs, doc comment — routed outputs accumulated as
 //     routing-weighted sums, then cast to BF16 and blended with the shared
 //     expert;
@@ -205,20 +211,23 @@ void oracle_router_logits_fmt(const uint16_t* x, const uint8_t* wr, const uint8_
 //   scoring 1 (sigmoid + correction bias): s = 1/(1+exp(-l)); selection score
 //       = s + bias; w = s of the selected experts (bias only selects), divided
 //       by their sum if norm != 0, then multiplied by rsf.
+//   scoring 2 (softmax + correction bias, the zero-expert routers): p =
+//       softmax(l); selection score = p + bias; w = p of the selected, divided
+//       by their sum if norm != 0, then multiplied by rsf.
 // Top-k: sort by selection score descending, ties to the lower expert index;
 // the first k in that order are the selected experts, in that order.
 // sel_score (optional, [E]) receives the selection score of every expert.
 void oracle_route_one(const double* l, const float* bias, int E, int k, int scoring,
                       int norm, double rsf, int32_t* idx, double* w, double* sel_score) {
     std::vector<double> score(E), base(E);
-    if (scoring == 0) {
+    if (scoring == 0 || scoring == 2) {
         double mx = l[0];
         for (int e = 1; e < E; ++e) mx = std::max(mx, l[e]);
         double den = 0.0;
         for (int e = 0; e < E; ++e) den += std::exp(l[e] - mx);
         for (int e = 0; e < E; ++e) {
             base[e] = std::exp(l[e] - mx) / den;
-            score[e] = base[e];
+            score[e] = base[e] + ((scoring == 2 && bias) ? (double)bias[e] : 0.0);
         }
     } else {
         for (int e = 0; e < E; ++e) {
@@ -240,7 +249,7 @@ void oracle_route_one(const double* l, const float* bias, int E, int k, int scor
     }
     if (norm)
         for (int j = 0; j < k; ++j) w[j] /= sum;
-    if (scoring == 1)
+    if (scoring != 0)
         for (int j = 0; j < k; ++j) w[j] *= rsf;
     if (sel_score)
         for (int e = 0; e < E; ++e) sel_score[e] = score[e];
@@ -340,22 +349,27 @@ struct oracle_weights {
 // shared expert.  out_bf16 is out_f64 rounded to BF16 (nearest even).
 // idx/w receive the routing ([N, k]); logits (optional) the router output.
 // router_fmt: 0 = BF16 router, 1 = NVFP4 router (router holds the codes).
+// Z zero experts: the router (and bias) has E + Z rows, routing runs over all
+// E + Z, and a slot that selects index >= E adds nothing; logits_out is
+// [N, E + Z].
 int oracle_moe_forward(int H, int inter, int E, int k, int scoring, int norm, double rsf,
                        int fmt, int Is, const oracle_weights* W, const uint16_t* x, int N,
                        double* out_f64, uint16_t* out_bf16, int32_t* idx, double* w,
-                       double* logits_out, int router_fmt) {
-    if (H <= 0 || inter <= 0 || E <= 0 || k <= 0 || k > E || N < 0) return 1;
+                       double* logits_out, int router_fmt, int Z) {
+    if (H <= 0 || inter <= 0 || E <= 0 || Z < 0 || k <= 0 || k > E + Z || N < 0) return 1;
+    if (scoring < 0 || scoring > 2) return 1;
+    const int R = E + Z;   // router width
     if (fmt < 0 || fmt > 3 || router_fmt < 0 || router_fmt > 1) return 1;
     const int gs = (fmt == 0) ? 16 : 32;
-    std::vector<double> logits((size_t)N * E);
+    std::vector<double> logits((size_t)N * R);
     if (router_fmt == 0)
-        oracle_router_logits(x, W->router, N, E, H, logits.data());
+        oracle_router_logits(x, W->router, N, R, H, logits.data());
     else
         oracle_router_logits_fmt(x, reinterpret_cast<const uint8_t*>(W->router), W->router_s,
-                                 W->router_s2 ? (double)W->router_s2[0] : 1.0, 1, N, E, H,
+                                 W->router_s2 ? (double)W->router_s2[0] : 1.0, 1, N, R, H,
                                  logits.data());
     if (logits_out) std::copy(logits.begin(), logits.end(), logits_out);
-    oracle_route(logits.data(), W->bias, N, E, k, scoring, norm, rsf, idx, w, nullptr);
+    oracle_route(logits.data(), W->bias, N, R, k, scoring, norm, rsf, idx, w, nullptr);
 
     // bytes per expert of each table (BF16: two bytes per element, no scales;
     // FP8: one byte per element, 4-byte scales per 128 x 128 block)
@@ -371,6 +385,7 @@ int oracle_moe_forward(int H, int inter, int E, int k, int scoring, int norm, do
         std::vector<double> acc(H, 0.0);
         for (int j = 0; j < k; ++j) {
             const int e = idx[(long)n * k + j];
+            if (e >= E) continue;              // zero expert: adds nothing
             const bool fp4 = !bf && !f8;   // only the FP4 formats have scale2
             const double g2 = (fp4 && W->gate_s2) ? W->gate_s2[e] : 1.0;
             const double u2 = (fp4 && W->up_s2) ? W->up_s2[e] : 1.0;

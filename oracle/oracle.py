@@ -77,7 +77,7 @@ def lib():
             L.oracle_moe_forward.restype = i32
             L.oracle_moe_forward.argtypes = [i32, i32, i32, i32, i32, i32, d, i32, i32,
                                              ctypes.POINTER(_Weights), vp, i32,
-                                             vp, vp, vp, vp, vp, i32]
+                                             vp, vp, vp, vp, vp, i32, i32]
             L.oracle_num_threads.restype = i32
             L.oracle_num_threads.argtypes = []
             _lib = L
@@ -111,6 +111,10 @@ def bf16(bits: int) -> float:
 
 def round_bf16(v: float) -> int:
     return lib().oracle_round_bf16(float(v))
+
+
+def scoring_code(scoring: str) -> int:
+    return {"softmax": 0, "sigmoid_bias": 1, "softmax_bias": 2}[scoring]
 
 
 def fmt_code(wfmt: str) -> int:
@@ -163,7 +167,7 @@ def route(logits: np.ndarray, k: int, scoring: str, norm: bool, rsf: float = 1.0
     w = np.empty((N, k), dtype=np.float64)
     sel = np.empty((N, E), dtype=np.float64)
     b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
-    lib().oracle_route(_p(logits), _p(b), N, E, k, 0 if scoring == "softmax" else 1,
+    lib().oracle_route(_p(logits), _p(b), N, E, k, scoring_code(scoring),
                        int(bool(norm)), float(rsf), _p(idx), _p(w), _p(sel))
     return idx, w, sel
 
@@ -217,13 +221,13 @@ def moe_forward(layer, x: np.ndarray):
     outb = np.empty((N, sp.H), dtype=np.uint16)
     idx = np.empty((N, sp.top_k), dtype=np.int32)
     w = np.empty((N, sp.top_k), dtype=np.float64)
-    logits = np.empty((N, sp.E), dtype=np.float64)
+    logits = np.empty((N, sp.E + sp.zero_experts), dtype=np.float64)
     W = _weights_struct(layer)
     rc = lib().oracle_moe_forward(
-        sp.H, sp.inter, sp.E, sp.top_k, 0 if sp.scoring == "softmax" else 1,
+        sp.H, sp.inter, sp.E, sp.top_k, scoring_code(sp.scoring),
         int(sp.norm_topk_prob), float(sp.routed_scaling_factor), fmt_code(sp.wfmt),
         sp.shared_inter, ctypes.byref(W), _p(x), N, _p(out), _p(outb), _p(idx), _p(w),
-        _p(logits), 1 if sp.router_fmt == "nvfp4" else 0)
+        _p(logits), 1 if sp.router_fmt == "nvfp4" else 0, sp.zero_experts)
     if rc != 0:
         raise ValueError(f"oracle_moe_forward rejected its arguments (code {rc})")
     return {"out_f64": out, "out_bf16": outb, "idx": idx, "w": w, "logits": logits}

@@ -257,6 +257,25 @@ def test_topk_bruteforce_tiny_E_sigmoid_bias(oracle_mod):
                     np.testing.assert_allclose(w[n], ref, rtol=1e-14)
 
 
+def test_topk_bruteforce_tiny_E_softmax_bias(oracle_mod):
+    """Softmax scores plus a correction bias select (the zero-expert routers'
+    softmax+bias arm); the weights are the selected softmax scores,
+    renormalised if asked, times the routed scaling factor."""
+    rng = np.random.default_rng(17)
+    for E in range(1, 9):
+        for k in range(1, E + 1):
+            logits = rng.standard_normal((2, E))
+            bias = (rng.standard_normal(E) * 0.2).astype(np.float32)
+            for norm in (False, True):
+                idx, w, sel = oracle_mod.route(logits, k, "softmax_bias", norm, 1.7, bias)
+                for n in range(2):
+                    p = scipy.special.softmax(logits[n])
+                    want = _brute_topk(p + bias.astype(np.float64), k)
+                    assert list(idx[n]) == want
+                    ref = p[want] / (p[want].sum() if norm else 1.0) * 1.7
+                    np.testing.assert_allclose(w[n], ref, rtol=1e-14)
+
+
 def test_routing_weights_sum(oracle_mod):
     rng = np.random.default_rng(8)
     logits = rng.standard_normal((16, 128)) * 2
@@ -499,6 +518,55 @@ def test_nvfp4_router_equals_bf16_router_with_the_same_values(oracle_mod):
     np.testing.assert_array_equal(r["logits"], rb["logits"])
     np.testing.assert_array_equal(r["idx"], rb["idx"])
     np.testing.assert_array_equal(r["out_f64"], rb["out_f64"])
+
+
+def test_zero_experts_add_nothing(oracle_mod):
+    """Zero experts (router width E + Z): slots that select an index >= E run
+    no expert.  (a) Zero experts pulled out by their bias: the layer equals
+    the same E experts without zero experts (renormalised weights do not see
+    the extra softmax terms).  (b) Zero experts pulled in for every slot: only
+    the shared expert is left.  (c) A mix: the output is the weighted sum over
+    the real-expert slots alone, computed expert by expert."""
+    import dataclasses
+    sp = _small_spec(E=6, top_k=3, H=96, inter=64, scoring=synth.SOFTMAX_BIAS,
+                     zero_experts=4, shared_inter=32, shared_gated=True)
+    L = synth.make_layer(sp, seed=51)
+    assert L.router.shape == (10, 96) and L.bias.shape == (10,)
+    x = synth.make_tokens(sp, 4, seed=52)
+    # (a)
+    # (the real experts' bias is zero here: the extra softmax terms scale every
+    # real score by one factor, which keeps their order only without a bias)
+    La = dataclasses.replace(L, bias=L.bias.copy())
+    La.bias[:6] = 0.0
+    La.bias[6:] = -10.0
+    spE = dataclasses.replace(sp, zero_experts=0)
+    LE = dataclasses.replace(L, spec=spE, router=L.router[:6].copy(), bias=La.bias[:6].copy())
+    ra, rE = oracle_mod.moe_forward(La, x), oracle_mod.moe_forward(LE, x)
+    assert ra["logits"].shape == (4, 10) and np.all(ra["idx"] < 6)
+    np.testing.assert_array_equal(ra["idx"], rE["idx"])
+    np.testing.assert_allclose(ra["out_f64"], rE["out_f64"], rtol=1e-12, atol=1e-15)
+    # (b)
+    Lb = dataclasses.replace(L, bias=L.bias.copy())
+    Lb.bias[6:] = 10.0
+    rb = oracle_mod.moe_forward(Lb, x)
+    assert np.all(rb["idx"] >= 6)
+    for n in range(4):
+        d = float(_bf16_arr(L.sh_gate_w) @ _bf16_arr(x[n]))
+        ref = scipy.special.expit(d) * _dense_shared(L, _bf16_arr(x[n]))
+        np.testing.assert_allclose(rb["out_f64"][n], ref, rtol=1e-12, atol=1e-15)
+    # (c)
+    Lc = dataclasses.replace(L, bias=L.bias.copy())
+    Lc.bias[6:8] = 10.0                      # two of the k = 3 slots are zero experts
+    Lc.bias[8:] = -10.0
+    rc = oracle_mod.moe_forward(Lc, x)
+    for n in range(4):
+        assert sum(int(e) >= 6 for e in rc["idx"][n]) == 2
+        x64 = _bf16_arr(x[n])
+        ref = sum(rc["w"][n, j] * _dense_swiglu(L, int(e), x64)
+                  for j, e in enumerate(rc["idx"][n]) if e < 6)
+        d = float(_bf16_arr(L.sh_gate_w) @ x64)
+        ref = ref + scipy.special.expit(d) * _dense_shared(L, x64)
+        np.testing.assert_allclose(rc["out_f64"][n], ref, rtol=1e-11, atol=1e-14)
 
 
 def test_scale2_scales_each_projection(oracle_mod):

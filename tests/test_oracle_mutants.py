@@ -30,7 +30,7 @@ MUTANTS = {
     "ties_to_higher_index": ("return a < b;", "return a > b;"),
     "ascending_sort": ("return score[a] > score[b];", "return score[a] < score[b];"),
     "no_renorm": ("if (norm)\n", "if (0)\n"),
-    "rsf_on_softmax": ("if (scoring == 1)\n        for (int j = 0; j < k; ++j) w[j] *= rsf;",
+    "rsf_on_softmax": ("if (scoring != 0)\n        for (int j = 0; j < k; ++j) w[j] *= rsf;",
                        "for (int j = 0; j < k; ++j) w[j] *= rsf;"),
     "softmax_denominator": ("den += std::exp(l[e] - mx);", "den += std::exp(l[e]);"),
     "down_transposed": ("oracle_weight(dq, dsc, d2, inter, fmt, r, i)",
@@ -43,6 +43,11 @@ MUTANTS = {
     "router_nvfp4_as_mxfp4": ("return oracle_fp4_weight(wr, rs, rs2, H, 0, e, h);",
                               "return oracle_fp4_weight(wr, rs, rs2, H, 1, e, h);"),
     "router_scale2_ignored": ("W->router_s2 ? (double)W->router_s2[0] : 1.0", "1.0"),
+    "softmax_bias_ignored": ("score[e] = base[e] + ((scoring == 2 && bias) ? (double)bias[e] : 0.0);",
+                             "score[e] = base[e];"),
+    "softmax_bias_no_rsf": ("if (scoring != 0)\n        for (int j = 0; j < k; ++j) w[j] *= rsf;",
+                            "if (scoring == 1)\n        for (int j = 0; j < k; ++j) w[j] *= rsf;"),
+    "zero_expert_runs_expert_0": ("if (e >= E) continue;", "if (e >= E) { }"),
     "fp8_row_block_ignored": ("s + 4 * ((r / 128) * kb + k / 128)", "s + 4 * (k / 128)"),
     "fp8_scale_ignored": ("return oracle_e4m3(q[r * (long)K + k]) * (double)sc;",
                           "return oracle_e4m3(q[r * (long)K + k]) * (sc > 0 ? 1.0 : 0.0);"),
