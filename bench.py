@@ -16,8 +16,9 @@ maximum over ranks is taken.  The line also carries "grouped": the many-token
 path (gpt-oss-shaped MXFP4 layer at N = 512, tcgen05 GEMMs),
 "bf16_experts" and "fp8_experts": the same Qwen3 shape with BF16 or FP8
 (128 x 128 block-scaled) routed experts at N = 1-4, and "nvfp4_router": the
-Qwen3 shape with an NVFP4-quantised router, all timed on the same GPU after
-the main measurement.  --impl reference
+Qwen3 shape with an NVFP4-quantised router, and "zero_experts": the Qwen3
+shape with 64 zero experts (softmax + correction-bias routing over 192
+router outputs), all timed on the same GPU after the main measurement.  --impl reference
 times the FP64 CPU oracle on a bounded sample of the same workload instead.
 """
 from __future__ import annotations
@@ -131,7 +132,7 @@ class ClockSampler:
 def algorithmic_bytes(spec, idx: np.ndarray, N: int) -> dict:
     """Bytes one call must move: touched routed experts, router, shared expert,
     x in and out."""
-    U = len(np.unique(idx))
+    U = len(np.unique(idx[idx < spec.E]))   # zero experts (index >= E) read no weights
     routed = U * spec.expert_bytes()
     other = spec.router_bytes() + spec.shared_bytes() + 2 * N * spec.H * 2
     return {"U": U, "routed": routed, "total": routed + other}
@@ -454,6 +455,9 @@ def run_gpu(args):
     if rank == 0 and not args.no_nvfp4_router:
         result["nvfp4_router"] = measure_decode_config(stream, "qwen3_30b_a3b_nvfp4_router",
                                                        (1, 2, 3, 4))
+    if rank == 0 and not args.no_zero_experts:
+        result["zero_experts"] = measure_decode_config(stream, "qwen3_30b_a3b_zero_experts",
+                                                       (1, 2, 3, 4))
     if rank == 0:
         result["clocks"] = clk.summary()
         if not args.no_cpu_baseline:
@@ -547,6 +551,8 @@ def main():
                     help="skip the FP8 routed-expert decode measurement")
     ap.add_argument("--no-nvfp4-router", action="store_true",
                     help="skip the NVFP4-router decode measurement")
+    ap.add_argument("--no-zero-experts", action="store_true",
+                    help="skip the zero-expert routing decode measurement")
     ap.add_argument("--no-grouped", action="store_true",
                     help="skip the grouped-path (gpt-oss N=512) measurement")
     args = ap.parse_args()

@@ -8,7 +8,10 @@
  *   2. top-k routing   softmax (optionally renormalised over the selected k)
  *                      or sigmoid + correction bias for selection, sigmoid
  *                      for the weights, optional renormalisation, times the
- *                      routed scaling factor;
+ *                      routed scaling factor; or softmax + correction bias
+ *                      (the zero-expert routers) likewise; with Z zero
+ *                      experts the router has E + Z outputs and a selected
+ *                      zero expert runs no expert;
  *   3. routed experts  SwiGLU with block-scaled FP4 weights:
  *                      h = SiLU(Dq(Wg) x) * (Dq(Wu) x),  y = Dq(Wd) h,
  *                      Dq(w) = E2M1(code) * blockscale * scale2;
@@ -48,8 +51,8 @@
  * given stream (a cudaStream_t passed as void*; NULL = legacy default stream).
  *
  * Weight layout (canonical, row-major, K contiguous):
- *   router     [E, H]          bf16
- *   bias       [E]             f32, sigmoid scoring only (NULL otherwise)
+ *   router     [E + Z, H]      bf16 (Z = zero experts, usually 0)
+ *   bias       [E + Z]         f32, the bias scorings only (NULL otherwise)
  *   gate_q     [E, inter, H/2] u8  two E2M1 codes per byte, element 2j in the
  *   up_q       [E, inter, H/2] u8  low nibble, 2j+1 in the high nibble
  *   down_q     [E, H, inter/2] u8
@@ -99,7 +102,11 @@ typedef enum {
   MOE_ERR_TIMEOUT = 5               /* a bounded device-side wait gave up */
 } moe_status_t;
 
-typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID_BIAS = 1 } moe_scoring_t;
+typedef enum {
+  MOE_SCORE_SOFTMAX = 0,        /* softmax; routed_scaling_factor not applied */
+  MOE_SCORE_SIGMOID_BIAS = 1,   /* sigmoid + correction bias */
+  MOE_SCORE_SOFTMAX_BIAS = 2    /* softmax + correction bias (zero-expert routers) */
+} moe_scoring_t;
 /* Routed-expert weight formats: NVFP4 (E2M1 + per-16 E4M3 scale + FP32
  * scale2), MXFP4 (E2M1 + per-32 E8M0 scale), BF16 (plain weights), FP8 (E4M3
  * + FP32 scale per 128 x 128 block). */
@@ -118,15 +125,17 @@ typedef struct {
   int32_t top_k;                 /* experts per token, 1..min(E, 32) */
   int32_t scoring;               /* moe_scoring_t */
   int32_t norm_topk_prob;        /* 0/1: renormalise the selected weights */
-  float routed_scaling_factor;   /* sigmoid scoring only; ignored for softmax */
+  float routed_scaling_factor;   /* the bias scorings only; ignored for plain softmax */
   int32_t wfmt;                  /* moe_wfmt_t */
   int32_t shared_inter;          /* shared expert intermediate size; 0 = none */
   int32_t router_fmt;            /* moe_rfmt_t (0 = BF16 router) */
+  int32_t zero_experts;          /* Z >= 0: router width E + Z (the pages' num_experts +
+                                    zero_expert_num); E + Z <= 1024 */
 } moe_layer_desc_t;
 
 typedef struct {
   const void* router;            /* bf16 [E, H], or E2M1 codes [E, H/2] (NVFP4 router) */
-  const float* bias;             /* f32 [E] (required iff scoring is sigmoid+bias) */
+  const float* bias;             /* f32 [E + Z] (required iff the scoring has a bias) */
   const uint8_t* gate_q;
   const uint8_t* up_q;
   const uint8_t* down_q;
@@ -169,9 +178,10 @@ MOE_API moe_status_t moe_workspace_init(void* workspace, size_t ws_bytes, void* 
  * N*top_k <= 256 runs one fused decode kernel; larger N runs the grouped
  * path (per-expert token groups on the tcgen05 tensor cores, the pages'
  * "grouped GEMM (more than 64 rows)" of forward_batched.rs), which takes
- * neither a shared expert nor BF16 / FP8 routed experts yet: N*top_k > 256
- * with shared_inter > 0 or wfmt MOE_W_BF16 / MOE_W_FP8 returns
- * MOE_ERR_UNSUPPORTED.  Asynchronous on `stream`; no host synchronisation,
+ * neither a shared expert, BF16 / FP8 routed experts nor zero experts yet:
+ * N*top_k > 256 with shared_inter > 0, wfmt MOE_W_BF16 / MOE_W_FP8 or
+ * zero_experts > 0 returns MOE_ERR_UNSUPPORTED.  With zero experts, topk_idx
+ * holds indices up to E + Z - 1 (>= E: a zero expert).  Asynchronous on `stream`; no host synchronisation,
  * no allocation, so it may be captured in a CUDA graph.  Argument errors are
  * returned before anything is enqueued; device-side timeouts are reported by
  * moe_get_error. */

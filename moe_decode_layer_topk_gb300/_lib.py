@@ -23,6 +23,7 @@ MOE_ERR_CUDA = 4
 MOE_ERR_TIMEOUT = 5
 MOE_SCORE_SOFTMAX = 0
 MOE_SCORE_SIGMOID_BIAS = 1
+MOE_SCORE_SOFTMAX_BIAS = 2
 MOE_W_NVFP4 = 0
 MOE_W_MXFP4 = 1
 MOE_W_BF16 = 2
@@ -46,7 +47,7 @@ class LayerDesc(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("scoring", ctypes.c_int32),
                 ("norm_topk_prob", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
                 ("wfmt", ctypes.c_int32), ("shared_inter", ctypes.c_int32),
-                ("router_fmt", ctypes.c_int32)]
+                ("router_fmt", ctypes.c_int32), ("zero_experts", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):

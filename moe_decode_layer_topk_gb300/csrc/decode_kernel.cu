@@ -185,7 +185,8 @@ __device__ bool grid_wait(Ctrl* c, unsigned long long target, uint64_t budget_ns
 __device__ __noinline__ void router_phase(const Params& p, int cta, int G, Tables& tb, int ctid) {
   const int H = p.H;
   const float rs2 = (p.router_fmt == 1 && p.router_s2) ? __ldg(p.router_s2) : 1.0f;
-  for (int e = cta; e < p.E; e += G) {
+  const int R = p.E + p.Z;   // router width (zero experts included)
+  for (int e = cta; e < R; e += G) {
     for (int n0 = 0; n0 < p.N; n0 += 8) {
       const int nn = min(8, p.N - n0);
       float acc[8];
@@ -213,7 +214,7 @@ __device__ __noinline__ void router_phase(const Params& p, int cta, int G, Table
 #pragma unroll
         for (int t = 1; t < 8; ++t)
           if (ctid == t) v = acc[t];
-        p.logits[(size_t)(n0 + ctid) * p.E + e] = v;
+        p.logits[(size_t)(n0 + ctid) * R + e] = v;
       }
     }
   }
@@ -290,8 +291,9 @@ __device__ __forceinline__ void topk_token(int E, int k, int scoring, int norm, 
 
 // Small case (S = N*k <= 32, every expert has <= kTB tokens): the same tables
 // as build_tables, from one slot per lane in registers.
-__device__ __forceinline__ bool build_tables_small(int k, int S, Tables& tb, int lane) {
-  const bool v = lane < S;
+__device__ __forceinline__ bool build_tables_small(int E, int k, int S, Tables& tb, int lane) {
+  // slots that selected a zero expert (index >= E) run no expert
+  const bool v = lane < S && tb.sel_e[lane] < E;
   const int e = v ? tb.sel_e[lane] : -1 - lane;
   const float wv = v ? tb.sel_w[lane] : 0.f;
   const uint32_t lt = (1u << lane) - 1u;
@@ -335,14 +337,15 @@ __device__ __forceinline__ void build_tables(int E, int k, int S, Tables& tb, in
   uint32_t* first = tb.cnt;              // first slot of each expert, then its unique index
   for (int e = lane; e < E; e += 32) first[e] = 0xFFFFFFFFu;
   __syncwarp();
-  for (int s = lane; s < S; s += 32) atomicMin(&first[tb.sel_e[s]], (uint32_t)s);
+  for (int s = lane; s < S; s += 32)
+    if (tb.sel_e[s] < E) atomicMin(&first[tb.sel_e[s]], (uint32_t)s);   // zero experts: none
   __syncwarp();
   const uint32_t lt = (1u << lane) - 1u;
   int U = 0;
   for (int b = 0; b < S; b += 32) {          // unique experts in first-slot order
     const int s = b + lane;
     const int e = (s < S) ? tb.sel_e[s] : 0;
-    const bool isfirst = (s < S) && first[e] == (uint32_t)s;
+    const bool isfirst = (s < S) && e < E && first[e] == (uint32_t)s;
     const uint32_t mask = __ballot_sync(0xffffffffu, isfirst);
     if (isfirst) {
       const int u = U + __popc(mask & lt);
@@ -356,7 +359,7 @@ __device__ __forceinline__ void build_tables(int E, int k, int S, Tables& tb, in
   // token positions within each expert, in slot order (peers = same expert)
   for (int b = 0; b < S; b += 32) {
     const int s = b + lane;
-    const bool v = s < S;
+    const bool v = s < S && tb.sel_e[s] < E;
     const int e = v ? tb.sel_e[s] : -1 - lane;
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
     int u = 0, pos = 0;
@@ -387,6 +390,7 @@ __device__ __forceinline__ void build_tables(int E, int k, int S, Tables& tb, in
   }
   __syncwarp();
   for (int s = lane; s < S; s += 32) {
+    if (tb.sel_e[s] >= E) continue;
     const int u = (int)(first[tb.sel_e[s]] & 0x7FFFFFFFu);
     const int slot = tb.hoff[u] + tb.unit_tb[s];
     tb.utok[slot] = (uint8_t)(s / k);
@@ -421,20 +425,21 @@ __device__ __forceinline__ void build_tables(int E, int k, int S, Tables& tb, in
 __device__ __noinline__ void routing_phase(const Params& p, int write_out, Tables& tb, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int E = p.E, k = p.k, S = p.N * p.k, scoring = p.scoring, norm = p.norm;
+  const int R = E + p.Z;   // top-k runs over the whole router width
   const float rsf = p.rsf;
   const float* bias = p.bias;
   for (int n = warp; n < p.N; n += kConsumerWarps) {
-    const float* lrow = p.logits + (size_t)n * E;
-    if (E <= 128) topk_token<4>(E, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
-    else if (E <= 256) topk_token<8>(E, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
-    else if (E <= 512) topk_token<16>(E, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
-    else topk_token<32>(E, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
+    const float* lrow = p.logits + (size_t)n * R;
+    if (R <= 128) topk_token<4>(R, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
+    else if (R <= 256) topk_token<8>(R, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
+    else if (R <= 512) topk_token<16>(R, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
+    else topk_token<32>(R, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
   }
   if (!p.route_only && warp == kConsumerWarps - 1)
     for (int n = lane; n < p.N; n += 32) tb.xe[n] = (int16_t)ld_cg_s32(p.xexp + n);
   consumer_sync();
   if (warp == 0) {
-    const bool done = (S <= 32) && build_tables_small(k, S, tb, lane);
+    const bool done = (S <= 32) && build_tables_small(E, k, S, tb, lane);
     if (!done) build_tables(E, k, S, tb, lane);
   }
   if (write_out && warp == 1) {

@@ -39,7 +39,7 @@ WsLayout ws_layout(const moe_layer_desc_t& d, int32_t N) {
     return o;
   };
   L.ctrl = take(256);
-  L.logits = take((size_t)N * d.E * 4);
+  L.logits = take((size_t)N * (d.E + d.zero_experts) * 4);
   L.x16 = take((size_t)N * d.H * 2);
   L.xexp = take((size_t)N * 4);
   L.gsig = take((size_t)N * 4);
@@ -104,15 +104,19 @@ size_t ws_total(const moe_layer_desc_t& d, int32_t max_tokens) {
 moe_status_t check_desc(const moe_layer_desc_t* d) {
   if (!d) return MOE_ERR_INVALID_ARG;
   if (d->H <= 0 || d->inter <= 0 || d->E <= 0 || d->top_k <= 0) return MOE_ERR_INVALID_ARG;
-  if (d->scoring != MOE_SCORE_SOFTMAX && d->scoring != MOE_SCORE_SIGMOID_BIAS)
+  if (d->scoring != MOE_SCORE_SOFTMAX && d->scoring != MOE_SCORE_SIGMOID_BIAS &&
+      d->scoring != MOE_SCORE_SOFTMAX_BIAS)
     return MOE_ERR_INVALID_ARG;
+  if (d->zero_experts < 0) return MOE_ERR_INVALID_ARG;
   if (d->wfmt != MOE_W_NVFP4 && d->wfmt != MOE_W_MXFP4 && d->wfmt != MOE_W_BF16 &&
       d->wfmt != MOE_W_FP8)
     return MOE_ERR_INVALID_ARG;
   if (d->shared_inter < 0) return MOE_ERR_INVALID_ARG;
   if (d->router_fmt != MOE_R_BF16 && d->router_fmt != MOE_R_NVFP4) return MOE_ERR_INVALID_ARG;
   if (d->H % 32 || d->inter % 32 || d->shared_inter % 32) return MOE_ERR_UNSUPPORTED;
-  if (d->E > moe::kMaxE || d->top_k > d->E || d->top_k > moe::kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  if (d->E + d->zero_experts > moe::kMaxE || d->top_k > d->E + d->zero_experts ||
+      d->top_k > moe::kMaxTopK)
+    return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -126,7 +130,7 @@ moe_status_t check_weights(const moe_layer_desc_t* d, const moe_weights_t* w) {
     for (const void* p : sc)
       if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
   }
-  if (d->scoring == MOE_SCORE_SIGMOID_BIAS && !w->bias) return MOE_ERR_INVALID_ARG;
+  if (d->scoring != MOE_SCORE_SOFTMAX && !w->bias) return MOE_ERR_INVALID_ARG;
   if (d->router_fmt == MOE_R_NVFP4 && (!w->router_s || !aligned16(w->router_s)))
     return MOE_ERR_INVALID_ARG;
   if (d->shared_inter > 0) {
@@ -300,6 +304,7 @@ moe_status_t run_grouped(const moe_layer_desc_t* d, const moe_weights_t* w, cons
   if (d->shared_inter > 0) return MOE_ERR_UNSUPPORTED;   // shared expert: decode sizes only
   if (d->wfmt == MOE_W_BF16 || d->wfmt == MOE_W_FP8)
     return MOE_ERR_UNSUPPORTED;   // BF16 / FP8 experts: decode sizes only
+  if (d->zero_experts > 0) return MOE_ERR_UNSUPPORTED;   // zero experts: decode sizes only
   const GWsLayout L = gws_layout(*d, N);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   int budget = 0, grid = 0;
@@ -325,7 +330,7 @@ moe_status_t run_grouped(const moe_layer_desc_t* d, const moe_weights_t* w, cons
   gp.router_fmt = d->router_fmt;
   gp.router_s = d->router_fmt == MOE_R_NVFP4 ? w->router_s : nullptr;
   gp.router_s2 = d->router_fmt == MOE_R_NVFP4 ? w->router_s2 : nullptr;
-  gp.bias = d->scoring == MOE_SCORE_SIGMOID_BIAS ? w->bias : nullptr;
+  gp.bias = d->scoring != MOE_SCORE_SOFTMAX ? w->bias : nullptr;
   gp.topk_idx = topk_idx;
   gp.topk_w = topk_w;
   gp.out = static_cast<uint16_t*>(out);
@@ -434,7 +439,8 @@ moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* 
   p.router_fmt = d->router_fmt;
   p.router_s = d->router_fmt == MOE_R_NVFP4 ? w->router_s : nullptr;
   p.router_s2 = d->router_fmt == MOE_R_NVFP4 ? w->router_s2 : nullptr;
-  p.bias = d->scoring == MOE_SCORE_SIGMOID_BIAS ? w->bias : nullptr;
+  p.bias = d->scoring != MOE_SCORE_SOFTMAX ? w->bias : nullptr;
+  p.Z = d->zero_experts;
   // BF16 experts read no scales; FP8 experts their f32 block scales; only
   // the FP4 formats have scale2
   const bool scales = d->wfmt != MOE_W_BF16;

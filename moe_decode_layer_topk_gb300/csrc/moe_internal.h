@@ -85,6 +85,7 @@ struct Params {
   uint32_t tm_valid;          // bit i set when tm[i] is encoded
   // layer
   int H, inter, E, k, scoring, norm;
+  int Z;     // zero experts: router width E + Z, selected zero experts run nothing
   float rsf;
   int fmt;   // FMT_NVFP4 / FMT_MXFP4 / FMT_BF16 / FMT_FP8 for the routed experts
   int Is;    // shared expert intermediate size (0 = none)

@@ -1,10 +1,12 @@
 // Warp-level top-k routing of one token, shared by the decode and grouped
 // kernels.  Scoring follows the gating step of the forward chain: softmax
 // (selection by logit, weights softmax over all E, optionally renormalised
-// over the selected) or sigmoid + correction bias (selection by
+// over the selected), sigmoid + correction bias (selection by
 // sigmoid(l) + bias, weights sigmoid(l) without the bias, optional
-// renormalisation, then times the routed scaling factor).  Ties go to the
-// lower expert index.
+// renormalisation, then times the routed scaling factor), or softmax +
+// correction bias (the zero-expert routers: selection by softmax(l) + bias,
+// weights softmax(l), optional renormalisation, times the routed scaling
+// factor).  Ties go to the lower expert index.
 #pragma once
 #include <math.h>
 #include <stdint.h>
@@ -59,13 +61,28 @@ __device__ __forceinline__ void topk_warp(int E, int k, int scoring, int norm, f
   uint32_t key[PER];
   float mx = -INFINITY;
 #pragma unroll
+  for (int i = 0; i < PER; ++i)
+    if (lane + 32 * i < E) mx = fmaxf(mx, lg[i]);
+  float den = 0.f;
+  if (scoring != 1) {   // softmax denominator over all E (weights; keys of scoring 2)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      if (lane + 32 * i < E) den += expf(lg[i] - mx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  }
+#pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int e = lane + 32 * i;
     key[i] = 0u;
     if (e < E) {
       const float l = lg[i];
-      mx = fmaxf(mx, l);
-      key[i] = order_key(scoring == 1 ? 1.0f / (1.0f + expf(-l)) + bias[e] : l);
+      const float sc = (scoring == 0) ? l
+                     : (scoring == 1) ? 1.0f / (1.0f + expf(-l)) + bias[e]
+                                      : expf(l - mx) / den + bias[e];
+      key[i] = order_key(sc);
     }
   }
   uint32_t bk = 0u, be = 0xFFFFFFFFu;   // lane-local best, lowest index among equals
@@ -89,16 +106,6 @@ __device__ __forceinline__ void topk_warp(int E, int k, int scoring, int norm, f
         if (key[i] > bk) { bk = key[i]; be = lane + 32 * i; }
     }
   }
-  float den = 0.f;
-  if (scoring == 0) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-#pragma unroll
-    for (int i = 0; i < PER; ++i)
-      if (lane + 32 * i < E) den += expf(lg[i] - mx);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-  }
   // logit of this lane's selection, from the lane that holds it
   float l = 0.f;
 #pragma unroll
@@ -107,13 +114,13 @@ __device__ __forceinline__ void topk_warp(int E, int k, int scoring, int norm, f
     if ((int)(mine >> 5) == i) l = v;
   }
   float w = 0.f;
-  if (lane < k) w = (scoring == 0) ? expf(l - mx) / den : 1.0f / (1.0f + expf(-l));
+  if (lane < k) w = (scoring != 1) ? expf(l - mx) / den : 1.0f / (1.0f + expf(-l));
   float wsum = w;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
   if (lane < k) {
     if (norm) w = w / wsum;
-    if (scoring == 1) w *= rsf;
+    if (scoring != 0) w *= rsf;
     *e_out = (int)mine;
     *w_out = w;
   }

@@ -11,19 +11,22 @@ import numpy as np
 import torch
 
 from . import _lib
-from .synth import BF16, FP8, HostLayer, LayerSpec, MXFP4, NVFP4, SOFTMAX
+from .synth import (BF16, FP8, HostLayer, LayerSpec, MXFP4, NVFP4, SIGMOID_BIAS, SOFTMAX,
+                    SOFTMAX_BIAS)
 
 
 def layer_desc(spec: LayerSpec) -> _lib.LayerDesc:
     d = _lib.LayerDesc()
     d.H, d.inter, d.E, d.top_k = spec.H, spec.inter, spec.E, spec.top_k
-    d.scoring = _lib.MOE_SCORE_SOFTMAX if spec.scoring == SOFTMAX else _lib.MOE_SCORE_SIGMOID_BIAS
+    d.scoring = {SOFTMAX: _lib.MOE_SCORE_SOFTMAX, SIGMOID_BIAS: _lib.MOE_SCORE_SIGMOID_BIAS,
+                 SOFTMAX_BIAS: _lib.MOE_SCORE_SOFTMAX_BIAS}[spec.scoring]
     d.norm_topk_prob = int(spec.norm_topk_prob)
     d.routed_scaling_factor = float(spec.routed_scaling_factor)
     d.wfmt = {NVFP4: _lib.MOE_W_NVFP4, MXFP4: _lib.MOE_W_MXFP4, BF16: _lib.MOE_W_BF16,
               FP8: _lib.MOE_W_FP8}[spec.wfmt]
     d.shared_inter = spec.shared_inter
     d.router_fmt = _lib.MOE_R_NVFP4 if spec.router_fmt == NVFP4 else _lib.MOE_R_BF16
+    d.zero_experts = spec.zero_experts
     return d
 
 

@@ -73,6 +73,13 @@ def test_bad_router_format_is_refused(lib):
     assert _lib.moe_workspace_size(d, 1) == 0
 
 
+@pytest.mark.parametrize("E,Z", [(8, -1), (1000, 25)])
+def test_bad_zero_expert_count_is_refused(lib, E, Z):
+    d = _desc(E=E)
+    d.zero_experts = Z
+    assert _lib.moe_workspace_size(d, 1) == 0
+
+
 def _fake_weights(shared=False):
     w = _lib.Weights()
     base = 1 << 20
@@ -128,6 +135,14 @@ def test_argument_refusals_happen_before_any_cuda_call(lib):
     wr = _fake_weights()
     wr.router_s = None
     assert _forward(lib, dr, wr) == _lib.MOE_ERR_INVALID_ARG
+    # softmax + bias needs its bias; zero experts: no grouped path yet
+    dz = _desc(scoring=_lib.MOE_SCORE_SOFTMAX_BIAS)
+    dz.zero_experts = 64
+    assert _forward(lib, dz, _fake_weights()) == _lib.MOE_ERR_INVALID_ARG
+    wz = _fake_weights()
+    wz.bias = 1 << 21
+    assert _forward(lib, dz, wz, N=300) == _lib.MOE_ERR_UNSUPPORTED
+    assert _lib.moe_workspace_size(dz, 4) > _lib.moe_workspace_size(_desc(), 4)
     ds = _desc(scoring=1)                                                 # sigmoid needs a bias
     assert _forward(lib, ds, _fake_weights()) == _lib.MOE_ERR_INVALID_ARG
     dsh = _desc(shared_inter=64)                                          # shared size, no weights

@@ -37,6 +37,9 @@ GROUPED = {
     "nvfp4_many_experts": (dict(H=512, inter=256, E=64, top_k=4), 96),
     # NVFP4-quantised router on the grouped router kernel
     "nvfp4_router": (dict(H=256, inter=128, E=16, top_k=4, router_fmt=NV), 100),
+    # softmax + correction bias routing on the grouped top-k
+    "softmax_bias": (dict(H=256, inter=128, E=16, top_k=4, scoring=synth.SOFTMAX_BIAS,
+                          routed_scaling_factor=1.5), 100),
 }
 
 

@@ -17,7 +17,7 @@ from oracle import compare, margin, oracle
 from .gpu_util import full_layer, run_forward, spec_from
 
 NV, MX, BF, F8 = synth.NVFP4, synth.MXFP4, synth.BF16, synth.FP8
-SM, SB = synth.SOFTMAX, synth.SIGMOID_BIAS
+SM, SB, SMB = synth.SOFTMAX, synth.SIGMOID_BIAS, synth.SOFTMAX_BIAS
 
 SMALL = {
     "tiny": (dict(), 1),
@@ -66,6 +66,15 @@ SMALL = {
                                          router_fmt=NV), 4),
     "nvfp4_router_fp8_experts": (dict(H=512, inter=256, E=24, top_k=4, wfmt=F8,
                                       router_fmt=NV), 3),
+    # softmax + correction bias, with and without zero experts
+    "softmax_bias": (dict(H=256, inter=128, E=16, top_k=4, scoring=SMB,
+                          routed_scaling_factor=1.5), 3),
+    "zero_experts": (dict(H=256, inter=128, E=16, top_k=4, scoring=SMB, zero_experts=8), 5),
+    "zero_experts_gated_shared": (dict(H=320, inter=96, E=32, top_k=6, scoring=SMB,
+                                       zero_experts=16, shared_inter=64, shared_gated=True,
+                                       routed_scaling_factor=2.0), 4),
+    "zero_experts_width_1024": (dict(H=64, inter=32, E=768, top_k=4, scoring=SMB,
+                                     zero_experts=256), 3),
 }
 
 
@@ -112,6 +121,22 @@ def test_zero_down_codes_gives_shared_alone():
 
 
 @pytest.mark.gpu
+def test_zero_experts_take_every_slot():
+    """Zero experts pulled in by their bias for every slot: no routed expert
+    runs, the output is the shared expert alone (and the routing outputs hold
+    the zero-expert indices >= E)."""
+    spec = spec_from("tiny", name="all_zero", H=256, inter=128, E=8, top_k=3, scoring=SMB,
+                     zero_experts=4, shared_inter=64, shared_gated=True)
+    host = synth.make_layer(spec, seed=19)
+    host.bias[8:] = 10.0
+    dev = DeviceLayer.upload(host)
+    x = margin.tokens_with_margin(host, 3, seed=20)
+    _check(host, dev, x)
+    _, idx, _ = run_forward(dev, x)
+    assert np.all(idx >= 8)
+
+
+@pytest.mark.gpu
 def test_scale2_is_applied():
     spec = spec_from("tiny", name="scale2", H=256, inter=128, E=8, top_k=2)
     host = synth.make_layer(spec, seed=15)
@@ -125,7 +150,8 @@ def test_scale2_is_applied():
 
 
 FULL = [(name, N) for name in ("tiny", "qwen3_30b_a3b", "mtp_verify", "deepseek_v3", "gpt_oss_120b",
-                               "qwen3_30b_a3b_bf16", "qwen3_30b_a3b_fp8", "qwen3_30b_a3b_nvfp4_router")
+                               "qwen3_30b_a3b_bf16", "qwen3_30b_a3b_fp8", "qwen3_30b_a3b_nvfp4_router",
+                               "qwen3_30b_a3b_zero_experts")
         for N in synth.CONFIGS[name].tokens if N <= 64]
 
 
