@@ -57,6 +57,7 @@ class LayerSpec:
     pool: int               # distinct experts drawn per projection
     router_fmt: str = BF16  # BF16 router, or NVFP4 (E2M1 + per-16 E4M3 + scale2)
     zero_experts: int = 0   # Z extra router outputs whose expert adds nothing
+    hash_vocab: int = 0     # V > 0: hash routing, experts from a [V, top_k] token-id table
 
     @property
     def gs(self) -> int:
@@ -271,12 +272,13 @@ class HostLayer:
     sh_gate_w: Optional[np.ndarray]  # uint16 [H] or None
     router_s: Optional[np.ndarray] = None   # NVFP4 router: uint8 E4M3 [E, H/16] (router: uint8 [E, H/2])
     router_s2: Optional[np.ndarray] = None  # NVFP4 router: float32 [1]
+    tid2eid: Optional[np.ndarray] = None    # hash routing: int32 [V, top_k]
 
     def tensors(self):
         return {k: getattr(self, k) for k in (
             "router", "bias", "gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s",
             "gate_s2", "up_s2", "down_s2", "sh_gate", "sh_up", "sh_down", "sh_gate_w",
-            "router_s", "router_s2")}
+            "router_s", "router_s2", "tid2eid")}
 
 
 def _quantize(spec: LayerSpec, w: np.ndarray):
@@ -346,9 +348,13 @@ def make_layer(spec: LayerSpec, seed: Optional[int] = None, pool: Optional[int] 
         if spec.shared_gated:
             sh_gate_w = f32_to_bf16_bits(rng.standard_normal(H, dtype=np.float32)
                                          * np.float32(1.0 / np.sqrt(H)))
+    tid2eid = None
+    if spec.hash_vocab > 0:   # k distinct experts per token id, uniformly drawn
+        tid2eid = np.stack([rng.permutation(E)[:spec.top_k]
+                            for _ in range(spec.hash_vocab)]).astype(np.int32)
     return HostLayer(spec, router, bias, gate_q, up_q, down_q, gate_s, up_s, down_s,
                      s2, None if s2 is None else s2.copy(), None if s2 is None else s2.copy(),
-                     sh_gate, sh_up, sh_down, sh_gate_w, router_s, router_s2)
+                     sh_gate, sh_up, sh_down, sh_gate_w, router_s, router_s2, tid2eid)
 
 
 def x_row(spec: LayerSpec, seed: int, row: int, attempt: int = 0) -> np.ndarray:

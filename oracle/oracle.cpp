@@ -34,6 +34,12 @@
 //     with softmax scores plus a correction bias for selection; a selected
 //     zero expert runs no expert.  The pages do not say what a zero expert
 //     adds; the reading taken is nothing (its output is zero);
+//   * forward_batched.rs, hash routing (moe_hash_route with the gate logits,
+//     tid2eid, the token's id, num_experts, top_k, norm_topk_prob and
+//     routed_scaling_factor) — the k experts of a token are row token_id of
+//     the tid2eid table; the weights come from the gate logits with the
+//     layer's scoring (the pages do not spell the rule out; the reading taken
+//     is the top-k rule applied to the table's experts);
 //   * forward_atomic_c4.rs, doc comment — routed outputs accumulated as
 //     routing-weighted sums, then cast to BF16 and blended with the shared
 //     expert;
@@ -255,6 +261,29 @@ void oracle_route_one(const double* l, const float* bias, int E, int k, int scor
         for (int e = 0; e < E; ++e) sel_score[e] = score[e];
 }
 
+// Hash routing of one token: the selected experts are the table row `row`
+// (k expert ids, in that order); their weights follow the scoring as in
+// oracle_route_one (softmax over all E for scorings 0 and 2, sigmoid for 1;
+// divided by their sum if norm != 0; times rsf unless scoring 0).  The bias
+// does not enter (it only ever selects).
+void oracle_route_hash_one(const double* l, const int32_t* row, int E, int k, int scoring,
+                           int norm, double rsf, int32_t* idx, double* w) {
+    double mx = l[0], den = 0.0;
+    for (int e = 1; e < E; ++e) mx = std::max(mx, l[e]);
+    for (int e = 0; e < E; ++e) den += std::exp(l[e] - mx);
+    double sum = 0.0;
+    for (int j = 0; j < k; ++j) {
+        const int e = row[j];
+        idx[j] = e;
+        w[j] = (scoring == 1) ? 1.0 / (1.0 + std::exp(-l[e])) : std::exp(l[e] - mx) / den;
+        sum += w[j];
+    }
+    if (norm)
+        for (int j = 0; j < k; ++j) w[j] /= sum;
+    if (scoring != 0)
+        for (int j = 0; j < k; ++j) w[j] *= rsf;
+}
+
 void oracle_route(const double* logits, const float* bias, int N, int E, int k, int scoring,
                   int norm, double rsf, int32_t* idx, double* w, double* sel_score) {
     for (int n = 0; n < N; ++n)
@@ -341,6 +370,7 @@ struct oracle_weights {
     const uint16_t* sh_gate_w;
     const uint8_t* router_s;     // NVFP4 router: E4M3 scales [E, H/16]
     const float* router_s2;      // NVFP4 router: scale2 (one float) or null = 1.0
+    const int32_t* tid2eid;      // hash routing: [V, k] expert ids per token id, or null
 };
 
 // out_f64 [N, H] = sum_j w[n,j] * expert_{idx[n,j]}(x_n) + g_s(x_n) * shared(x_n)
@@ -355,7 +385,7 @@ struct oracle_weights {
 int oracle_moe_forward(int H, int inter, int E, int k, int scoring, int norm, double rsf,
                        int fmt, int Is, const oracle_weights* W, const uint16_t* x, int N,
                        double* out_f64, uint16_t* out_bf16, int32_t* idx, double* w,
-                       double* logits_out, int router_fmt, int Z) {
+                       double* logits_out, int router_fmt, int Z, const int32_t* token_ids) {
     if (H <= 0 || inter <= 0 || E <= 0 || Z < 0 || k <= 0 || k > E + Z || N < 0) return 1;
     if (scoring < 0 || scoring > 2) return 1;
     const int R = E + Z;   // router width
@@ -369,7 +399,14 @@ int oracle_moe_forward(int H, int inter, int E, int k, int scoring, int norm, do
                                  W->router_s2 ? (double)W->router_s2[0] : 1.0, 1, N, R, H,
                                  logits.data());
     if (logits_out) std::copy(logits.begin(), logits.end(), logits_out);
-    oracle_route(logits.data(), W->bias, N, R, k, scoring, norm, rsf, idx, w, nullptr);
+    if (W->tid2eid) {   // hash routing: token n takes table row token_ids[n]
+        if (!token_ids || Z != 0) return 1;
+        for (int n = 0; n < N; ++n)
+            oracle_route_hash_one(logits.data() + (long)n * R, W->tid2eid + (long)token_ids[n] * k,
+                                  R, k, scoring, norm, rsf, idx + (long)n * k, w + (long)n * k);
+    } else {
+        oracle_route(logits.data(), W->bias, N, R, k, scoring, norm, rsf, idx, w, nullptr);
+    }
 
     // bytes per expert of each table (BF16: two bytes per element, no scales;
     // FP8: one byte per element, 4-byte scales per 128 x 128 block)

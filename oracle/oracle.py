@@ -39,7 +39,7 @@ class _Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "router", "bias", "gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s",
         "gate_s2", "up_s2", "down_s2", "sh_gate", "sh_up", "sh_down", "sh_gate_w",
-        "router_s", "router_s2")]
+        "router_s", "router_s2", "tid2eid")]
 
 
 def lib():
@@ -77,7 +77,7 @@ def lib():
             L.oracle_moe_forward.restype = i32
             L.oracle_moe_forward.argtypes = [i32, i32, i32, i32, i32, i32, d, i32, i32,
                                              ctypes.POINTER(_Weights), vp, i32,
-                                             vp, vp, vp, vp, vp, i32, i32]
+                                             vp, vp, vp, vp, vp, i32, i32, vp]
             L.oracle_num_threads.restype = i32
             L.oracle_num_threads.argtypes = []
             _lib = L
@@ -211,7 +211,7 @@ def _weights_struct(layer) -> _Weights:
     return W
 
 
-def moe_forward(layer, x: np.ndarray):
+def moe_forward(layer, x: np.ndarray, token_ids: Optional[np.ndarray] = None):
     """Full layer forward.  Returns dict with out_f64 [N,H], out_bf16 [N,H]
     (uint16 bits), idx [N,k] int32, w [N,k] float64, logits [N,E]."""
     sp = layer.spec
@@ -223,11 +223,12 @@ def moe_forward(layer, x: np.ndarray):
     w = np.empty((N, sp.top_k), dtype=np.float64)
     logits = np.empty((N, sp.E + sp.zero_experts), dtype=np.float64)
     W = _weights_struct(layer)
+    tid = None if token_ids is None else np.ascontiguousarray(token_ids, dtype=np.int32)
     rc = lib().oracle_moe_forward(
         sp.H, sp.inter, sp.E, sp.top_k, scoring_code(sp.scoring),
         int(sp.norm_topk_prob), float(sp.routed_scaling_factor), fmt_code(sp.wfmt),
         sp.shared_inter, ctypes.byref(W), _p(x), N, _p(out), _p(outb), _p(idx), _p(w),
-        _p(logits), 1 if sp.router_fmt == "nvfp4" else 0, sp.zero_experts)
+        _p(logits), 1 if sp.router_fmt == "nvfp4" else 0, sp.zero_experts, _p(tid))
     if rc != 0:
         raise ValueError(f"oracle_moe_forward rejected its arguments (code {rc})")
     return {"out_f64": out, "out_bf16": outb, "idx": idx, "w": w, "logits": logits}

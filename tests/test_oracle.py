@@ -569,6 +569,52 @@ def test_zero_experts_add_nothing(oracle_mod):
         np.testing.assert_allclose(rc["out_f64"][n], ref, rtol=1e-11, atol=1e-14)
 
 
+@pytest.mark.parametrize("scoring", [synth.SOFTMAX, synth.SIGMOID_BIAS, synth.SOFTMAX_BIAS])
+def test_hash_routing_with_the_topk_table_equals_topk_routing(oracle_mod, scoring):
+    """Hash routing (experts from the tid2eid row of the token's id, weights by
+    the layer's scoring): a table whose rows are the tokens' own top-k
+    selections reproduces the top-k layer exactly, token ids permuted."""
+    import dataclasses
+    sp = _small_spec(E=12, top_k=3, H=96, inter=64, scoring=scoring, routed_scaling_factor=1.5)
+    L = synth.make_layer(sp, seed=61)
+    x = synth.make_tokens(sp, 5, seed=62)
+    r = oracle_mod.moe_forward(L, x)
+    perm = np.array([3, 0, 4, 1, 2], dtype=np.int32)            # token n has id perm[n]
+    table = np.zeros((7, 3), dtype=np.int32)
+    table[perm] = r["idx"]
+    Lh = dataclasses.replace(L, spec=dataclasses.replace(sp, hash_vocab=7), tid2eid=table)
+    rh = oracle_mod.moe_forward(Lh, x, token_ids=perm)
+    np.testing.assert_array_equal(rh["idx"], r["idx"])
+    np.testing.assert_allclose(rh["w"], r["w"], rtol=1e-15)
+    np.testing.assert_array_equal(rh["out_f64"], r["out_f64"])
+
+
+def test_hash_routing_weights(oracle_mod):
+    """Weights of arbitrary table rows: the scoring's scores of those experts
+    (softmax over all experts, or sigmoid), renormalised, times the scaling
+    factor (not for plain softmax); the order is the table's."""
+    import dataclasses
+    for scoring, norm in ((synth.SOFTMAX, True), (synth.SOFTMAX, False),
+                          (synth.SIGMOID_BIAS, True), (synth.SOFTMAX_BIAS, False)):
+        sp = _small_spec(E=10, top_k=4, H=64, inter=32, scoring=scoring, norm_topk_prob=norm,
+                         routed_scaling_factor=2.5, hash_vocab=6)
+        L = synth.make_layer(sp, seed=63)
+        assert L.tid2eid.shape == (6, 4)
+        assert all(len(set(r)) == 4 and max(r) < 10 for r in L.tid2eid.tolist())
+        x = synth.make_tokens(sp, 3, seed=64)
+        ids = np.array([5, 0, 5], dtype=np.int32)
+        rh = oracle_mod.moe_forward(L, x, token_ids=ids)
+        for n in range(3):
+            row = L.tid2eid[ids[n]]
+            assert list(rh["idx"][n]) == list(row)
+            l = rh["logits"][n]
+            s = scipy.special.expit(l) if scoring == synth.SIGMOID_BIAS else scipy.special.softmax(l)
+            ref = s[row] / (s[row].sum() if norm else 1.0)
+            if scoring != synth.SOFTMAX:
+                ref = ref * 2.5
+            np.testing.assert_allclose(rh["w"][n], ref, rtol=1e-13)
+
+
 def test_scale2_scales_each_projection(oracle_mod):
     sp = _small_spec(E=1, top_k=1)
     L = synth.make_layer(sp, seed=13)

@@ -48,6 +48,9 @@ MUTANTS = {
     "softmax_bias_no_rsf": ("if (scoring != 0)\n        for (int j = 0; j < k; ++j) w[j] *= rsf;",
                             "if (scoring == 1)\n        for (int j = 0; j < k; ++j) w[j] *= rsf;"),
     "zero_expert_runs_expert_0": ("if (e >= E) continue;", "if (e >= E) { }"),
+    "hash_row_by_position": ("W->tid2eid + (long)token_ids[n] * k", "W->tid2eid + (long)n * k"),
+    "hash_sigmoid_as_softmax": ("w[j] = (scoring == 1) ? 1.0 / (1.0 + std::exp(-l[e])) : std::exp(l[e] - mx) / den;",
+                                "w[j] = std::exp(l[e] - mx) / den;"),
     "fp8_row_block_ignored": ("s + 4 * ((r / 128) * kb + k / 128)", "s + 4 * (k / 128)"),
     "fp8_scale_ignored": ("return oracle_e4m3(q[r * (long)K + k]) * (double)sc;",
                           "return oracle_e4m3(q[r * (long)K + k]) * (sc > 0 ? 1.0 : 0.0);"),
