@@ -11,7 +11,9 @@
  *                      routed scaling factor; or softmax + correction bias
  *                      (the zero-expert routers) likewise; with Z zero
  *                      experts the router has E + Z outputs and a selected
- *                      zero expert runs no expert;
+ *                      zero expert runs no expert; or hash routing: the k
+ *                      experts of a token are the tid2eid row of its token
+ *                      id, weighted by the scoring of their logits;
  *   3. routed experts  SwiGLU with block-scaled FP4 weights:
  *                      h = SiLU(Dq(Wg) x) * (Dq(Wu) x),  y = Dq(Wd) h,
  *                      Dq(w) = E2M1(code) * blockscale * scale2;
@@ -131,6 +133,9 @@ typedef struct {
   int32_t router_fmt;            /* moe_rfmt_t (0 = BF16 router) */
   int32_t zero_experts;          /* Z >= 0: router width E + Z (the pages' num_experts +
                                     zero_expert_num); E + Z <= 1024 */
+  int32_t hash_vocab;            /* V > 0: hash routing with a [V, top_k] tid2eid table
+                                    (forward_batched.rs, moe_hash_route); calls go
+                                    through moe_forward_ids; needs zero_experts == 0 */
 } moe_layer_desc_t;
 
 typedef struct {
@@ -151,6 +156,8 @@ typedef struct {
   const void* sh_gate_w;         /* bf16 [H] or NULL (ungated) */
   const uint8_t* router_s;       /* NVFP4 router: E4M3 scales [E, H/16]; else NULL */
   const float* router_s2;        /* NVFP4 router: one f32 scale2, NULL = 1.0 */
+  const int32_t* tid2eid;        /* hash routing: int32 [V, top_k] expert ids per token id
+                                    (in [0, E)), else NULL */
 } moe_weights_t;
 
 /* Bytes of device workspace moe_forward needs for any 1 <= N <= max_tokens.
@@ -189,6 +196,18 @@ MOE_API moe_status_t moe_forward(const moe_layer_desc_t* desc, const moe_weights
                          const void* x, int32_t N, void* out,
                          int32_t* topk_idx, float* topk_w,
                          void* workspace, size_t ws_bytes, void* stream);
+
+/* moe_forward for a hash-routed layer (desc->hash_vocab > 0): token_ids is
+ * int32 [N] device, the token ids of the rows of x (each clamped into
+ * [0, hash_vocab)); token n's experts are tid2eid row token_ids[n] in table
+ * order (ids outside [0, E) are clamped), weighted as top-k routing weights
+ * are for the layer's scoring.  A hash-routed layer refuses moe_forward,
+ * moe_route and the other entry points (MOE_ERR_INVALID_ARG: no token ids),
+ * and N*top_k > 256 (MOE_ERR_UNSUPPORTED).  Otherwise as moe_forward. */
+MOE_API moe_status_t moe_forward_ids(const moe_layer_desc_t* desc, const moe_weights_t* weights,
+                                     const void* x, const int32_t* token_ids, int32_t N,
+                                     void* out, int32_t* topk_idx, float* topk_w,
+                                     void* workspace, size_t ws_bytes, void* stream);
 
 /* Router logits and top-k routing only (steps 1-2): writes topk_idx/topk_w
  * (both required).  Same constraints and ownership as moe_forward. */

@@ -33,7 +33,8 @@ MOE_R_NVFP4 = 1
 
 EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_forward", "moe_route",
             "moe_host_staging_size", "moe_forward_host", "moe_get_error", "moe_status_string",
-            "moe_abi_version", "moe_debug_set_wait_budget_ns", "moe_forward_noalloc")
+            "moe_abi_version", "moe_debug_set_wait_budget_ns", "moe_forward_noalloc",
+            "moe_forward_ids")
 
 
 class MoeError(RuntimeError):
@@ -47,14 +48,15 @@ class LayerDesc(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("scoring", ctypes.c_int32),
                 ("norm_topk_prob", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
                 ("wfmt", ctypes.c_int32), ("shared_inter", ctypes.c_int32),
-                ("router_fmt", ctypes.c_int32), ("zero_experts", ctypes.c_int32)]
+                ("router_fmt", ctypes.c_int32), ("zero_experts", ctypes.c_int32),
+                ("hash_vocab", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "router", "bias", "gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s",
         "gate_s2", "up_s2", "down_s2", "sh_gate", "sh_up", "sh_down", "sh_gate_w",
-        "router_s", "router_s2")]
+        "router_s", "router_s2", "tid2eid")]
 
 
 _lock = threading.Lock()
@@ -92,6 +94,8 @@ def load() -> ctypes.CDLL:
         L.moe_abi_version.argtypes = []
         L.moe_forward_noalloc.restype = i32
         L.moe_forward_noalloc.argtypes = [pd, pw, vp, i32, vp, vp, vp, vp]
+        L.moe_forward_ids.restype = i32
+        L.moe_forward_ids.argtypes = [pd, pw, vp, vp, i32, vp, vp, vp, vp, sz, vp]
         L.moe_debug_set_wait_budget_ns.restype = None
         L.moe_debug_set_wait_budget_ns.argtypes = [ctypes.c_ulonglong]
         if L.moe_abi_version() != ABI_VERSION:
@@ -147,6 +151,18 @@ def moe_forward(desc: LayerDesc, weights: Weights, x, out, ws, topk_idx=None, to
                             ws.numel() * ws.element_size(), _stream(stream))
     if check:
         _check(st, "moe_forward")
+    return st
+
+
+def moe_forward_ids(desc: LayerDesc, weights: Weights, x, token_ids, out, ws, topk_idx=None,
+                    topk_w=None, stream=None, check: bool = True) -> int:
+    """moe_forward of a hash-routed layer; token_ids an int32 device tensor [N]."""
+    st = load().moe_forward_ids(ctypes.byref(desc), ctypes.byref(weights), _ptr(x),
+                                _ptr(token_ids), int(x.shape[0]), _ptr(out), _ptr(topk_idx),
+                                _ptr(topk_w), _ptr(ws), ws.numel() * ws.element_size(),
+                                _stream(stream))
+    if check:
+        _check(st, "moe_forward_ids")
     return st
 
 

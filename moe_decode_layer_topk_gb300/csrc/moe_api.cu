@@ -108,6 +108,8 @@ moe_status_t check_desc(const moe_layer_desc_t* d) {
       d->scoring != MOE_SCORE_SOFTMAX_BIAS)
     return MOE_ERR_INVALID_ARG;
   if (d->zero_experts < 0) return MOE_ERR_INVALID_ARG;
+  if (d->hash_vocab < 0) return MOE_ERR_INVALID_ARG;
+  if (d->hash_vocab > 0 && d->zero_experts > 0) return MOE_ERR_UNSUPPORTED;
   if (d->wfmt != MOE_W_NVFP4 && d->wfmt != MOE_W_MXFP4 && d->wfmt != MOE_W_BF16 &&
       d->wfmt != MOE_W_FP8)
     return MOE_ERR_INVALID_ARG;
@@ -133,6 +135,7 @@ moe_status_t check_weights(const moe_layer_desc_t* d, const moe_weights_t* w) {
   if (d->scoring != MOE_SCORE_SOFTMAX && !w->bias) return MOE_ERR_INVALID_ARG;
   if (d->router_fmt == MOE_R_NVFP4 && (!w->router_s || !aligned16(w->router_s)))
     return MOE_ERR_INVALID_ARG;
+  if (d->hash_vocab > 0 && !w->tid2eid) return MOE_ERR_INVALID_ARG;
   if (d->shared_inter > 0) {
     const void* sh[] = {w->sh_gate, w->sh_up, w->sh_down};
     for (const void* p : sh)
@@ -305,6 +308,7 @@ moe_status_t run_grouped(const moe_layer_desc_t* d, const moe_weights_t* w, cons
   if (d->wfmt == MOE_W_BF16 || d->wfmt == MOE_W_FP8)
     return MOE_ERR_UNSUPPORTED;   // BF16 / FP8 experts: decode sizes only
   if (d->zero_experts > 0) return MOE_ERR_UNSUPPORTED;   // zero experts: decode sizes only
+  if (d->hash_vocab > 0) return MOE_ERR_UNSUPPORTED;     // hash routing: decode sizes only
   const GWsLayout L = gws_layout(*d, N);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   int budget = 0, grid = 0;
@@ -404,11 +408,13 @@ moe_status_t run_grouped(const moe_layer_desc_t* d, const moe_weights_t* w, cons
 
 moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* x, int32_t N,
                  void* out, int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
-                 void* stream, int route_only) {
+                 void* stream, int route_only, const int32_t* token_ids = nullptr) {
   moe_status_t st = check_desc(d);
   if (st != MOE_OK) return st;
   st = check_weights(d, w);
   if (st != MOE_OK) return st;
+  // hash routing needs the call's token ids, and only hash routing takes them
+  if ((d->hash_vocab > 0) != (token_ids != nullptr)) return MOE_ERR_INVALID_ARG;
   if (N < 1) return MOE_ERR_INVALID_ARG;
   if (!x || !aligned16(x) || !ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
   if (!route_only && (!out || !aligned16(out))) return MOE_ERR_INVALID_ARG;
@@ -441,6 +447,9 @@ moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* 
   p.router_s2 = d->router_fmt == MOE_R_NVFP4 ? w->router_s2 : nullptr;
   p.bias = d->scoring != MOE_SCORE_SOFTMAX ? w->bias : nullptr;
   p.Z = d->zero_experts;
+  p.hash_V = d->hash_vocab;
+  p.tid2eid = d->hash_vocab > 0 ? w->tid2eid : nullptr;
+  p.token_ids = token_ids;
   // BF16 experts read no scales; FP8 experts their f32 block scales; only
   // the FP4 formats have scale2
   const bool scales = d->wfmt != MOE_W_BF16;
@@ -542,6 +551,15 @@ moe_status_t moe_forward(const moe_layer_desc_t* desc, const moe_weights_t* weig
                          int32_t N, void* out, int32_t* topk_idx, float* topk_w, void* workspace,
                          size_t ws_bytes, void* stream) {
   return run(desc, weights, x, N, out, topk_idx, topk_w, workspace, ws_bytes, stream, 0);
+}
+
+moe_status_t moe_forward_ids(const moe_layer_desc_t* desc, const moe_weights_t* weights,
+                             const void* x, const int32_t* token_ids, int32_t N, void* out,
+                             int32_t* topk_idx, float* topk_w, void* workspace, size_t ws_bytes,
+                             void* stream) {
+  if (!token_ids) return MOE_ERR_INVALID_ARG;
+  return run(desc, weights, x, N, out, topk_idx, topk_w, workspace, ws_bytes, stream, 0,
+             token_ids);
 }
 
 moe_status_t moe_route(const moe_layer_desc_t* desc, const moe_weights_t* weights, const void* x,

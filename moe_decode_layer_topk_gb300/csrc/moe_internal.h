@@ -86,6 +86,9 @@ struct Params {
   // layer
   int H, inter, E, k, scoring, norm;
   int Z;     // zero experts: router width E + Z, selected zero experts run nothing
+  int hash_V;                 // > 0: hash routing with a [hash_V, k] tid2eid table
+  const int32_t* tid2eid;     // hash routing: expert ids per token id
+  const int32_t* token_ids;   // hash routing: [N] token ids of this call
   float rsf;
   int fmt;   // FMT_NVFP4 / FMT_MXFP4 / FMT_BF16 / FMT_FP8 for the routed experts
   int Is;    // shared expert intermediate size (0 = none)

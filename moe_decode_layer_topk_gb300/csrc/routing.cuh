@@ -126,4 +126,45 @@ __device__ __forceinline__ void topk_warp(int E, int k, int scoring, int norm, f
   }
 }
 
+// Hash routing of one token: the k experts are `row` (the token id's row of
+// the tid2eid table, in table order; ids clamped into [0, E)); their weights
+// follow the scoring as in topk_warp (softmax over all E for scorings 0 and 2,
+// sigmoid for 1; renormalised if asked; times rsf unless plain softmax).
+// Lane j < k returns slot j in *e_out / *w_out.
+template <int PER>
+__device__ __forceinline__ void hash_warp(int E, int k, int scoring, int norm, float rsf,
+                                          const int32_t* row, const float (&lg)[PER], int lane,
+                                          int* e_out, float* w_out) {
+  float mx = -INFINITY, den = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    if (lane + 32 * i < E) mx = fmaxf(mx, lg[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    if (lane + 32 * i < E) den += expf(lg[i] - mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  int e = 0;
+  if (lane < k) e = min(max(__ldg(row + lane), 0), E - 1);
+  float l = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const float v = __shfl_sync(0xffffffffu, lg[i], e & 31);
+    if ((e >> 5) == i) l = v;
+  }
+  float w = 0.f;
+  if (lane < k) w = (scoring == 1) ? 1.0f / (1.0f + expf(-l)) : expf(l - mx) / den;
+  float wsum = w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+  if (lane < k) {
+    if (norm) w = w / wsum;
+    if (scoring != 0) w *= rsf;
+    *e_out = e;
+    *w_out = w;
+  }
+}
+
 }  // namespace moe

@@ -27,6 +27,7 @@ def layer_desc(spec: LayerSpec) -> _lib.LayerDesc:
     d.shared_inter = spec.shared_inter
     d.router_fmt = _lib.MOE_R_NVFP4 if spec.router_fmt == NVFP4 else _lib.MOE_R_BF16
     d.zero_experts = spec.zero_experts
+    d.hash_vocab = spec.hash_vocab
     return d
 
 

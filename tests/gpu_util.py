@@ -24,7 +24,7 @@ def full_layer(name: str):
     return host, DeviceLayer.upload(host)
 
 
-def run_forward(dev: DeviceLayer, x_bits: np.ndarray, ws=None):
+def run_forward(dev: DeviceLayer, x_bits: np.ndarray, ws=None, token_ids=None):
     spec = dev.spec
     N = x_bits.shape[0]
     x = bf16_tensor(x_bits)
@@ -32,7 +32,11 @@ def run_forward(dev: DeviceLayer, x_bits: np.ndarray, ws=None):
     idx = torch.full((N, spec.top_k), -1, dtype=torch.int32, device="cuda")
     w = torch.full((N, spec.top_k), float("nan"), dtype=torch.float32, device="cuda")
     ws = workspace(spec, N) if ws is None else ws
-    _lib.moe_forward(dev.desc, dev.weights, x, out, ws, idx, w)
+    if token_ids is None:
+        _lib.moe_forward(dev.desc, dev.weights, x, out, ws, idx, w)
+    else:
+        tid = torch.from_numpy(np.ascontiguousarray(token_ids, dtype=np.int32)).cuda()
+        _lib.moe_forward_ids(dev.desc, dev.weights, x, tid, out, ws, idx, w)
     torch.cuda.synchronize()
     assert _lib.moe_get_error(ws) == _lib.MOE_OK
     return (out.view(torch.int16).cpu().numpy().view(np.uint16), idx.cpu().numpy(),

@@ -143,6 +143,23 @@ def test_argument_refusals_happen_before_any_cuda_call(lib):
     wz.bias = 1 << 21
     assert _forward(lib, dz, wz, N=300) == _lib.MOE_ERR_UNSUPPORTED
     assert _lib.moe_workspace_size(dz, 4) > _lib.moe_workspace_size(_desc(), 4)
+    # hash routing: token ids required (and only for hash routing), the table
+    # required, no grouped path, no zero experts with it
+    dh = _desc()
+    dh.hash_vocab = 100
+    assert _forward(lib, dh, _fake_weights()) == _lib.MOE_ERR_INVALID_ARG
+    ids = 1 << 22
+    assert lib.moe_forward_ids(ctypes.byref(dh), ctypes.byref(_fake_weights()), 1 << 24, ids,
+                               300, 1 << 25, None, None, 1 << 26, 1 << 30,
+                               None) == _lib.MOE_ERR_UNSUPPORTED
+    wt = _fake_weights()
+    wt.tid2eid = None
+    assert lib.moe_forward_ids(ctypes.byref(dh), ctypes.byref(wt), 1 << 24, ids, 1, 1 << 25,
+                               None, None, 1 << 26, 1 << 30, None) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_forward_ids(ctypes.byref(d), ctypes.byref(w), 1 << 24, ids, 1, 1 << 25,
+                               None, None, 1 << 26, 1 << 30, None) == _lib.MOE_ERR_INVALID_ARG
+    dh.zero_experts = 4
+    assert _lib.moe_workspace_size(dh, 1) == 0
     ds = _desc(scoring=1)                                                 # sigmoid needs a bias
     assert _forward(lib, ds, _fake_weights()) == _lib.MOE_ERR_INVALID_ARG
     dsh = _desc(shared_inter=64)                                          # shared size, no weights

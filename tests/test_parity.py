@@ -136,6 +136,34 @@ def test_zero_experts_take_every_slot():
     assert np.all(idx >= 8)
 
 
+HASHED = {
+    "hash_softmax": (dict(H=256, inter=128, E=16, top_k=4, hash_vocab=50), 5),
+    "hash_sigmoid_shared": (dict(H=320, inter=96, E=32, top_k=3, scoring=SB,
+                                 routed_scaling_factor=2.5, shared_inter=64, hash_vocab=1000), 4),
+    "hash_softmax_no_norm_fp8": (dict(H=512, inter=256, E=24, top_k=2, wfmt=F8,
+                                      norm_topk_prob=False, hash_vocab=7), 6),
+}
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", sorted(HASHED))
+def test_hash_routing(case):
+    """Hash routing through moe_forward_ids: experts from the tid2eid row of
+    each token id (repeated ids included), weights by the layer's scoring."""
+    kw, N = HASHED[case]
+    spec = spec_from("tiny", name=case, **kw)
+    host = synth.make_layer(spec, seed=7300 + len(case))
+    dev = DeviceLayer.upload(host)
+    x = synth.make_tokens(spec, N, seed=7400 + len(case))
+    ids = np.random.default_rng(7500 + len(case)).integers(0, spec.hash_vocab, N).astype(np.int32)
+    ids[-1] = ids[0]
+    ref = oracle.moe_forward(host, x, token_ids=ids)
+    out, idx, w = run_forward(dev, x, token_ids=ids)
+    np.testing.assert_array_equal(idx, ref["idx"])          # table order, bit for bit
+    np.testing.assert_allclose(w, ref["w"], rtol=1e-4, atol=1e-6)
+    compare.check_output(out, ref["out_f64"])
+
+
 @pytest.mark.gpu
 def test_scale2_is_applied():
     spec = spec_from("tiny", name="scale2", H=256, inter=128, E=8, top_k=2)
