@@ -64,7 +64,9 @@ __device__ __forceinline__ void topk_warp(int E, int k, int scoring, int norm, f
   for (int i = 0; i < PER; ++i)
     if (lane + 32 * i < E) mx = fmaxf(mx, lg[i]);
   float den = 0.f;
-  if (scoring != 1) {   // softmax denominator over all E (weights; keys of scoring 2)
+  // softmax max and denominator over all E: before the selection when the
+  // keys need them (scoring 2), after it when only the weights do (scoring 0)
+  auto softmax_den = [&]() {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
 #pragma unroll
@@ -72,7 +74,8 @@ __device__ __forceinline__ void topk_warp(int E, int k, int scoring, int norm, f
       if (lane + 32 * i < E) den += expf(lg[i] - mx);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-  }
+  };
+  if (scoring == 2) softmax_den();
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int e = lane + 32 * i;
@@ -106,6 +109,7 @@ __device__ __forceinline__ void topk_warp(int E, int k, int scoring, int norm, f
         if (key[i] > bk) { bk = key[i]; be = lane + 32 * i; }
     }
   }
+  if (scoring == 0) softmax_den();
   // logit of this lane's selection, from the lane that holds it
   float l = 0.f;
 #pragma unroll
