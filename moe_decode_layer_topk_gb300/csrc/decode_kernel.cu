@@ -273,7 +273,7 @@ __device__ __noinline__ void token_prep(const Params& p, int cta, int G, Tables&
 template <int PER>
 __device__ __forceinline__ void topk_token(int E, int k, int scoring, int norm, float rsf,
                                            const float* bias, const float* lrow, int n,
-                                           const int32_t* hash_row, Tables& tb, int lane) {
+                                           Tables& tb, int lane) {
   float lg[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
@@ -282,8 +282,28 @@ __device__ __forceinline__ void topk_token(int E, int k, int scoring, int norm, 
   }
   int se = 0;
   float sw = 0.f;
-  if (hash_row) hash_warp<PER>(E, k, scoring, norm, rsf, hash_row, lg, lane, &se, &sw);
-  else topk_warp<PER>(E, k, scoring, norm, rsf, bias, lg, lane, &se, &sw);
+  topk_warp<PER>(E, k, scoring, norm, rsf, bias, lg, lane, &se, &sw);
+  if (lane < k) {
+    tb.sel_e[n * k + lane] = (int16_t)se;
+    tb.sel_w[n * k + lane] = sw;
+  }
+}
+
+// Hash routing of token n (experts from its tid2eid row), out of line so the
+// top-k path's code stays compact.
+template <int PER>
+__device__ __noinline__ void hash_token(int E, int k, int scoring, int norm, float rsf,
+                                        const float* lrow, int n, const int32_t* hash_row,
+                                        Tables& tb, int lane) {
+  float lg[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = lane + 32 * i;
+    lg[i] = (e < E) ? ld_cg_f32(lrow + e) : -INFINITY;
+  }
+  int se = 0;
+  float sw = 0.f;
+  hash_warp<PER>(E, k, scoring, norm, rsf, hash_row, lg, lane, &se, &sw);
   if (lane < k) {
     tb.sel_e[n * k + lane] = (int16_t)se;
     tb.sel_w[n * k + lane] = sw;
@@ -431,14 +451,20 @@ __device__ __noinline__ void routing_phase(const Params& p, int write_out, Table
   const float* bias = p.bias;
   for (int n = warp; n < p.N; n += kConsumerWarps) {
     const float* lrow = p.logits + (size_t)n * R;
-    // hash routing: the token id's row of tid2eid (ids clamped into the table)
-    const int32_t* hrow = nullptr;
-    if (p.hash_V > 0)
-      hrow = p.tid2eid + (size_t)min(max(__ldg(p.token_ids + n), 0), p.hash_V - 1) * k;
-    if (R <= 128) topk_token<4>(R, k, scoring, norm, rsf, bias, lrow, n, hrow, tb, lane);
-    else if (R <= 256) topk_token<8>(R, k, scoring, norm, rsf, bias, lrow, n, hrow, tb, lane);
-    else if (R <= 512) topk_token<16>(R, k, scoring, norm, rsf, bias, lrow, n, hrow, tb, lane);
-    else topk_token<32>(R, k, scoring, norm, rsf, bias, lrow, n, hrow, tb, lane);
+    if (p.hash_V > 0) {
+      // hash routing: the token id's row of tid2eid (ids clamped into the table)
+      const int32_t* hrow =
+          p.tid2eid + (size_t)min(max(__ldg(p.token_ids + n), 0), p.hash_V - 1) * k;
+      if (R <= 128) hash_token<4>(R, k, scoring, norm, rsf, lrow, n, hrow, tb, lane);
+      else if (R <= 256) hash_token<8>(R, k, scoring, norm, rsf, lrow, n, hrow, tb, lane);
+      else if (R <= 512) hash_token<16>(R, k, scoring, norm, rsf, lrow, n, hrow, tb, lane);
+      else hash_token<32>(R, k, scoring, norm, rsf, lrow, n, hrow, tb, lane);
+      continue;
+    }
+    if (R <= 128) topk_token<4>(R, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
+    else if (R <= 256) topk_token<8>(R, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
+    else if (R <= 512) topk_token<16>(R, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
+    else topk_token<32>(R, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
   }
   if (!p.route_only && warp == kConsumerWarps - 1)
     for (int n = lane; n < p.N; n += 32) tb.xe[n] = (int16_t)ld_cg_s32(p.xexp + n);
