@@ -182,10 +182,12 @@ __device__ bool grid_wait(Ctrl* c, unsigned long long target, uint64_t budget_ns
 
 // ---------------------------------------------------------------- router
 // logits[n, e] = sum_h x[n, h] * Wr[e, h], FP32 accumulation of BF16 products.
+// EXT = false: a BF16 router of width E only (the common layers).
+template <bool EXT>
 __device__ __noinline__ void router_phase(const Params& p, int cta, int G, Tables& tb, int ctid) {
   const int H = p.H;
-  const float rs2 = (p.router_fmt == 1 && p.router_s2) ? __ldg(p.router_s2) : 1.0f;
-  const int R = p.E + p.Z;   // router width (zero experts included)
+  const float rs2 = (EXT && p.router_fmt == 1 && p.router_s2) ? __ldg(p.router_s2) : 1.0f;
+  const int R = EXT ? p.E + p.Z : p.E;   // router width (zero experts included)
   for (int e = cta; e < R; e += G) {
     for (int n0 = 0; n0 < p.N; n0 += 8) {
       const int nn = min(8, p.N - n0);
@@ -194,7 +196,7 @@ __device__ __noinline__ void router_phase(const Params& p, int cta, int G, Table
       for (int t = 0; t < 8; ++t) acc[t] = 0.f;
       for (int kk = ctid * 8; kk < H; kk += kConsumerThreads * 8) {
         float wf[8];
-        router_w8(p.router, p.router_fmt, p.router_s, rs2, H, e, kk, wf);
+        router_w8(p.router, EXT ? p.router_fmt : 0, p.router_s, rs2, H, e, kk, wf);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
           if (t < nn) {
@@ -270,7 +272,7 @@ __device__ __noinline__ void token_prep(const Params& p, int cta, int G, Tables&
 // ------------------------------------------------------------------- top-k
 // One warp routes token n (logits from L2: other CTAs wrote them) into the
 // per-slot selection tables.
-template <int PER>
+template <int PER, bool EXT>
 __device__ __forceinline__ void topk_token(int E, int k, int scoring, int norm, float rsf,
                                            const float* bias, const float* lrow, int n,
                                            Tables& tb, int lane) {
@@ -282,7 +284,7 @@ __device__ __forceinline__ void topk_token(int E, int k, int scoring, int norm, 
   }
   int se = 0;
   float sw = 0.f;
-  topk_warp<PER>(E, k, scoring, norm, rsf, bias, lg, lane, &se, &sw);
+  topk_warp<PER, EXT>(E, k, scoring, norm, rsf, bias, lg, lane, &se, &sw);
   if (lane < k) {
     tb.sel_e[n * k + lane] = (int16_t)se;
     tb.sel_w[n * k + lane] = sw;
@@ -443,15 +445,18 @@ __device__ __forceinline__ void build_tables(int E, int k, int S, Tables& tb, in
 }
 
 // Routing for all tokens + unique-expert tables (identical in every CTA).
+// EXT = false: top-k routing with the softmax / sigmoid + bias scorings over E
+// router outputs only (no zero experts, no hash routing).
+template <bool EXT>
 __device__ __noinline__ void routing_phase(const Params& p, int write_out, Tables& tb, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int E = p.E, k = p.k, S = p.N * p.k, scoring = p.scoring, norm = p.norm;
-  const int R = E + p.Z;   // top-k runs over the whole router width
+  const int R = EXT ? E + p.Z : E;   // top-k runs over the whole router width
   const float rsf = p.rsf;
   const float* bias = p.bias;
   for (int n = warp; n < p.N; n += kConsumerWarps) {
     const float* lrow = p.logits + (size_t)n * R;
-    if (p.hash_V > 0) {
+    if (EXT && p.hash_V > 0) {
       // hash routing: the token id's row of tid2eid (ids clamped into the table)
       const int32_t* hrow =
           p.tid2eid + (size_t)min(max(__ldg(p.token_ids + n), 0), p.hash_V - 1) * k;
@@ -461,10 +466,10 @@ __device__ __noinline__ void routing_phase(const Params& p, int write_out, Table
       else hash_token<32>(R, k, scoring, norm, rsf, lrow, n, hrow, tb, lane);
       continue;
     }
-    if (R <= 128) topk_token<4>(R, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
-    else if (R <= 256) topk_token<8>(R, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
-    else if (R <= 512) topk_token<16>(R, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
-    else topk_token<32>(R, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
+    if (R <= 128) topk_token<4, EXT>(R, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
+    else if (R <= 256) topk_token<8, EXT>(R, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
+    else if (R <= 512) topk_token<16, EXT>(R, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
+    else topk_token<32, EXT>(R, k, scoring, norm, rsf, bias, lrow, n, tb, lane);
   }
   if (!p.route_only && warp == kConsumerWarps - 1)
     for (int n = lane; n < p.N; n += 32) tb.xe[n] = (int16_t)ld_cg_s32(p.xexp + n);
@@ -1666,7 +1671,9 @@ __device__ __noinline__ void consume_down(const Params& p, Tables& tb, const Con
 
 // ------------------------------------------------------------------- kernel
 
-template <int WF>
+// EXT: the routing variants (softmax + bias scoring, zero experts, hash
+// routing, NVFP4 router) are compiled in; the common layers launch EXT = false.
+template <int WF, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 128-byte-swizzled TMA boxes need a 1024-byte aligned destination
@@ -1761,7 +1768,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
   }
 
   // P0: router, token prep, zero the readiness counters and the block accumulator
-  router_phase(p, cta, G, tb, ctid);
+  router_phase<EXT>(p, cta, G, tb, ctid);
   const int nrbl = p.route_only ? 0 : dn_blocks(p, cta, G);
   if (!p.route_only) {
     token_prep(p, cta, G, tb, ctid);
@@ -1787,7 +1794,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
   }
 
   // P1: routing
-  routing_phase(p, cta == 0, tb, ctid);
+  routing_phase<EXT>(p, cta == 0, tb, ctid);
   if (p.route_only) return;
   if (ctid == 0) mbar_arrive(rr);
 
@@ -1909,10 +1916,14 @@ int decode_grid(int device, int smem_bytes) {
   smem_bytes += 1024;   // alignment headroom of the ring (see the kernel prologue)
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
-  const void* kernels[4] = {(const void*)moe_decode_kernel<FMT_NVFP4>,
-                            (const void*)moe_decode_kernel<FMT_MXFP4>,
-                            (const void*)moe_decode_kernel<FMT_BF16>,
-                            (const void*)moe_decode_kernel<FMT_FP8>};
+  const void* kernels[8] = {(const void*)moe_decode_kernel<FMT_NVFP4, false>,
+                            (const void*)moe_decode_kernel<FMT_MXFP4, false>,
+                            (const void*)moe_decode_kernel<FMT_BF16, false>,
+                            (const void*)moe_decode_kernel<FMT_FP8, false>,
+                            (const void*)moe_decode_kernel<FMT_NVFP4, true>,
+                            (const void*)moe_decode_kernel<FMT_MXFP4, true>,
+                            (const void*)moe_decode_kernel<FMT_BF16, true>,
+                            (const void*)moe_decode_kernel<FMT_FP8, true>};
   for (const void* k : kernels) {
     int nb = 0;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
@@ -1935,10 +1946,18 @@ cudaError_t launch_decode(const Params& p, int grid, cudaStream_t stream) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (p.fmt == 0) return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_NVFP4>, p);
-  if (p.fmt == 1) return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_MXFP4>, p);
-  if (p.fmt == 2) return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_BF16>, p);
-  return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_FP8>, p);
+  // the routing variants run the EXT build of the kernel
+  const bool ext = p.scoring == 2 || p.Z > 0 || p.hash_V > 0 || p.router_fmt != 0;
+  if (ext) {
+    if (p.fmt == 0) return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_NVFP4, true>, p);
+    if (p.fmt == 1) return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_MXFP4, true>, p);
+    if (p.fmt == 2) return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_BF16, true>, p);
+    return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_FP8, true>, p);
+  }
+  if (p.fmt == 0) return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_NVFP4, false>, p);
+  if (p.fmt == 1) return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_MXFP4, false>, p);
+  if (p.fmt == 2) return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_BF16, false>, p);
+  return cudaLaunchKernelEx(&cfg, moe_decode_kernel<FMT_FP8, false>, p);
 }
 
 }  // namespace moe

@@ -53,8 +53,10 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 
 // lg[i] = logit of expert lane + 32*i (-inf where that index is >= E).  The k
 // selections are k rounds of a warp arg-max; lane j < k returns selection j
-// (expert and weight) in *e_out / *w_out, in selection order.
-template <int PER>
+// (expert and weight) in *e_out / *w_out, in selection order.  EXT = false
+// compiles only the softmax and sigmoid + bias scorings (a smaller routine for
+// the common layers).
+template <int PER, bool EXT = true>
 __device__ __forceinline__ void topk_warp(int E, int k, int scoring, int norm, float rsf,
                                           const float* bias, const float (&lg)[PER], int lane,
                                           int* e_out, float* w_out) {
@@ -75,7 +77,7 @@ __device__ __forceinline__ void topk_warp(int E, int k, int scoring, int norm, f
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
   };
-  if (scoring == 2) softmax_den();
+  if (EXT && scoring == 2) softmax_den();
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int e = lane + 32 * i;
@@ -83,8 +85,8 @@ __device__ __forceinline__ void topk_warp(int E, int k, int scoring, int norm, f
     if (e < E) {
       const float l = lg[i];
       const float sc = (scoring == 0) ? l
-                     : (scoring == 1) ? 1.0f / (1.0f + expf(-l)) + bias[e]
-                                      : expf(l - mx) / den + bias[e];
+                     : (!EXT || scoring == 1) ? 1.0f / (1.0f + expf(-l)) + bias[e]
+                                              : expf(l - mx) / den + bias[e];
       key[i] = order_key(sc);
     }
   }
