@@ -182,42 +182,54 @@ __device__ bool grid_wait(Ctrl* c, unsigned long long target, uint64_t budget_ns
 
 // ---------------------------------------------------------------- router
 // logits[n, e] = sum_h x[n, h] * Wr[e, h], FP32 accumulation of BF16 products.
+// Logits of expert e for tokens n0 .. n0 + nn - 1 (nn <= NT): one thread per
+// 8 elements of H, then a block reduction.  Only the NT-token variant that
+// runs is fetched, so small token counts execute little code.
+template <bool EXT, int NT>
+__device__ __forceinline__ void router_group(const Params& p, Tables& tb, int ctid, int R, int e,
+                                             int n0, int nn, float rs2) {
+  const int H = p.H;
+  float acc[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+  for (int kk = ctid * 8; kk < H; kk += kConsumerThreads * 8) {
+    float wf[8];
+    router_w8(p.router, EXT ? p.router_fmt : 0, p.router_s, rs2, H, e, kk, wf);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      if (t < nn) {
+        const uint4 xv = ld_nc_u4(p.x + (size_t)(n0 + t) * H + kk);
+        const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[t] = fmaf(wf[2 * i], bf16_lo(xa[i]), acc[t]);
+          acc[t] = fmaf(wf[2 * i + 1], bf16_hi(xa[i]), acc[t]);
+        }
+      }
+    }
+  }
+  block_reduce<NT, false>(acc, tb, ctid);
+  if (ctid < nn) {
+    float v = acc[0];
+#pragma unroll
+    for (int t = 1; t < NT; ++t)
+      if (ctid == t) v = acc[t];
+    p.logits[(size_t)(n0 + ctid) * R + e] = v;
+  }
+}
+
 // EXT = false: a BF16 router of width E only (the common layers).
 template <bool EXT>
 __device__ __noinline__ void router_phase(const Params& p, int cta, int G, Tables& tb, int ctid) {
-  const int H = p.H;
   const float rs2 = (EXT && p.router_fmt == 1 && p.router_s2) ? __ldg(p.router_s2) : 1.0f;
   const int R = EXT ? p.E + p.Z : p.E;   // router width (zero experts included)
   for (int e = cta; e < R; e += G) {
     for (int n0 = 0; n0 < p.N; n0 += 8) {
       const int nn = min(8, p.N - n0);
-      float acc[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) acc[t] = 0.f;
-      for (int kk = ctid * 8; kk < H; kk += kConsumerThreads * 8) {
-        float wf[8];
-        router_w8(p.router, EXT ? p.router_fmt : 0, p.router_s, rs2, H, e, kk, wf);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          if (t < nn) {
-            const uint4 xv = ld_nc_u4(p.x + (size_t)(n0 + t) * H + kk);
-            const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              acc[t] = fmaf(wf[2 * i], bf16_lo(xa[i]), acc[t]);
-              acc[t] = fmaf(wf[2 * i + 1], bf16_hi(xa[i]), acc[t]);
-            }
-          }
-        }
-      }
-      block_reduce<8, false>(acc, tb, ctid);
-      if (ctid < nn) {
-        float v = acc[0];
-#pragma unroll
-        for (int t = 1; t < 8; ++t)
-          if (ctid == t) v = acc[t];
-        p.logits[(size_t)(n0 + ctid) * R + e] = v;
-      }
+      if (nn == 1) router_group<EXT, 1>(p, tb, ctid, R, e, n0, nn, rs2);
+      else if (nn == 2) router_group<EXT, 2>(p, tb, ctid, R, e, n0, nn, rs2);
+      else if (nn <= 4) router_group<EXT, 4>(p, tb, ctid, R, e, n0, nn, rs2);
+      else router_group<EXT, 8>(p, tb, ctid, R, e, n0, nn, rs2);
     }
   }
 }
@@ -1375,6 +1387,45 @@ __device__ __forceinline__ void compute_dn_bf16(const uint8_t* st, const SG& g, 
 // Shared expert: BF16 h of 32 rows.  Routed: lanes 0-15 of the tile are gate
 // rows, 16-31 up rows; h = SiLU(g)*u for the 16 rows, stored as f16 times
 // 2^-e with e chosen from the group's largest |h| (max in [64, 128)).
+// Routed group epilogue for NT token slots (nt <= NT of them used).
+template <int NT>
+__device__ __forceinline__ void rg_epilogue_ar(const Params& p, const Tables& tb, const RG& r,
+                                               const float* red, int lane) {
+  const int j = lane;
+  const float g2 = tb.s2[0][r.u], u2 = tb.s2[1][r.u];
+  float h[NT];
+  float m = 0.f;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    h[t] = 0.f;
+    if (t < r.nt) {
+      float g = 0.f, u = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        g += red[((w * 2) * kTB + t) * 32 + j];
+        u += red[((w * 2) * kTB + t) * 32 + 16 + j];
+      }
+      // FP4 / FP8 experts ran on x * 2^-xe; BF16 routed experts on x itself
+      const float xs = (p.fmt == FMT_BF16) ? 1.0f : exp2i(tb.xe[rg_token<KIND_AR>(tb, r, t)]);
+      g *= xs * g2;
+      u *= xs * u2;
+      h[t] = silu(g) * u;
+      m = fmaxf(m, fabsf(h[t]));
+    }
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0x0000ffffu, m, o));
+  const int e = min(max(scale_exponent(m), -126), 127);
+  const float sc = pow2i(-e);
+  const int slot0 = tb.hoff[r.u] + r.tb * kTB;
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+    if (t < r.nt)
+      p.h16[(size_t)(slot0 + t) * p.inter + r.rg * kDnRows + j] =
+          __half_as_ushort(__float2half_rn(h[t] * sc));
+  if (j == 0) p.hexp[(size_t)r.unit * p.hstride + r.rg] = (int8_t)e;
+}
+
 template <int KIND>
 __device__ __forceinline__ void rg_epilogue(const Params& p, const Tables& tb, const RG& r,
                                             const float* red, int lane) {
@@ -1391,39 +1442,9 @@ __device__ __forceinline__ void rg_epilogue(const Params& p, const Tables& tb, c
       p.hs[(size_t)n * p.Is + r.rg * kRows + lane] = *reinterpret_cast<const uint16_t*>(&hb);
     }
   } else if (lane < 16) {
-    const int j = lane;
-    const float g2 = tb.s2[0][r.u], u2 = tb.s2[1][r.u];
-    float h[kTB];
-    float m = 0.f;
-#pragma unroll
-    for (int t = 0; t < kTB; ++t) {
-      h[t] = 0.f;
-      if (t < r.nt) {
-        float g = 0.f, u = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          g += red[((w * 2) * kTB + t) * 32 + j];
-          u += red[((w * 2) * kTB + t) * 32 + 16 + j];
-        }
-        // FP4 experts ran on x * 2^-xe; BF16 routed experts on x itself
-        const float xs = (p.fmt == FMT_BF16) ? 1.0f : exp2i(tb.xe[rg_token<KIND>(tb, r, t)]);
-        g *= xs * g2;
-        u *= xs * u2;
-        h[t] = silu(g) * u;
-        m = fmaxf(m, fabsf(h[t]));
-      }
-    }
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0x0000ffffu, m, o));
-    const int e = min(max(scale_exponent(m), -126), 127);
-    const float sc = pow2i(-e);
-    const int slot0 = tb.hoff[r.u] + r.tb * kTB;
-#pragma unroll
-    for (int t = 0; t < kTB; ++t)
-      if (t < r.nt)
-        p.h16[(size_t)(slot0 + t) * p.inter + r.rg * kDnRows + j] =
-            __half_as_ushort(__float2half_rn(h[t] * sc));
-    if (j == 0) p.hexp[(size_t)r.unit * p.hstride + r.rg] = (int8_t)e;
+    if (r.nt == 1) rg_epilogue_ar<1>(p, tb, r, red, lane);
+    else if (r.nt == 2) rg_epilogue_ar<2>(p, tb, r, red, lane);
+    else rg_epilogue_ar<kTB>(p, tb, r, red, lane);
   }
 }
 
