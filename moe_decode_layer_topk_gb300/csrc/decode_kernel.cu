@@ -7,30 +7,39 @@
 // (forward_atomic_c4.rs, doc comment of forward_atomic_c4_decode).
 //
 // Execution model: a persistent grid, one CTA per SM, every CTA resident at
-// once (cooperative launch).  Each CTA has 8 compute ("consumer") warps and
-// 4 producer threads (lane 0 of 4 warps, stage k issued by producer k mod 4:
-// a TMA instruction from DRAM holds its thread for a few hundred cycles) that
-// stream weights into a ring of shared-memory stages with TMA (2D tensor-map
-// boxes of 16 or 32 rows x 128 bytes, 128-byte swizzle), completion tracked
-// by mbarriers.
+// once (cooperative launch).  Each CTA has 8 compute ("consumer") warps, one
+// epilogue warp, and 4 producer threads (lane 0 of 4 warps, stage k issued by
+// producer k mod 4: a TMA instruction from DRAM holds its thread for a few
+// hundred cycles) that stream weights into a ring of shared-memory stages
+// with TMA (3D tensor-map copies of whole 512-byte chunks, or 2D boxes of 16
+// or 32 rows x 128 bytes; 128-byte swizzle), completion tracked by mbarriers.
+//
+// Instruction fetch is a first-order cost here (the code a launch runs does
+// not stay in the SM's instruction cache), so the kernel is built twice per
+// weight format (the routing variants apart) and count-dependent steps
+// dispatch to one template instance per token count.
 //
 // Phases of one call (per CTA):
-//   P0  router GEMV for rows e = cta, cta+G, ... (128-bit loads); token prep
+//   P0  router GEMV for rows e = cta, cta+G, ... (128-bit loads; BF16 or NVFP4
+//       router, E + Z rows with zero experts); token prep
 //       (f16 copy of x scaled by a power of two, shared-expert gate) on the
 //       last CTAs; zero the per-unit readiness counters.
 //   --  grid barrier B1 (arrive).  Shared-expert gate/up row groups need only
 //       x, so they are streamed and computed before waiting on B1.
-//   P1  every CTA computes the same top-k for all N tokens and the same table
+//   P1  every CTA computes the same top-k (or hash routing) for all N tokens
+//       and the same table
 //       of unique experts, per-expert token lists and (expert, token batch)
-//       units: each routed expert's weights are then read once for all its
-//       tokens (forward_batched.rs: "streams its weights once for all rows").
+//       units (zero-expert slots run nothing): each routed expert's weights
+//       are then read once for all its tokens (forward_batched.rs: "streams
+//       its weights once for all rows").
 //   P2  routed gate/up row groups of 16 rows (gate rows and up rows stacked
-//       as one 32-row tile, lane j < 16 gate, lane j >= 16 up): h = SiLU(g)*u
-//       stored as f16 with one power-of-two exponent per 16 rows; each row
-//       group bumps its unit's readiness counter.
+//       as one 32-row tile, lane j < 16 gate, lane j >= 16 up); the epilogue
+//       warp forms h = SiLU(g)*u, stored as f16 with one power-of-two
+//       exponent per 16 rows, and publishes the CTA's row groups to the
+//       units' readiness counters.
 //   P3  down: each CTA owns whole 16-row blocks of the output.  Every unit
-//       (and shared-expert token batch) is one job for one warp (half-warps
-//       split K); the producer prefetches the down weights during P2 and adds
+//       (and shared-expert token batch) is one job for S = 8 / jobs-per-block
+//       warps (half-warps split K); the producer prefetches the down weights during P2 and adds
 //       a job's activations to its stage once the unit's counter says its h
 //       is complete.  Jobs add their routing-weighted rows into shared
 //       memory; the block is cast to BF16 and written once: no second grid
@@ -46,7 +55,10 @@
 // scaled by a power of two that keeps every partial below 2^14; each block
 // partial is then multiplied by its E4M3/E8M0 scale (times the h exponent in
 // the down projection) and accumulated in FP32.  The shared expert (BF16)
-// uses fma.rn.f32.bf16 (BF16 products, FP32 accumulation).
+// uses fma.rn.f32.bf16 (BF16 products, FP32 accumulation).  FP8 experts:
+// E4M3 -> f16 (exact), products with f16 x or h formed and summed in FP32,
+// each 32-element step times its 128 x 128 block scale.  BF16 experts: BF16
+// products with the BF16 x (gate/up) or the f16 h (down) in FP32.
 //
 // Every wait (grid barrier, stage, readiness) is bounded by a time budget; on
 // expiry the kernel records an error bit in the workspace and drains.
