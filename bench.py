@@ -12,14 +12,17 @@ back from the routing outputs before timing).  value = sum of bytes / time.
 
 Timed region: K steps replayed from a captured CUDA graph, bracketed by a
 barrier and torch.cuda.synchronize(), CUDA events on the launch stream; the
-maximum over ranks is taken.  The line also carries "grouped": the many-token
+maximum over ranks is taken.  "per_n" gives each token count's latency
+(median of five repeats of a round-robin loop) and "per_n_l2_flush" the same
+from single calls after an L2-sized buffer write.  The line also carries "grouped": the many-token
 path (gpt-oss-shaped MXFP4 layer at N = 512, tcgen05 GEMMs),
 "bf16_experts" and "fp8_experts": the same Qwen3 shape with BF16 or FP8
 (128 x 128 block-scaled) routed experts at N = 1-4, and "nvfp4_router": the
 Qwen3 shape with an NVFP4-quantised router, and "zero_experts": the Qwen3
 shape with 64 zero experts (softmax + correction-bias routing over 192
 router outputs), all timed on the same GPU after the main measurement.  --impl reference
-times the FP64 CPU oracle on a bounded sample of the same workload instead.
+times the FP64 CPU oracle on a bounded sample of the same workload instead;
+"cpu_baseline" also holds the oracle's single-thread per-call times.
 """
 from __future__ import annotations
 
@@ -36,6 +39,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 PEAK_FALLBACK_GBS = 6800.0
+PER_N_REPEATS = 5   # per-N latency: median over this many repeats of the timed loop
 NOMINAL_HBM_GBS = 8000.0
 METRIC = "MoE layer us and expert-weight HBM GB/s (fraction of 8 TB/s) at N=1-4 tokens"
 
@@ -368,26 +372,38 @@ def run_gpu(args):
                 for dev, n_, x, out, ws, _ in sub:
                     _lib.moe_forward(dev.desc, dev.weights, x, out, ws, stream=stream)
         rounds = max(1, reps // len(sub))
-        with torch.cuda.stream(stream):
-            if g is not None:
-                g.replay()
-            e0.record(stream)
-            for _ in range(rounds):
+        rep_us = []
+        for _ in range(PER_N_REPEATS):
+            with torch.cuda.stream(stream):
                 if g is not None:
                     g.replay()
-                else:
-                    for dev, n_, x, out, ws, _ in sub:
-                        _lib.moe_forward(dev.desc, dev.weights, x, out, ws, stream=stream)
-            e1.record(stream)
-        torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / (rounds * len(sub))
+                e0.record(stream)
+                for _ in range(rounds):
+                    if g is not None:
+                        g.replay()
+                    else:
+                        for dev, n_, x, out, ws, _ in sub:
+                            _lib.moe_forward(dev.desc, dev.weights, x, out, ws, stream=stream)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            rep_us.append(e0.elapsed_time(e1) * 1e3 / (rounds * len(sub)))
+        us = float(np.median(rep_us))
         b = float(np.mean([c[5]["total"] for c in sub]))
         br = float(np.mean([c[5]["routed"] for c in sub]))
-        per_n[str(N)] = {"us_per_layer": round(us, 3), "tokens_per_s": round(N / us * 1e6, 1),
+        per_n[str(N)] = {"us_per_layer": round(us, 3),
+                         "us_repeats": [round(u, 3) for u in rep_us],
+                         "calls_per_repeat": rounds * len(sub),
+                         "tokens_per_s": round(N / us * 1e6, 1),
                          "GBps": round(b / us / 1e3, 1),
                          "frac_of_8TBs": round(b / us / 1e3 / NOMINAL_HBM_GBS, 4),
                          "U_mean": float(np.mean([c[5]["U"] for c in sub])),
                          "bytes_mean": int(b), "routed_bytes_mean": int(br)}
+
+    # cross-check of the L2 defeat: one call at a time on layer copy 0 after
+    # writing a buffer twice the L2 size (so nothing of the call is cached)
+    per_n_flush = None
+    if rank == 0 and not args.no_l2_flush:
+        per_n_flush = l2_flush_latency(stream, calls, tokens, l2)
 
     # end to end through the host-buffer entry point (pinned host x / out)
     e2e = None
@@ -437,6 +453,7 @@ def run_gpu(args):
         "frac_of_8TBs": round(value / world / NOMINAL_HBM_GBS, 4),
         "us_per_layer_mean": round(avg_launch_us, 3),
         "per_n": per_n,
+        "per_n_l2_flush": per_n_flush,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": None if traffic is None else int(traffic),
@@ -467,8 +484,79 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def l2_flush_latency(stream, calls, tokens, l2_bytes: int, reps: int = 30) -> dict:
+    """Per token count: median CUDA-event time of single moe_forward calls on
+    layer copy 0, each one after a write of 2 x L2 bytes on the same stream
+    (L2 holds none of the call's bytes), as a check on the round-robin
+    figures, which defeat L2 by cycling layer copies instead."""
+    import torch
+    from moe_decode_layer_topk_gb300 import _lib
+    flush = torch.empty(2 * l2_bytes, dtype=torch.uint8, device="cuda")
+    res = {}
+    for N in tokens:
+        dev, _, x, out, ws, b = next(c for c in calls if c[1] == N)
+        evs = []
+        with torch.cuda.stream(stream):
+            for i in range(reps + 3):
+                flush.fill_(i & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                _lib.moe_forward(dev.desc, dev.weights, x, out, ws, stream=stream)
+                e1.record(stream)
+                if i >= 3:
+                    evs.append((e0, e1))
+        torch.cuda.synchronize()
+        assert _lib.moe_get_error(ws) == _lib.MOE_OK
+        us = float(np.median([a.elapsed_time(z) * 1e3 for a, z in evs]))
+        res[str(N)] = {"us_per_layer": round(us, 3), "GBps": round(b["total"] / us / 1e3, 1),
+                       "U": b["U"], "calls": reps}
+    del flush
+    torch.cuda.empty_cache()
+    return {"method": f"write of {2 * l2_bytes} bytes before each call, layer copy 0, "
+                      f"median of {reps} calls", "per_n": res}
+
+
+def oracle_single_thread(budget_s: float = 8.0) -> dict:
+    """The oracle on one host thread, one call each on the small, Qwen3 and
+    MTP-verify layers (per-call milliseconds), then the thread count restored."""
+    from moe_decode_layer_topk_gb300 import synth
+    from oracle import oracle
+    full = oracle.num_threads()
+    oracle.set_num_threads(1)
+    res, t_all = {}, 0.0
+    try:
+        for name, N, calls in (("tiny", 1, 20), ("qwen3_30b_a3b", 1, 1), ("mtp_verify", 3, 1)):
+            if t_all > budget_s:
+                break
+            spec = synth.CONFIGS[name]
+            host = synth.make_layer(spec)
+            x = synth.make_tokens(spec, N, seed=71000 + N)
+            t0 = time.perf_counter()
+            for _ in range(calls):
+                oracle.moe_forward(host, x)
+            dt = time.perf_counter() - t0
+            t_all += dt
+            res[f"{name}_n{N}"] = {"ms_per_call": round(dt / calls * 1e3, 2), "calls": calls}
+    finally:
+        oracle.set_num_threads(full)
+    return {"cores": 1, "per_config": res}
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
 def cpu_baseline(spec, tokens, budget_s: float):
-    """The FP64 oracle (as it stands) on a bounded sample of the workload."""
+    """The FP64 oracle (as it stands) on a bounded sample of the workload, on
+    all host threads, plus the single-thread per-call times of the small,
+    Qwen3 and MTP-verify layers."""
     from moe_decode_layer_topk_gb300 import synth
     from oracle import oracle
     host = synth.make_layer(spec)
@@ -484,7 +572,9 @@ def cpu_baseline(spec, tokens, budget_s: float):
     return {"value": round(nbytes / t_total / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
             "kind": "oracle",
             "sample": f"{steps} steps of moe_forward at N={','.join(map(str, tokens))} on "
-                      f"{spec.name} ({t_total:.1f} s of CPU time)"}
+                      f"{spec.name} ({t_total:.1f} s of CPU time)",
+            "cpu_model": cpu_model(), "host_cpus": os.cpu_count(),
+            "single_thread": oracle_single_thread()}
 
 
 def run_reference(args):
@@ -545,6 +635,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-l2-flush", action="store_true",
+                    help="skip the per-N L2-flush cross-check")
     ap.add_argument("--no-bf16", action="store_true",
                     help="skip the BF16 routed-expert decode measurement")
     ap.add_argument("--no-fp8", action="store_true",

@@ -460,4 +460,15 @@ int oracle_num_threads(void) {
 #endif
 }
 
+// Threads of the oracle's later parallel loops (n >= 1).  Each output element
+// is still summed by one thread in index order, so the results do not depend
+// on it; only the timing does.
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 }  // extern "C"

@@ -80,6 +80,8 @@ def lib():
                                              vp, vp, vp, vp, vp, i32, i32, vp]
             L.oracle_num_threads.restype = i32
             L.oracle_num_threads.argtypes = []
+            L.oracle_set_num_threads.restype = None
+            L.oracle_set_num_threads.argtypes = [i32]
             _lib = L
     return _lib
 
@@ -236,3 +238,9 @@ def moe_forward(layer, x: np.ndarray, token_ids: Optional[np.ndarray] = None):
 
 def num_threads() -> int:
     return lib().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops from now on (timing only: every
+    output element is summed by one thread in index order either way)."""
+    lib().oracle_set_num_threads(int(n))
