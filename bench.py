@@ -172,10 +172,15 @@ def decode_traffic(calls, launches_per_cycle: int):
 
 
 def kernels_per_call(spec, N: int) -> int:
-    """Kernels one moe_forward enqueues: the fused decode kernel, or the
-    grouped chain (router, top-k, plan, gather, gate/up GEMM, pack, down GEMM,
-    combine) once N * top_k exceeds the decode slot table (256)."""
-    return 1 if N * spec.top_k <= 256 else 8
+    """Kernels one moe_forward enqueues, as the library reports its path: the
+    fused decode kernel, or the grouped chain (router, top-k, plan, gather,
+    gate/up GEMM, pack, down GEMM, combine)."""
+    from moe_decode_layer_topk_gb300 import _lib
+    from moe_decode_layer_topk_gb300.device import layer_desc
+    g = _lib.moe_uses_grouped_path(layer_desc(spec), N)
+    if g < 0:
+        raise ValueError(f"invalid layer or token count: {spec.name}, N={N}")
+    return 8 if g else 1
 
 
 def measure_grouped(stream, name: str = "gpt_oss_120b", N: int = 512, reps: int = 10) -> dict:

@@ -164,10 +164,20 @@ typedef struct {
  * Returns 0 if the descriptor is invalid.  The workspace holds the router
  * logits, the routing table, the gate/up activations, the FP32 output
  * accumulator and the grid-barrier words (the scratch the pages carve out of
- * ctx.buffers.scratch() in forward_atomic_c4.rs); when max_tokens * top_k >
- * 256 it also covers the grouped path's expert-sorted activation copies
- * (about S * (2H + 4 max(H, inter) + 2 inter) bytes, S = max_tokens * top_k). */
+ * ctx.buffers.scratch() in forward_atomic_c4.rs); when max_tokens runs the
+ * grouped path (see moe_forward) it also covers that path's expert-sorted
+ * activation copies (about S * (2H + 4 max(H, inter) + 2 inter) bytes,
+ * S = max_tokens * top_k). */
 MOE_API size_t moe_workspace_size(const moe_layer_desc_t* desc, int32_t max_tokens);
+
+/* The path moe_forward (and moe_route, moe_forward_ids, moe_forward_host)
+ * takes for N token rows of this layer: 1 = the grouped path (eight
+ * kernels: router, top-k, plan, gather, gate/up GEMM, pack, down GEMM,
+ * combine; moe_route stops after the top-k), 0 = the fused decode kernel
+ * (one kernel), -1 = invalid descriptor or N < 1.  Host-only: makes no
+ * CUDA call.  The rule is the one moe_forward's description states; the
+ * grouped path refuses the layers it does not run (MOE_ERR_UNSUPPORTED). */
+MOE_API int32_t moe_uses_grouped_path(const moe_layer_desc_t* desc, int32_t N);
 
 /* Zero a workspace before its first use (and after MOE_ERR_TIMEOUT).  Enqueues
  * a memset on `stream`.  Afterwards moe_forward keeps the workspace's barrier
@@ -182,12 +192,16 @@ MOE_API moe_status_t moe_workspace_init(void* workspace, size_t ws_bytes, void* 
  *   topk_w    f32 [N, top_k] device or NULL: their routing weights
  *   workspace device, >= moe_workspace_size(desc, N) bytes, zeroed once by
  *             moe_workspace_init; one workspace per concurrently running call
- * N*top_k <= 256 runs one fused decode kernel; larger N runs the grouped
+ * N*top_k <= 256 runs one fused decode kernel, N*top_k > 256 the grouped
  * path (per-expert token groups on the tcgen05 tensor cores, the pages'
- * "grouped GEMM (more than 64 rows)" of forward_batched.rs), which takes
- * neither a shared expert, BF16 / FP8 routed experts nor zero experts yet:
- * N*top_k > 256 with shared_inter > 0, wfmt MOE_W_BF16 / MOE_W_FP8 or
- * zero_experts > 0 returns MOE_ERR_UNSUPPORTED.  With zero experts, topk_idx
+ * "grouped GEMM (more than 64 rows)" of forward_batched.rs).  Layers the
+ * grouped path runs (NVFP4 / MXFP4 experts, no shared expert, no zero
+ * experts, no hash routing) whose experts hold >= 1 MiB of weights
+ * (3 * inter * H * (1/2 + 1/gs) bytes) take it from N*top_k >= 128, where
+ * it is the faster of the two.  The grouped path takes neither a shared
+ * expert, BF16 / FP8 routed experts nor zero experts yet: N*top_k > 256
+ * with shared_inter > 0, wfmt MOE_W_BF16 / MOE_W_FP8 or zero_experts > 0
+ * returns MOE_ERR_UNSUPPORTED.  With zero experts, topk_idx
  * holds indices up to E + Z - 1 (>= E: a zero expert).  Asynchronous on `stream`; no host synchronisation,
  * no allocation, so it may be captured in a CUDA graph.  Argument errors are
  * returned before anything is enqueued; device-side timeouts are reported by

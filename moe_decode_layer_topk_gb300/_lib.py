@@ -34,7 +34,7 @@ MOE_R_NVFP4 = 1
 EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_forward", "moe_route",
             "moe_host_staging_size", "moe_forward_host", "moe_get_error", "moe_status_string",
             "moe_abi_version", "moe_debug_set_wait_budget_ns", "moe_forward_noalloc",
-            "moe_forward_ids")
+            "moe_forward_ids", "moe_uses_grouped_path")
 
 
 class MoeError(RuntimeError):
@@ -76,6 +76,8 @@ def load() -> ctypes.CDLL:
         pd, pw = ctypes.POINTER(LayerDesc), ctypes.POINTER(Weights)
         L.moe_workspace_size.restype = sz
         L.moe_workspace_size.argtypes = [pd, i32]
+        L.moe_uses_grouped_path.restype = i32
+        L.moe_uses_grouped_path.argtypes = [pd, i32]
         L.moe_host_staging_size.restype = sz
         L.moe_host_staging_size.argtypes = [pd, i32]
         L.moe_workspace_init.restype = i32
@@ -132,6 +134,10 @@ def moe_abi_version() -> int:
 
 def moe_workspace_size(desc: LayerDesc, max_tokens: int) -> int:
     return load().moe_workspace_size(ctypes.byref(desc), int(max_tokens))
+
+
+def moe_uses_grouped_path(desc: LayerDesc, N: int) -> int:
+    return load().moe_uses_grouped_path(ctypes.byref(desc), int(N))
 
 
 def moe_host_staging_size(desc: LayerDesc, max_tokens: int) -> int:

@@ -88,12 +88,33 @@ GWsLayout gws_layout(const moe_layer_desc_t& d, int32_t N) {
   return L;
 }
 
+// Layers the grouped path runs: FP4 experts, no shared expert, no zero
+// experts, no hash routing.
+bool grouped_capable(const moe_layer_desc_t& d) {
+  return (d.wfmt == MOE_W_NVFP4 || d.wfmt == MOE_W_MXFP4) && d.shared_inter == 0 &&
+         d.zero_experts == 0 && d.hash_vocab == 0;
+}
+
+// The decode kernel takes up to kMaxSlots (token, slot) pairs.  Layers the
+// grouped path runs switch to it from kGroupedMinSlots pairs when an expert
+// holds at least kGroupedMinExpertBytes of weights: there its GEMMs stream
+// the experts about twice as fast (GB300, same experts touched: gpt-oss
+// shape 750 us at N = 65 against 2022 us for the decode kernel at N = 64;
+// Qwen3 shape 181 us at N = 33 against 322 us at N = 32).  Monotone in N, so
+// a workspace sized for max_tokens covers every smaller N.
+constexpr long long kGroupedMinSlots = 128;
+constexpr double kGroupedMinExpertBytes = 1024.0 * 1024.0;
+
 bool grouped_path(const moe_layer_desc_t& d, int32_t N) {
-  return (long long)N * d.top_k > moe::kMaxSlots;
+  const long long slots = (long long)N * d.top_k;
+  if (slots > moe::kMaxSlots) return true;
+  if (slots < kGroupedMinSlots || !grouped_capable(d)) return false;
+  const double per_byte = 0.5 + (d.wfmt == MOE_W_NVFP4 ? 1.0 / 16 : 1.0 / 32);   // codes + scales
+  return 3.0 * d.inter * d.H * per_byte >= kGroupedMinExpertBytes;
 }
 
 // Workspace bytes for any N <= max_tokens (decode layout up to the slot
-// limit, grouped layout beyond it).
+// limit, grouped layout where grouped_path takes max_tokens).
 size_t ws_total(const moe_layer_desc_t& d, int32_t max_tokens) {
   const int32_t ndec = std::min(max_tokens, (int32_t)(moe::kMaxSlots / d.top_k));
   size_t t = ndec >= 1 ? ws_layout(d, ndec).total : 0;
@@ -533,6 +554,11 @@ extern "C" {
 size_t moe_workspace_size(const moe_layer_desc_t* desc, int32_t max_tokens) {
   if (check_desc(desc) != MOE_OK || max_tokens < 1) return 0;
   return ws_total(*desc, max_tokens);
+}
+
+int32_t moe_uses_grouped_path(const moe_layer_desc_t* desc, int32_t N) {
+  if (check_desc(desc) != MOE_OK || N < 1) return -1;
+  return grouped_path(*desc, N) ? 1 : 0;
 }
 
 size_t moe_host_staging_size(const moe_layer_desc_t* desc, int32_t max_tokens) {

@@ -95,6 +95,30 @@ def _forward(lib, d, w, N=1, x=1 << 24, out=1 << 25, ws=1 << 26, ws_bytes=1 << 3
     return lib.moe_forward(ctypes.byref(d), ctypes.byref(w), x, N, out, None, None, ws, ws_bytes, None)
 
 
+def test_dispatch_rule(lib):
+    """Decode kernel up to 256 (token, slot) pairs, grouped path beyond; FP4
+    layers without a shared expert, zero experts or hash routing whose
+    experts hold >= 1 MiB of weights switch at 128 pairs.  Host-only."""
+    from moe_decode_layer_topk_gb300.device import layer_desc
+
+    def g(spec, N):
+        return _lib.moe_uses_grouped_path(layer_desc(spec), N)
+
+    oss, q3 = synth.CONFIGS["gpt_oss_120b"], synth.CONFIGS["qwen3_30b_a3b"]
+    assert [g(oss, n) for n in (1, 4, 31, 32, 64, 65, 512)] == [0, 0, 0, 1, 1, 1, 1]
+    assert [g(q3, n) for n in (1, 4, 15, 16, 32, 33)] == [0, 0, 0, 1, 1, 1]
+    assert g(synth.CONFIGS["qwen3_30b_a3b_nvfp4_router"], 16) == 1
+    for name in ("deepseek_v3", "mtp_verify", "qwen3_30b_a3b_bf16", "qwen3_30b_a3b_fp8",
+                 "qwen3_30b_a3b_zero_experts"):       # decode up to the slot limit
+        sp = synth.CONFIGS[name]
+        assert (g(sp, 256 // sp.top_k), g(sp, 256 // sp.top_k + 1)) == (0, 1), name
+    tiny = synth.CONFIGS["tiny"]                      # 55 KB experts
+    assert (g(tiny, 128), g(tiny, 129)) == (0, 1)
+    assert g(tiny, 0) == -1
+    ws = [_lib.moe_workspace_size(layer_desc(oss), n) for n in range(1, 80)]
+    assert all(a <= b for a, b in zip(ws, ws[1:]))
+
+
 def test_argument_refusals_happen_before_any_cuda_call(lib):
     """Every case below is refused by the host checks (no GPU needed)."""
     d, w = _desc(), _fake_weights()
