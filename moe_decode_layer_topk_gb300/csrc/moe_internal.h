@@ -128,7 +128,8 @@ struct Params {
 };
 
 // ------------------------------------------------------------ grouped path
-// Many-token forward (N * top_k beyond kMaxSlots): per-expert token groups on
+// Many-token forward (N * top_k beyond kMaxSlots, or from 128 for large FP4
+// experts; moe_api.cu grouped_path): per-expert token groups on
 // the tensor cores (grouped_kernel.cu).
 constexpr int kGTileTok = 32;   // positions per token tile (MMA N <= 32)
 

@@ -1,6 +1,7 @@
 """Grouped (many-token) path vs the FP64 oracle, through the C ABI.
 
-When N * top_k exceeds the decode kernel's slot table, moe_forward runs the
+When N * top_k exceeds the decode kernel's slot table (or reaches 128 for a
+layer whose FP4 experts hold >= 1 MiB each), moe_forward runs the
 per-expert token-group GEMMs on the tcgen05 tensor cores.  The small cases
 span ragged 128-row weight tiles (32-row tails), a ragged K chunk, experts
 with more positions than one 64-position token tile, both formats, both
