@@ -38,7 +38,7 @@
  *     accumulation of the routed down projections, then a BF16 cast and the
  *     shared-expert blend; the scratch carve-out and its size check;
  *   - forward_batched.rs: one router GEMM for N rows, per-token routing, and
- *     "each routed and shared expert streams its weights once for all rows";
+ *     every routed and shared expert's weights read in one pass for all rows;
  *     its BF16 expert branch (bf16 gate/up/down weight pointers, the same
  *     kernels as the FP4 forward) for the BF16 routed-expert format, and the
  *     FP8 expert branch (weight_ptrs + scale_ptrs of moe_expert_gate_up_
@@ -94,7 +94,7 @@ extern "C" {
 #endif
 
 /* Status codes.  A refusal names what is wrong instead of computing a wrong
- * answer (forward_k3.rs: "Named refusal, not silent wrongness"). */
+ * answer (the rule of forward_k3.rs's zero-expert guard). */
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,          /* null required pointer, N < 1, bad alignment */
@@ -193,8 +193,8 @@ MOE_API moe_status_t moe_workspace_init(void* workspace, size_t ws_bytes, void* 
  *   workspace device, >= moe_workspace_size(desc, N) bytes, zeroed once by
  *             moe_workspace_init; one workspace per concurrently running call
  * N*top_k <= 256 runs one fused decode kernel, N*top_k > 256 the grouped
- * path (per-expert token groups on the tcgen05 tensor cores, the pages'
- * "grouped GEMM (more than 64 rows)" of forward_batched.rs).  Layers the
+ * path (per-expert token groups on the tcgen05 tensor cores, the grouped
+ * GEMM forward_batched.rs switches to for larger row counts).  Layers the
  * grouped path runs (NVFP4 / MXFP4 experts, no shared expert, no zero
  * experts, no hash routing) whose experts hold >= 1 MiB of weights
  * (3 * inter * H * (1/2 + 1/gs) bytes) take it from N*top_k >= 128, where

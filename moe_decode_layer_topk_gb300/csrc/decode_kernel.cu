@@ -30,8 +30,8 @@
 //       and the same table
 //       of unique experts, per-expert token lists and (expert, token batch)
 //       units (zero-expert slots run nothing): each routed expert's weights
-//       are then read once for all its tokens (forward_batched.rs: "streams
-//       its weights once for all rows").
+//       are then read once for all its tokens (forward_batched.rs: one pass
+//       over an expert's weights serves every row routed to it).
 //   P2  routed gate/up row groups of 16 rows (gate rows and up rows stacked
 //       as one 32-row tile, lane j < 16 gate, lane j >= 16 up); the epilogue
 //       warp forms h = SiLU(g)*u, stored as f16 with one power-of-two

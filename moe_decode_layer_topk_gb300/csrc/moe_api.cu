@@ -1,8 +1,8 @@
 // C ABI of the MoE decode-layer forward (include/moe.h): argument checks,
 // workspace carve-out, and the launch of the fused decode kernel.
 //
-// Checks follow the pages' "named refusal, not silent wrongness" rule
-// (forward_k3.rs, the zero-expert guard) and the scratch-size check of
+// Checks follow the pages' rule of refusing an unsupported case by name
+// rather than computing a wrong result (forward_k3.rs, the zero-expert guard) and the scratch-size check of
 // forward_atomic_c4.rs: every refusal returns a status before anything is
 // enqueued.
 

@@ -10,14 +10,14 @@
 //   * forward_k3.rs, doc comment of MoeLayer::forward_k3 — the chain
 //     router logits -> top-k -> expert gate+up -> SiLU+down -> weighted sum
 //     + shared-expert blend;
-//   * forward_k3.rs, step "2. Batched topK" (moe_topk_sigmoid_batched /
+//   * forward_k3.rs, the batched top-k step (moe_topk_sigmoid_batched /
 //     moe_topk_softmax_batched arguments) — softmax with optional
 //     renormalisation, or sigmoid + correction bias with norm_topk_prob and
 //     routed_scaling_factor;
 //   * forward_k3.rs, the E8M0 guard (GS16 vs GS32 scale groups) — NVFP4
 //     (E2M1 + per-16 E4M3) and MXFP4 (E2M1 + per-32 E8M0) expert formats;
 //   * forward_batched.rs, the BF16 expert branch (bf16_gate/up/down weight
-//     pointers, "BF16 experts, with the same kernels") — BF16 routed experts,
+//     pointers, run through the plain forward's kernels) — BF16 routed experts,
 //     the same chain with plain BF16 weights (no block scales);
 //   * forward_k3.rs / forward_batched.rs, the FP8 expert branch (fp8 gate/up/
 //     down weight_ptrs + scale_ptrs into moe_expert_gate_up_shared_fp8 and
@@ -28,9 +28,9 @@
 //     into w4a16_gemv_batch3 / w4a16_gemm / w4a16_decode_gemv) — the router
 //     weight may be NVFP4 (E2M1 + per-16 E4M3 scale + FP32 scale2) against the
 //     BF16 activations;
-//   * forward_k3.rs / forward_batched.rs, the zero-expert guards ("LongCat
-//     zero-experts", a router of width num_experts + zero_expert_num "served
-//     only through the softmax+bias arm") — routing over E + Z router outputs
+//   * forward_k3.rs / forward_batched.rs, the zero-expert guards (a router of
+//     width num_experts + zero_expert_num, run only with softmax + bias
+//     scoring) — routing over E + Z router outputs
 //     with softmax scores plus a correction bias for selection; a selected
 //     zero expert runs no expert.  The pages do not say what a zero expert
 //     adds; the reading taken is nothing (its output is zero);
@@ -43,8 +43,8 @@
 //   * forward_atomic_c4.rs, doc comment — routed outputs accumulated as
 //     routing-weighted sums, then cast to BF16 and blended with the shared
 //     expert;
-//   * forward_k3.rs, the EP all-reduce block ("Add shared expert with sigmoid
-//     gate") — a null shared_expert_gate adds the shared expert as is,
+//   * forward_k3.rs, the EP all-reduce block (the sigmoid-gated shared-expert
+//     add) — a null shared_expert_gate adds the shared expert as is,
 //     otherwise it is blended with sigmoid(w_s . x).
 // Readings where the pages are silent (nibble order, tie order, bias only in
 // selection, scaling only on the sigmoid path) are stated at each function.
