@@ -678,6 +678,24 @@ def test_per_token_independence(oracle_mod):
         np.testing.assert_array_equal(one["idx"][0], full["idx"][n])
 
 
+def test_thread_count_does_not_change_results(oracle_mod):
+    """Every output element is summed by one thread in index order, so one
+    thread and all threads give the same bits (the benchmark times both)."""
+    sp = _small_spec(E=8, top_k=2, shared_inter=32, shared_gated=True)
+    L = synth.make_layer(sp, seed=23)
+    x = synth.make_tokens(sp, 5, seed=24)
+    full = oracle_mod.num_threads()
+    ref = oracle_mod.moe_forward(L, x)
+    oracle_mod.set_num_threads(1)
+    try:
+        one = oracle_mod.moe_forward(L, x)
+    finally:
+        oracle_mod.set_num_threads(full)
+    assert oracle_mod.num_threads() == full
+    for key in ("out_f64", "idx", "w", "logits"):
+        np.testing.assert_array_equal(one[key], ref[key])
+
+
 def test_expert_permutation_invariance(oracle_mod):
     sp = _small_spec(E=8, top_k=3, scoring=synth.SIGMOID_BIAS, routed_scaling_factor=1.7)
     L = synth.make_layer(sp, seed=23)
