@@ -1,9 +1,9 @@
 """moe_forward_noalloc: the layer forward for callers that cannot allocate
 device memory (no workspace argument; the library's built-in device scratch
 is used instead).  Its results must match moe_forward with a caller
-workspace.  This file is collected last so a stop-at-first-failure run has
-already run every other test; it builds everything it needs itself, so it also
-passes alone in a fresh process."""
+workspace.  This file is collected after the parity files so a
+stop-at-first-failure run has already run them; it builds everything it needs
+itself, so it also passes alone in a fresh process."""
 import ctypes
 
 import numpy as np
