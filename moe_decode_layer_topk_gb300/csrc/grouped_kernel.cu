@@ -3,9 +3,9 @@
 // Same mathematics as the decode kernel (forward chain of forward_k3.rs:
 // router GEMV -> top-k -> expert gate+up -> SiLU -> down -> weighted sum),
 // organised as per-expert token groups so that each routed expert's weights
-// are streamed once for all of its tokens ("grouped GEMM (more than 64
-// rows)", forward_batched.rs) and the contractions run on the tcgen05 tensor
-// cores.  Stream-ordered launches:
+// are streamed once for all of its tokens (the grouped GEMM that
+// forward_batched.rs switches to for larger row counts) and the contractions
+// run on the tcgen05 tensor cores.  Stream-ordered launches:
 //
 //   router    logits[n,e] (FP32, CUDA cores)
 //   top-k     warp top-k per token; per-token power-of-two exponent of x
