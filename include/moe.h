@@ -101,7 +101,9 @@ typedef enum {
   MOE_ERR_UNSUPPORTED = 2,          /* shape/format outside what the kernels take */
   MOE_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes < moe_workspace_size(desc, N) */
   MOE_ERR_CUDA = 4,                 /* a CUDA runtime call failed */
-  MOE_ERR_TIMEOUT = 5               /* a bounded device-side wait gave up */
+  MOE_ERR_TIMEOUT = 5,              /* a bounded device-side wait gave up */
+  MOE_ERR_RANGE = 6                 /* an activation held as f16 exceeded +-65504 and was
+                                       saturated (the result is not reliable) */
 } moe_status_t;
 
 typedef enum {
@@ -239,9 +241,14 @@ MOE_API moe_status_t moe_forward_host(const moe_layer_desc_t* desc, const moe_we
                               const void* x_host, int32_t N, void* out_host,
                               void* workspace, size_t ws_bytes, void* stream);
 
-/* Sticky device-side error of a workspace (MOE_OK or MOE_ERR_TIMEOUT).
+/* Sticky device-side error of a workspace: MOE_OK, MOE_ERR_TIMEOUT (a bounded
+ * wait expired; re-initialise the workspace), or MOE_ERR_RANGE (the fused
+ * decode kernel holds the routed experts' SiLU(g)*u, times the routing weight
+ * and the down scale2, as f16; a value beyond +-65504 was saturated).
  * Enqueues a 4-byte read on `stream`, synchronises the stream, clears the
- * word, and returns the status of the calls that ran since the last check. */
+ * word, and returns the status of the calls that ran since the last check.
+ * workspace == NULL reads the built-in scratch of moe_forward_noalloc on the
+ * current device. */
 MOE_API moe_status_t moe_get_error(void* workspace, void* stream);
 
 /* Static description of a status code. */
@@ -261,17 +268,20 @@ MOE_API int32_t moe_abi_version(void);
  * It calls no cudaMalloc, cudaFree or allocating library routine.
  *   - A shape whose moe_workspace_size(desc, N) exceeds 8 MiB is refused with
  *     MOE_ERR_WORKSPACE_TOO_SMALL; use moe_forward with a caller workspace.
- *   - The first call on a device looks up the array's device address with
- *     cudaGetSymbolAddress (once per device, with that device current); make
- *     that first call before any stream capture.
+ *   - The first call on a device (and the first after the current CUDA
+ *     context changed, e.g. after cudaDeviceReset) looks up the array's device
+ *     address with cudaGetSymbolAddress, with that device current; make that
+ *     first call before any stream capture.
  *   - Every call on a device shares the one array and it keeps the last call's
- *     contents; each call clears its control words (an async memset on
- *     `stream`) and the kernel zeroes its accumulator, so nothing carries over
- *     between calls that run one after another.  Calls that overlap on the GPU
- *     (different streams, no ordering between them) race on the array: order
- *     them on one stream.
- *   - Device-side wait timeouts are not reported for this variant (there is no
- *     caller workspace to hand to moe_get_error).
+ *     contents; each call, once its arguments have passed every check,
+ *     restarts the array's call counter and tagged router logits (async
+ *     memsets on `stream`), and the kernels clear their own accumulators, so
+ *     nothing carries over between calls that run one after another.  Calls
+ *     that overlap on the GPU (different streams, no ordering between them)
+ *     race on the array: order them on one stream.
+ *   - Device-side errors stay in the array's sticky error word until read:
+ *     moe_get_error(NULL, stream) reports and clears them for the current
+ *     device.
  * The pages have no counterpart of this entry point; it exists for callers
  * that cannot allocate. */
 MOE_API moe_status_t moe_forward_noalloc(const moe_layer_desc_t* desc,

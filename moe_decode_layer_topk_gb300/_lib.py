@@ -13,7 +13,7 @@ from typing import Optional
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
-ABI_VERSION = 2
+ABI_VERSION = 3
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = 1
@@ -21,6 +21,7 @@ MOE_ERR_UNSUPPORTED = 2
 MOE_ERR_WORKSPACE_TOO_SMALL = 3
 MOE_ERR_CUDA = 4
 MOE_ERR_TIMEOUT = 5
+MOE_ERR_RANGE = 6
 MOE_SCORE_SOFTMAX = 0
 MOE_SCORE_SIGMOID_BIAS = 1
 MOE_SCORE_SOFTMAX_BIAS = 2

@@ -13,7 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmoe.so")
-SOURCES = ["moe_api.cu", "decode_kernel.cu", "grouped_kernel.cu"]
+SOURCES = ["moe_api.cu", "decode_kernel.cu", "grouped_kernel.cu", "stream_kernel.cu"]
 HEADERS = ["moe_internal.h", "ptx.cuh", "routing.cuh", "tc.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

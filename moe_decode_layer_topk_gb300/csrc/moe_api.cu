@@ -19,12 +19,65 @@
 
 namespace {
 
-constexpr int32_t kAbiVersion = 2;
+constexpr int32_t kAbiVersion = 3;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The stream kernel's cross-CTA words (router logits, the routed
+// intermediate h, shared-expert readiness flags and part counters) are 64-bit
+// words tagged with the call number,
+// in a region right after the control block that no other path writes and
+// that the stream kernel writes only with such words, so no stale word can
+// look current whatever shapes ran before.  Its layout depends on the layer
+// alone (sized for kSkMaxTok rows), not on N.
+struct TaggedLayout {
+  size_t logits, hw, sflag, scnt, total;
+};
+
+TaggedLayout tagged_layout(const moe_layer_desc_t& d) {
+  TaggedLayout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, kAlign);
+    return o;
+  };
+  const size_t Ts = (size_t)std::max(d.shared_inter, 0) / 16;
+  L.logits = take((size_t)moe::kSkMaxTok * (d.E + d.zero_experts) * 8);
+  L.hw = take((size_t)moe::kSkMaxTok * d.top_k * (d.inter / 2) * 8);
+  L.sflag = take(Ts * 8);
+  L.scnt = take(Ts * 8);
+  L.total = off;
+  return L;
+}
+
+size_t tagged_bytes(const moe_layer_desc_t& d) { return tagged_layout(d).total; }
+
+// Workspace of the stream kernel (FP4 experts, N <= kSkMaxTok).
+struct SWsLayout {
+  size_t ctrl, tagged, hs, shpart, total;
+};
+
+SWsLayout sws_layout(const moe_layer_desc_t& d, int32_t N) {
+  SWsLayout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, kAlign);
+    return o;
+  };
+  const size_t Ts = (size_t)std::max(d.shared_inter, 0) / 16;
+  L.ctrl = take(256);
+  L.tagged = take(tagged_bytes(d));
+  L.hs = take((size_t)N * std::max(d.shared_inter, 0) * 2);
+  // K parts x tiles <= the grid (at most kSkMaxGrid CTAs)
+  L.shpart = take(Ts ? (size_t)std::max<size_t>(Ts, moe::kSkMaxGrid) * 256 * 4 : 0);
+  L.total = off;
+  return L;
+}
 
 struct WsLayout {
   size_t ctrl, logits, x16, xexp, gsig, h16, hexp, hs, ready, total;
@@ -39,6 +92,7 @@ WsLayout ws_layout(const moe_layer_desc_t& d, int32_t N) {
     return o;
   };
   L.ctrl = take(256);
+  take(tagged_bytes(d));
   L.logits = take((size_t)N * (d.E + d.zero_experts) * 4);
   L.x16 = take((size_t)N * d.H * 2);
   L.xexp = take((size_t)N * 4);
@@ -70,6 +124,7 @@ GWsLayout gws_layout(const moe_layer_desc_t& d, int32_t N) {
   const size_t S = (size_t)N * d.top_k;
   const size_t T = S / moe::kGTileTok + std::min((size_t)d.E, S) + 1;   // token tiles, bound
   L.ctrl = take(256);
+  take(tagged_bytes(d));
   L.logits = take((size_t)N * d.E * 4);
   L.xexp = take((size_t)N * 4);
   L.sel_e = take(S * 4);
@@ -119,6 +174,7 @@ size_t ws_total(const moe_layer_desc_t& d, int32_t max_tokens) {
   const int32_t ndec = std::min(max_tokens, (int32_t)(moe::kMaxSlots / d.top_k));
   size_t t = ndec >= 1 ? ws_layout(d, ndec).total : 0;
   if (grouped_path(d, max_tokens)) t = std::max(t, gws_layout(d, max_tokens).total);
+  t = std::max(t, sws_layout(d, std::min(max_tokens, (int32_t)moe::kSkMaxTok)).total);
   return t;
 }
 
@@ -188,6 +244,7 @@ moe_status_t device_info(int* budget, int* grid) {
     di.grid = moe::decode_grid(dev, di.budget);
     if (di.grid <= 0) return MOE_ERR_CUDA;
     if (moe::grouped_set_smem(di.budget + 1024) != cudaSuccess) return MOE_ERR_CUDA;
+    if (moe::stream_set_smem(di.budget) != cudaSuccess) return MOE_ERR_CUDA;
     di.ready = true;
   }
   *budget = di.budget;
@@ -322,9 +379,10 @@ bool encode_scales(moe::Params& p, int slot, const void* ptr, const moe::Geo& g,
 
 // Grouped path: router/top-k, plan, gather, gate/up GEMM, pack, down GEMM,
 // combine (grouped_kernel.cu).  Arguments are already checked.
+template <class Head>
 moe_status_t run_grouped(const moe_layer_desc_t* d, const moe_weights_t* w, const void* x,
                          int32_t N, void* out, int32_t* topk_idx, float* topk_w, void* ws,
-                         size_t ws_bytes, void* stream, int route_only) {
+                         size_t ws_bytes, void* stream, int route_only, Head head) {
   if (d->shared_inter > 0) return MOE_ERR_UNSUPPORTED;   // shared expert: decode sizes only
   if (d->wfmt == MOE_W_BF16 || d->wfmt == MOE_W_FP8)
     return MOE_ERR_UNSUPPORTED;   // BF16 / FP8 experts: decode sizes only
@@ -421,15 +479,76 @@ moe_status_t run_grouped(const moe_layer_desc_t* d, const moe_weights_t* w, cons
               encode_2d(&gd.tmB, gp.h16, (uint64_t)d->inter * 2, S, 128, 128, 64);
     if (!ok) return MOE_ERR_CUDA;
   }
+  st = head();
+  if (st != MOE_OK) return st;
   if (moe::launch_grouped(gp, gu, gd, grid, smem_gu, smem_gd,
                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
+// Layers the stream kernel takes: FP4 experts, BF16 router, no zero experts,
+// no hash routing; up to kSkMaxTok rows.
+bool stream_capable(const moe_layer_desc_t& d, int32_t N) {
+  return (d.wfmt == MOE_W_NVFP4 || d.wfmt == MOE_W_MXFP4) && d.router_fmt == MOE_R_BF16 &&
+         d.zero_experts == 0 && d.hash_vocab == 0 && N >= 1 && N <= moe::kSkMaxTok;
+}
+
+// Fills the stream kernel's parameters; false if the shape does not fit it.
+bool stream_params(moe::StreamParams& p, const moe_layer_desc_t* d, const moe_weights_t* w,
+                   const void* x, int32_t N, void* out, int32_t* topk_idx, float* topk_w,
+                   void* ws, int route_only, int budget, int grid) {
+  memset(&p, 0, sizeof(p));
+  p.H = d->H;
+  p.inter = d->inter;
+  p.E = d->E;
+  p.k = d->top_k;
+  p.scoring = d->scoring;
+  p.norm = d->norm_topk_prob ? 1 : 0;
+  p.rsf = d->routed_scaling_factor;
+  p.fmt = d->wfmt;
+  p.N = N;
+  p.Is = d->shared_inter;
+  p.route_only = route_only;
+  p.router = static_cast<const uint16_t*>(w->router);
+  p.bias = d->scoring != MOE_SCORE_SOFTMAX ? w->bias : nullptr;
+  p.gq = w->gate_q;
+  p.uq = w->up_q;
+  p.dq = w->down_q;
+  p.gsc = w->gate_s;
+  p.usc = w->up_s;
+  p.dsc = w->down_s;
+  p.g2 = w->gate_s2;
+  p.u2 = w->up_s2;
+  p.d2 = w->down_s2;
+  if (d->shared_inter > 0) {
+    p.shg = static_cast<const uint16_t*>(w->sh_gate);
+    p.shu = static_cast<const uint16_t*>(w->sh_up);
+    p.shd = static_cast<const uint16_t*>(w->sh_down);
+    p.shw = static_cast<const uint16_t*>(w->sh_gate_w);
+  }
+  p.x = static_cast<const uint16_t*>(x);
+  p.out = static_cast<uint16_t*>(out);
+  p.topk_idx = topk_idx;
+  p.topk_w = topk_w;
+  const SWsLayout L = sws_layout(*d, N);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  p.ctrl = reinterpret_cast<moe::Ctrl*>(b + L.ctrl);
+  const TaggedLayout T = tagged_layout(*d);
+  p.logits = reinterpret_cast<unsigned long long*>(b + L.tagged + T.logits);
+  p.hw = reinterpret_cast<unsigned long long*>(b + L.tagged + T.hw);
+  p.sflag = reinterpret_cast<unsigned long long*>(b + L.tagged + T.sflag);
+  p.scnt = reinterpret_cast<unsigned long long*>(b + L.tagged + T.scnt);
+  p.hs = reinterpret_cast<uint16_t*>(b + L.hs);
+  p.shpart = reinterpret_cast<float*>(b + L.shpart);
+  p.timeout_ns = g_timeout_ns;
+  return moe::plan_stream(p, budget, grid);
+}
+
 moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* x, int32_t N,
                  void* out, int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
-                 void* stream, int route_only, const int32_t* token_ids = nullptr) {
+                 void* stream, int route_only, const int32_t* token_ids = nullptr,
+                 bool clear_head = false) {
   moe_status_t st = check_desc(d);
   if (st != MOE_OK) return st;
   st = check_weights(d, w);
@@ -440,8 +559,33 @@ moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* 
   if (!x || !aligned16(x) || !ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
   if (!route_only && (!out || !aligned16(out))) return MOE_ERR_INVALID_ARG;
   if (route_only && (!topk_idx || !topk_w)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < ws_total(*d, N)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  // clear_head: the built-in scratch of moe_forward_noalloc restarts its
+  // call counter and tagged logits each call, once every check has passed
+  auto head = [&]() -> moe_status_t {
+    if (!clear_head) return MOE_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;   // call counters
+    if (cudaMemsetAsync(static_cast<uint8_t*>(ws) + 256, 0, tagged_bytes(*d), s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  };
   if (grouped_path(*d, N))
-    return run_grouped(d, w, x, N, out, topk_idx, topk_w, ws, ws_bytes, stream, route_only);
+    return run_grouped(d, w, x, N, out, topk_idx, topk_w, ws, ws_bytes, stream, route_only, head);
+  if (stream_capable(*d, N)) {
+    if (ws_bytes < sws_layout(*d, N).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    int budget = 0, grid = 0;
+    moe_status_t st2 = device_info(&budget, &grid);
+    if (st2 != MOE_OK) return st2;
+    moe::StreamParams sp;
+    if (stream_params(sp, d, w, x, N, out, topk_idx, topk_w, ws, route_only, budget, grid)) {
+      st2 = head();
+      if (st2 != MOE_OK) return st2;
+      if (moe::launch_stream(sp, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      return MOE_OK;
+    }
+  }
   const WsLayout L = ws_layout(*d, N);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
 
@@ -514,6 +658,8 @@ moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* 
            encode_rows(p, moe::TM_SD, w->sh_down, p.geo[moe::KIND_BS], (uint64_t)d->H);
     if (!ok) return MOE_ERR_CUDA;
   }
+  st = head();
+  if (st != MOE_OK) return st;
   if (moe::launch_decode(p, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
@@ -532,18 +678,40 @@ constexpr size_t kNoAllocScratchBytes = 8u << 20;   // 8 MiB
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[64] = {nullptr};
+// The address is looked up once per (device, CUDA context): a reset device or
+// another context current on the device gets its own lookup.
+struct NoallocEntry {
+  CUcontext ctx;
+  void* ptr;
+};
+NoallocEntry g_noalloc[64] = {};
+PFN_cuCtxGetCurrent_v4000 g_ctx_get = nullptr;
 
 moe_status_t noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  // make the runtime's context current for this thread before reading it
+  if (cudaFree(nullptr) != cudaSuccess) return MOE_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  if (!g_ctx_get) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return MOE_ERR_CUDA;
+    g_ctx_get = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  }
+  CUcontext ctx = nullptr;
+  if (g_ctx_get(&ctx) != CUDA_SUCCESS || !ctx) return MOE_ERR_CUDA;
+  NoallocEntry& en = g_noalloc[dev];
+  if (!en.ptr || en.ctx != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-    g_noalloc_ptr[dev] = p;
+    en.ptr = p;
+    en.ctx = ctx;
   }
-  *out = g_noalloc_ptr[dev];
+  *out = en.ptr;
   return MOE_OK;
 }
 
@@ -619,7 +787,10 @@ moe_status_t moe_forward_host(const moe_layer_desc_t* desc, const moe_weights_t*
 }
 
 moe_status_t moe_get_error(void* workspace, void* stream) {
-  if (!workspace) return MOE_ERR_INVALID_ARG;
+  if (!workspace) {   // the built-in scratch of moe_forward_noalloc on this device
+    const moe_status_t st = noalloc_scratch(&workspace);
+    if (st != MOE_OK) return st;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint32_t word = 0;
   uint32_t* err = &static_cast<moe::Ctrl*>(workspace)->error;
@@ -629,7 +800,7 @@ moe_status_t moe_get_error(void* workspace, void* stream) {
   if (word == 0) return MOE_OK;
   if (cudaMemsetAsync(err, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
-  return MOE_ERR_TIMEOUT;
+  return (word & ~moe::kErrRange) ? MOE_ERR_TIMEOUT : MOE_ERR_RANGE;
 }
 
 const char* moe_status_string(moe_status_t status) {
@@ -640,6 +811,7 @@ const char* moe_status_string(moe_status_t status) {
     case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than moe_workspace_size()";
     case MOE_ERR_CUDA: return "CUDA runtime error";
     case MOE_ERR_TIMEOUT: return "a bounded device-side wait expired";
+    case MOE_ERR_RANGE: return "an expert activation exceeded the f16 range and was saturated";
   }
   return "unknown status";
 }
@@ -661,11 +833,11 @@ moe_status_t moe_forward_noalloc(const moe_layer_desc_t* desc, const moe_weights
   void* ws = nullptr;
   st = noalloc_scratch(&ws);
   if (st != MOE_OK) return st;
-  // the control block (grid-barrier words, error word) must start at zero;
-  // the kernel itself zeroes its accumulator and counters every call
-  if (cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  return run(desc, weights, x, N, out, topk_idx, topk_w, ws, kNoAllocScratchBytes, stream, 0);
+  // the call counter and the tagged logits restart every call (enqueued by
+  // run() once every check has passed); the kernels zero their own
+  // accumulators and counters, and the error word stays sticky
+  return run(desc, weights, x, N, out, topk_idx, topk_w, ws, kNoAllocScratchBytes, stream, 0,
+             nullptr, true);
 }
 
 /* Test hook: budget of every bounded device wait, in nanoseconds, for calls

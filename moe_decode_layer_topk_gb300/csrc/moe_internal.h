@@ -54,9 +54,11 @@ constexpr uint32_t kErrTimeoutProducer = 4u;
 // Workspace control block (first 256 bytes of the workspace).
 struct Ctrl {
   unsigned long long arrivals;   // grid-barrier arrivals, monotonic (1 per CTA per call)
+  unsigned long long calls;      // stream-kernel call counter: + 256 per call (tag = calls / 256)
   uint32_t error;                // sticky error bits
-  uint32_t pad[61];
+  uint32_t pad[59];
 };
+static_assert(sizeof(Ctrl) == 256, "control block is the first 256 bytes of a workspace");
 
 // Stage geometry of one kind of row group (see decode_kernel.cu).
 struct Geo {
@@ -126,6 +128,66 @@ struct Params {
   int nrb, nrb_cta;  // down blocks (H/16) and at most this many per CTA
   unsigned long long timeout_ns;
 };
+
+// ------------------------------------------------------------ stream kernel
+// Fused forward for up to kSkMaxTok token rows with FP4 routed experts
+// (stream_kernel.cu): every lane streams its own 16-byte pieces of the
+// touched experts' rows with cp.async into a per-warp shared-memory ring,
+// dequantises them in registers and runs the dot products as m16n8k16
+// tensor-core MMAs with the token rows as the 8 MMA columns.
+constexpr int kSkWarps = 16;
+constexpr int kSkThreads = kSkWarps * 32;
+constexpr int kSkMaxTok = 8;       // MMA N: every token of a call is one column
+constexpr int kSkMaxStages = 8;    // cp.async ring depth per warp
+constexpr int kSkMaxMt = 4;        // 16-row output tiles a CTA may own in the down phase
+constexpr int kSkSplitSlots = 16;  // gate/up tiles shared by several warps of one CTA
+constexpr int kSkStageCodes = 4 * 32 * 16;   // bytes per warp and stage: 4 pieces of 16 B per lane
+constexpr int kSkStageAux = 32 * 16;     // 16 B per lane: block-scale words or a B piece
+constexpr int kSkMaxGrid = 256;   // CTAs; bounds the shared-expert K-part slots
+constexpr uint32_t kErrRange = 8u;       // an activation left the f16 range
+
+struct StreamParams {
+  // layer
+  int H, inter, E, k, scoring, norm, fmt, N, Is, route_only;
+  float rsf;
+  // weights (device)
+  const uint16_t* router;            // bf16 [E, H]
+  const float* bias;                 // [E] or null
+  const uint8_t *gq, *uq, *dq;       // E2M1 codes [E, rows, K/2]
+  const uint8_t *gsc, *usc, *dsc;    // block scales [E, rows, K/gs]
+  const float *g2, *u2, *d2;         // per-expert scale2 or null
+  const uint16_t *shg, *shu, *shd;   // shared expert, bf16 (null if Is == 0)
+  const uint16_t* shw;               // shared-expert gate vector [H] or null
+  // activations / outputs (device)
+  const uint16_t* x;
+  uint16_t* out;
+  int32_t* topk_idx;
+  float* topk_w;
+  // workspace (device)
+  Ctrl* ctrl;
+  // Words whose upper half is a call tag, in a region that only this kernel
+  // writes and only with 64-bit words of that form, so a word left by an
+  // earlier call (of any shape) never carries the current tag.
+  unsigned long long* logits;   // [N, E]: (call tag << 32) | f32 bits
+  unsigned long long* hw;       // [N*k, inter/2]: (call tag << 32) | two f16 of
+                                //   w * scale2 * SiLU(g) * u per slot (elements 2i, 2i+1)
+  unsigned long long* sflag;    // [Is/16] call tag << 32 once a shared tile is published
+  unsigned long long* scnt;     // [Is/16] (call tag << 32) | K-parts of a shared tile finished
+  // plain data, read only after its flag or counter says it is current
+  uint16_t* hs;                 // [N, Is] bf16 of gate * SiLU(g) * u (shared expert)
+  float* shpart;                // [Is/16, sh_parts, 256] K-part partial sums of shared tiles
+  // geometry
+  int stages;                   // cp.async ring depth
+  int sh_parts;                 // K-parts of one shared gate/up tile
+  int off_ring, off_aux, off_x16, off_tab, off_split, off_oacc, smem_bytes;
+  unsigned long long timeout_ns;
+};
+
+// Layers and token counts the stream kernel runs; fills the shared-memory
+// layout.  False if the shape is outside what it takes.
+bool plan_stream(StreamParams& p, int smem_budget, int grid);
+cudaError_t launch_stream(const StreamParams& p, int grid, cudaStream_t stream);
+cudaError_t stream_set_smem(int smem_bytes);
 
 // ------------------------------------------------------------ grouped path
 // Many-token forward (N * top_k beyond kMaxSlots, or from 128 for large FP4

@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for st in range(6):
+    for st in range(7):
         assert _lib.moe_status_string(st)
     assert "unknown" in _lib.moe_status_string(99)
 

@@ -36,32 +36,69 @@ def test_noalloc_refuses_shapes_beyond_its_scratch(lib):
     assert st == _lib.MOE_ERR_WORKSPACE_TOO_SMALL
 
 
+def _spec(**kw):
+    base = dict(synth.CONFIGS["tiny"].__dict__)
+    base.update(pool=64, **kw)
+    return synth.LayerSpec(**base)
+
+
+def _compare_call(spec, host, dev, N, seed, what):
+    """One moe_forward_noalloc call against moe_forward on a fresh caller
+    workspace (same routing bit for bit, outputs within the tolerance) and
+    against the FP64 oracle."""
+    import torch
+    from moe_decode_layer_topk_gb300.device import bf16_tensor, workspace
+    from oracle import compare, margin, oracle
+
+    xb = margin.tokens_with_margin(host, N, seed=seed)
+    x = bf16_tensor(xb)
+    ref_out = torch.empty_like(x)
+    ref_idx = torch.empty((N, spec.top_k), dtype=torch.int32, device="cuda")
+    ref_w = torch.empty((N, spec.top_k), dtype=torch.float32, device="cuda")
+    ws = workspace(spec, N)
+    _lib.moe_forward(dev.desc, dev.weights, x, ref_out, ws, ref_idx, ref_w)
+    out = torch.full_like(x, float("nan"))
+    idx = torch.full((N, spec.top_k), -1, dtype=torch.int32, device="cuda")
+    w = torch.full((N, spec.top_k), float("nan"), dtype=torch.float32, device="cuda")
+    _lib.moe_forward_noalloc(dev.desc, dev.weights, x, out, idx, w)
+    torch.cuda.synchronize()
+    assert _lib.moe_get_error(ws) == _lib.MOE_OK
+    assert _lib.moe_get_error(None) == _lib.MOE_OK      # the built-in scratch's error word
+    assert torch.equal(idx, ref_idx), what
+    torch.testing.assert_close(w, ref_w, rtol=1e-6, atol=1e-7)
+    bits = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = compare.bf16_bits_to_f64(ref_out.view(torch.int16).cpu().numpy().view(np.uint16))
+    compare.check_output(bits, ref, what=f"{what} vs moe_forward")
+    orc = oracle.moe_forward(host, xb)
+    compare.check_routing(idx.cpu().numpy(), w.cpu().numpy(), orc["idx"], orc["w"],
+                          margin.selection_keys(host, xb))
+    compare.check_output(bits, orc["out_f64"], what=f"{what} vs oracle")
+
+
 @pytest.mark.gpu
 def test_noalloc_matches_moe_forward_on_two_calls_in_a_row(lib):
-    import torch
-    from moe_decode_layer_topk_gb300.device import DeviceLayer, bf16_tensor, workspace
-    from oracle import compare
+    from moe_decode_layer_topk_gb300.device import DeviceLayer
 
-    base = dict(synth.CONFIGS["tiny"].__dict__)
-    base.update(name="noalloc", H=512, inter=256, E=16, top_k=4, shared_inter=128,
-                shared_gated=True, pool=64)
-    spec = synth.LayerSpec(**base)
-    dev = DeviceLayer.upload(synth.make_layer(spec, seed=4242))
+    spec = _spec(name="noalloc", H=512, inter=256, E=16, top_k=4, shared_inter=128,
+                 shared_gated=True)
+    host = synth.make_layer(spec, seed=4242)
+    dev = DeviceLayer.upload(host)
     for call, N in enumerate((4, 3)):           # two calls in a row, different batches
-        x = bf16_tensor(synth.make_tokens(spec, N, seed=5000 + call))
-        ref_out = torch.empty_like(x)
-        ref_idx = torch.empty((N, spec.top_k), dtype=torch.int32, device="cuda")
-        ref_w = torch.empty((N, spec.top_k), dtype=torch.float32, device="cuda")
-        ws = workspace(spec, N)
-        _lib.moe_forward(dev.desc, dev.weights, x, ref_out, ws, ref_idx, ref_w)
-        out = torch.full_like(x, float("nan"))
-        idx = torch.full((N, spec.top_k), -1, dtype=torch.int32, device="cuda")
-        w = torch.full((N, spec.top_k), float("nan"), dtype=torch.float32, device="cuda")
-        _lib.moe_forward_noalloc(dev.desc, dev.weights, x, out, idx, w)
-        torch.cuda.synchronize()
-        assert _lib.moe_get_error(ws) == _lib.MOE_OK
-        assert torch.equal(idx, ref_idx)
-        torch.testing.assert_close(w, ref_w, rtol=1e-6, atol=1e-7)
-        ref = compare.bf16_bits_to_f64(ref_out.view(torch.int16).cpu().numpy().view(np.uint16))
-        compare.check_output(out.view(torch.int16).cpu().numpy().view(np.uint16), ref,
-                             what=f"noalloc call {call}")
+        _compare_call(spec, host, dev, N, 5000 + call, f"noalloc call {call}")
+
+
+@pytest.mark.gpu
+def test_noalloc_switches_between_the_paths_in_one_array(lib):
+    """The one built-in array serves the grouped path (N*k > 256), the
+    fused kernel for up to 8 rows and the fused kernel for more rows, one call
+    after another; stale state of one layout must not leak into the next."""
+    from moe_decode_layer_topk_gb300.device import DeviceLayer
+
+    spec = _spec(name="noalloc_paths", H=256, inter=128, E=16, top_k=8)
+    host = synth.make_layer(spec, seed=4343)
+    dev = DeviceLayer.upload(host)
+    d = dev.desc
+    assert _lib.moe_uses_grouped_path(d, 40) == 1 and _lib.moe_uses_grouped_path(d, 3) == 0
+    assert _lib.moe_workspace_size(d, 40) < 8 << 20
+    for call, N in enumerate((40, 3, 12, 2, 40)):
+        _compare_call(spec, host, dev, N, 5100 + call, f"noalloc path call {call} (N={N})")
