@@ -58,7 +58,7 @@ size_t tagged_bytes(const moe_layer_desc_t& d) { return tagged_layout(d).total; 
 
 // Workspace of the stream kernel (FP4 experts, N <= kSkMaxTok).
 struct SWsLayout {
-  size_t ctrl, tagged, hs, shpart, total;
+  size_t ctrl, tagged, hs, shpart, oacc, total;
 };
 
 SWsLayout sws_layout(const moe_layer_desc_t& d, int32_t N) {
@@ -75,6 +75,7 @@ SWsLayout sws_layout(const moe_layer_desc_t& d, int32_t N) {
   L.hs = take((size_t)N * std::max(d.shared_inter, 0) * 2);
   // K parts x tiles <= the grid (at most kSkMaxGrid CTAs)
   L.shpart = take(Ts ? (size_t)std::max<size_t>(Ts, moe::kSkMaxGrid) * 256 * 4 : 0);
+  L.oacc = take((size_t)d.H * ((N + 1) & ~1) * 4);
   L.total = off;
   return L;
 }
@@ -541,6 +542,7 @@ bool stream_params(moe::StreamParams& p, const moe_layer_desc_t* d, const moe_we
   p.scnt = reinterpret_cast<unsigned long long*>(b + L.tagged + T.scnt);
   p.hs = reinterpret_cast<uint16_t*>(b + L.hs);
   p.shpart = reinterpret_cast<float*>(b + L.shpart);
+  p.oacc = reinterpret_cast<float*>(b + L.oacc);
   p.timeout_ns = g_timeout_ns;
   return moe::plan_stream(p, budget, grid);
 }
@@ -565,7 +567,7 @@ moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* 
   auto head = [&]() -> moe_status_t {
     if (!clear_head) return MOE_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(ws, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;   // call counters
+    if (cudaMemsetAsync(ws, 0, 24, s) != cudaSuccess) return MOE_ERR_CUDA;   // call counters
     if (cudaMemsetAsync(static_cast<uint8_t*>(ws) + 256, 0, tagged_bytes(*d), s) != cudaSuccess)
       return MOE_ERR_CUDA;
     return MOE_OK;

@@ -55,8 +55,9 @@ constexpr uint32_t kErrTimeoutProducer = 4u;
 struct Ctrl {
   unsigned long long arrivals;   // grid-barrier arrivals, monotonic (1 per CTA per call)
   unsigned long long calls;      // stream-kernel call counter: + 256 per call (tag = calls / 256)
+  unsigned long long fin;        // stream-kernel end counter: + 256 per call
   uint32_t error;                // sticky error bits
-  uint32_t pad[59];
+  uint32_t pad[57];
 };
 static_assert(sizeof(Ctrl) == 256, "control block is the first 256 bytes of a workspace");
 
@@ -139,7 +140,6 @@ constexpr int kSkWarps = 16;
 constexpr int kSkThreads = kSkWarps * 32;
 constexpr int kSkMaxTok = 8;       // MMA N: every token of a call is one column
 constexpr int kSkMaxStages = 8;    // cp.async ring depth per warp
-constexpr int kSkMaxMt = 4;        // 16-row output tiles a CTA may own in the down phase
 constexpr int kSkSplitSlots = 16;  // gate/up tiles shared by several warps of one CTA
 constexpr int kSkStageCodes = 4 * 32 * 16;   // bytes per warp and stage: 4 pieces of 16 B per lane
 constexpr int kSkStageAux = 32 * 16;     // 16 B per lane: block-scale words or a B piece
@@ -176,10 +176,11 @@ struct StreamParams {
   // plain data, read only after its flag or counter says it is current
   uint16_t* hs;                 // [N, Is] bf16 of gate * SiLU(g) * u (shared expert)
   float* shpart;                // [Is/16, sh_parts, 256] K-part partial sums of shared tiles
+  float* oacc;                  // [H, N rounded up to even] FP32 output accumulator (zeroed each call)
   // geometry
   int stages;                   // cp.async ring depth
   int sh_parts;                 // K-parts of one shared gate/up tile
-  int off_ring, off_aux, off_x16, off_tab, off_split, off_oacc, smem_bytes;
+  int off_ring, off_aux, off_x16, off_tab, off_split, smem_bytes;
   unsigned long long timeout_ns;
 };
 

@@ -45,9 +45,7 @@
 // ring of `stages` stages, plus a 16-byte side slot (the two 4-byte words
 // holding its block scales, or its piece of the B operand), so the bytes in
 // flight are bounded by shared memory, not registers, and each lane reads
-// back only what it copied.  Weight copies carry an L2 evict-first policy:
-// they are read once per call and should not push the code, x, the logits
-// and h out of L2.
+// back only what it copied.
 //
 // Arithmetic: E2M1 -> f16 by cvt, times the E4M3 block scale (exact in f16:
 // at most 6 significant bits, range 2^-10 .. 2688), or for MXFP4 times
@@ -69,9 +67,7 @@ namespace {
 
 constexpr int kW = kSkWarps;
 constexpr int kT = kSkThreads;
-constexpr int kRouterPart = 2048;     // router elements per warp part (8 x 16 B per lane)
 constexpr int kMaxRouterRows = 8;     // router rows per CTA (E <= 1024, G >= 128)
-constexpr int kMaxRouterParts = 16;
 
 struct SkTab {
   int U;
@@ -89,7 +85,6 @@ struct SkTab {
   uint32_t u_mask[kMaxSlots];
   float u_w[kMaxSlots][kSkMaxTok];
   int16_t u_slot[kMaxSlots][kSkMaxTok];
-  float rpart[kMaxRouterRows * kMaxRouterParts * kSkMaxTok];
   uint32_t split_cnt[kSkSplitSlots];
   float part[kSkMaxTok][8][2];   // per token and 128-expert part: max, sum exp(l - max)
   uint32_t xmax[kSkMaxTok];   // max |x| per token (float bits)
@@ -98,21 +93,15 @@ struct SkTab {
 };
 
 // ------------------------------------------------------------------ helpers
-__device__ __forceinline__ uint64_t evict_first_policy() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-// 16-byte weight piece (zero fill past n bytes), L2 evict-first.
-__device__ __forceinline__ void cpa16w(uint32_t dst, const void* src, uint32_t n, uint64_t pol) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint.L2::256B [%0], [%1], 16, %2, %3;" ::"r"(dst),
-               "l"(src), "r"(n), "l"(pol)
+// 16-byte weight piece (zero fill past n bytes) with a 256-byte L2 prefetch
+// (the row's next pieces are other items of the same CTA or its neighbours).
+__device__ __forceinline__ void cpa16w(uint32_t dst, const void* src, uint32_t n) {
+  asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
                : "memory");
 }
-// 4-byte block-scale word, L2 evict-first.
-__device__ __forceinline__ void cpa4w(uint32_t dst, const void* src, uint32_t n, uint64_t pol) {
-  asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 4, %2, %3;" ::"r"(dst), "l"(src),
-               "r"(n), "l"(pol)
+// 4-byte block-scale word.
+__device__ __forceinline__ void cpa4w(uint32_t dst, const void* src, uint32_t n) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(n)
                : "memory");
 }
 // 16-byte activation piece (x or h), default L2 policy.
@@ -211,6 +200,11 @@ __device__ __noinline__ void set_error(const StreamParams& p, SkTab& tb, uint32_
 
 // Lanes 0..n-1 each wait until *(words[lane]) == tag (bounded, with backoff);
 // then every lane's later reads are ordered after the observed writes.
+__device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ uint32_t ld_acquire_tag(const unsigned long long* p) {
   unsigned long long v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -245,6 +239,16 @@ __device__ __noinline__ void wait_tags(const StreamParams& p, SkTab& tb,
 __device__ __forceinline__ void st_tagged(unsigned long long* p, uint32_t v, uint32_t tag) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p),
                "l"(((unsigned long long)tag << 32) | v)
+               : "memory");
+}
+// Adds a lane's C fragment (rows r, r + 8; columns 2t, 2t+1) to the FP32
+// output accumulator [H][ld] (ld even) at o = row r, column 2t: two vector
+// reductions, fire and forget.
+__device__ __forceinline__ void red_out(float* o, int ld, const float (&c)[4]) {
+  asm volatile("red.relaxed.gpu.global.add.v2.f32 [%0], {%1, %2};" ::"l"(o), "f"(c[0]), "f"(c[1])
+               : "memory");
+  asm volatile("red.relaxed.gpu.global.add.v2.f32 [%0], {%1, %2};" ::"l"(o + 8 * ld), "f"(c[2]),
+               "f"(c[3])
                : "memory");
 }
 // This lane's 32 h values (16 tagged words from w) as f16 pairs in b, once
@@ -296,34 +300,42 @@ __device__ __forceinline__ uint32_t tagged_count(const StreamParams& p, SkTab& t
 // ---------------------------------------------------- one K segment of MMAs
 // rg / rg8: 32 E2M1 codes of rows g and g+8 (this lane's piece); b: the B
 // fragments of the segment (b[m] = elements 2m, 2m+1 of the lane's piece of
-// token column g).  Accumulates into c (FP32, the m16n8 C fragment).
+// token column g).  seg_scales gives the f16x2 multipliers of the codes
+// (sa* for row g, sb* for row g+8; *0 for piece elements 0-15, *1 for 16-31)
+// and the FP32 factors of the segment's partial sums (fa row g, fb row g+8).
 // NVFP4: s0 / s8 = the piece's two E4M3 block scales (low byte: elements
-// 0-15) of rows g and g+8.  MXFP4: s0 / s8 = the piece's E8M0 byte; the four
-// lanes of a row hold the four 32-element blocks of the segment; each is
-// scaled by 2^(its code - the largest of the four) in f16 and the segment's
-// FP32 result by 2^(largest - 127).
+// 0-15), E2M1 x E4M3 exact in f16, factors 1.  MXFP4: s0 / s8 = the piece's
+// E8M0 byte; the four lanes of a row hold the four 32-element blocks of the
+// segment; each is scaled by 2^(its code - the largest of the four) in f16
+// and the segment's partial by 2^(largest - 127).
 template <int FMT>
-__device__ __forceinline__ void seg_fp4(float (&c)[4], const uint4& rg, const uint4& rg8,
-                                        uint32_t s0, uint32_t s8, const uint32_t (&b)[16]) {
-  uint32_t sa0, sa1, sb0, sb1;
-  int mg = 0, mh = 0;
+__device__ __forceinline__ void seg_scales(uint32_t s0, uint32_t s8, uint32_t& sa0, uint32_t& sa1,
+                                           uint32_t& sb0, uint32_t& sb1, float& fa, float& fb) {
   if (FMT == FMT_NVFP4) {
     const uint32_t fg = e4m3x2_to_f16x2(s0), fh = e4m3x2_to_f16x2(s8);
     sa0 = dup_lo(fg);
     sa1 = dup_hi(fg);
     sb0 = dup_lo(fh);
     sb1 = dup_hi(fh);
+    fa = fb = 1.f;
   } else {
-    mg = (int)s0;
-    mh = (int)s8;
+    int mg = (int)s0, mh = (int)s8;
     mg = max(mg, __shfl_xor_sync(0xffffffffu, mg, 1));
     mh = max(mh, __shfl_xor_sync(0xffffffffu, mh, 1));
     mg = max(mg, __shfl_xor_sync(0xffffffffu, mg, 2));
     mh = max(mh, __shfl_xor_sync(0xffffffffu, mh, 2));
     sa0 = sa1 = pow2_f16x2((int)s0 - mg);
     sb0 = sb1 = pow2_f16x2((int)s8 - mh);
+    fa = e8m0_to_f32((uint32_t)mg);
+    fb = e8m0_to_f32((uint32_t)mh);
   }
-  float cs[4] = {0.f, 0.f, 0.f, 0.f};
+}
+// The segment's 8 MMA K steps of one row pair: even steps into c0, odd ones
+// into c1 (two accumulator chains; c0 and c1 may be the same array).
+template <int FMT>
+__device__ __forceinline__ void seg_mma(float (&c0)[4], float (&c1)[4], const uint4& rg,
+                                        const uint4& rg8, uint32_t sa0, uint32_t sa1, uint32_t sb0,
+                                        uint32_t sb1, const uint32_t (&b)[16]) {
   const uint32_t wg[4] = {rg.x, rg.y, rg.z, rg.w};
   const uint32_t wh[4] = {rg8.x, rg8.y, rg8.z, rg8.w};
 #pragma unroll
@@ -337,18 +349,8 @@ __device__ __forceinline__ void seg_fp4(float (&c)[4], const uint4& rg, const ui
       const int s = 2 * w + h;
       const uint32_t a[4] = {hmul2(og[2 * h], sa), hmul2(oh[2 * h], sb), hmul2(og[2 * h + 1], sa),
                              hmul2(oh[2 * h + 1], sb)};
-      mma_f16(cs, a, b[2 * s], b[2 * s + 1]);
+      mma_f16(h == 0 ? c0 : c1, a, b[2 * s], b[2 * s + 1]);
     }
-  }
-  if (FMT == FMT_NVFP4) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) c[q] += cs[q];
-  } else {
-    const float fa = e8m0_to_f32((uint32_t)mg), fb = e8m0_to_f32((uint32_t)mh);
-    c[0] = fmaf(cs[0], fa, c[0]);
-    c[1] = fmaf(cs[1], fa, c[1]);
-    c[2] = fmaf(cs[2], fb, c[2]);
-    c[3] = fmaf(cs[3], fb, c[3]);
   }
 }
 
@@ -362,56 +364,70 @@ __device__ __forceinline__ void seg_bf16(float (&c)[4], const uint4& rg, const u
   mma_bf16(c, a1, bv.z, bv.w);
 }
 
-// ------------------------------------------------------------------ P0 / P1
-// f16 copy of x in MMA B-fragment order: piece ((seg*4 + i)*N + n)*4 + t
-// holds x[n][128 seg + 32 t + 8 i .. +8] * 2^-xe[n] (16 bytes); and the
-// shared-expert gate sigmoid(w_s . x_n) (1 without a gate vector).
-__device__ void x_prep(const StreamParams& p, SkTab& tb, uint8_t* smem, int tid) {
-  const int H = p.H, N = p.N;
-  const int S = (H + 127) >> 7;
-  const int pieces = S * 4 * N * 4;
-  // piece idx -> token n and first element k0
-  auto coords = [&](int idx, int& n, int& k0) {
-    int r = idx >> 2;
-    const int rq = divs(r, N);
-    n = r - rq * N;
-    r = rq;
-    k0 = 128 * (r >> 2) + 32 * (idx & 3) + 8 * (r & 3);
-  };
-  // pass 1: each thread loads up to R pieces at once (the first DRAM round
-  // trip of the call) and keeps them; max |x| and w_s . x per token meet in
-  // shared memory (the maxima as non-negative float bits)
-  constexpr int R = 4;
-  uint4 xv[R];
+__device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int idx = tid + kT * r;
-    int n, k0;
-    coords(idx, n, k0);
-    xv[r] = idx < pieces && k0 < H ? ld_nc_u4(p.x + (size_t)n * H + k0) : make_uint4(0u, 0u, 0u, 0u);
-  }
-  __syncthreads();   // the zeroed maxima and sums (and the caller's tables) are visible
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ------------------------------------------------------------------ P0 / P1
+// Piece idx of the f16 fragment copy of x -> token n and first element k0:
+// piece ((seg*4 + i)*N + n)*4 + t holds x[n][128 seg + 32 t + 8 i .. +8].
+__device__ __forceinline__ void x_coords(int idx, int N, int& n, int& k0) {
+  int r = idx >> 2;
+  const int rq = divs(r, N);
+  n = r - rq * N;
+  k0 = 128 * (rq >> 2) + 32 * (idx & 3) + 8 * (rq & 3);
+}
+
+// Copies issued at kernel start (the first DRAM round trip of the call):
+// the raw BF16 x into its fragment slots and this CTA's router rows into the
+// ring (free until the shared expert or the logits use it).
+__device__ void issue_inputs(const StreamParams& p, uint8_t* smem, int c, int G, int nq, int tid) {
+  const int H = p.H, N = p.N;
+  const int pieces = ((H + 127) >> 7) * 16 * N;
+  const uint32_t xs = smem_u32(smem + p.off_x16);
 #pragma unroll 1
   for (int idx = tid; idx < pieces; idx += kT) {
-    const int r = (idx - tid) / kT;
     int n, k0;
-    coords(idx, n, k0);
-    if (k0 >= H) continue;
-    uint4 v;
-    if (r < R) {
-      v = xv[0];
-#pragma unroll
-      for (int q = 1; q < R; ++q)
-        if (r == q) v = xv[q];
-    } else {
-      v = ld_nc_u4(p.x + (size_t)n * H + k0);
-    }
+    x_coords(idx, N, n, k0);
+    const bool in = k0 < H;
+    cpa16(xs + idx * 16, p.x + (in ? (size_t)n * H + k0 : 0), in ? 16u : 0u);
+  }
+  const uint32_t rw = smem_u32(smem + p.off_ring);
+#pragma unroll 1
+  for (int q = 0; q < nq; ++q) {
+    const uint16_t* row = p.router + (size_t)(c + G * q) * H;
+#pragma unroll 1
+    for (int k8 = tid; k8 < (H >> 3); k8 += kT) cpa16(rw + (q * H + 8 * k8) * 2, row + 8 * k8, 16u);
+  }
+  cpa_commit();
+}
+
+// x in fragment order as f16 scaled by 2^-xe[n] (max |x_n| * 2^-xe[n] in
+// [2^14, 2^15): every BF16 value down to 2^-10 of the maximum stays exact),
+// converted in place; and the shared-expert gate sigmoid(w_s . x_n) (1
+// without a gate vector).
+__device__ void x_prep(const StreamParams& p, SkTab& tb, uint8_t* smem, int tid) {
+  const int H = p.H, N = p.N;
+  const int pieces = ((H + 127) >> 7) * 16 * N;
+  uint4* xs = reinterpret_cast<uint4*>(smem + p.off_x16);
+#pragma unroll 1
+  for (int idx = tid; idx < pieces; idx += kT) {
+    int n, k0;
+    x_coords(idx, N, n, k0);
+    const uint4 v = xs[idx];
     const uint32_t xa[4] = {v.x, v.y, v.z, v.w};
     float m = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf_lo(xa[j])), fabsf(bf_hi(xa[j]))));
-    atomicMax(&tb.xmax[n], __float_as_uint(m));
-    if (p.shw) {
+    atomicMax(&tb.xmax[n], __float_as_uint(m));   // non-negative floats order as integers
+    if (p.shw && k0 < H) {
       const uint4 wv = ld_nc_u4(p.shw + k0);
       const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w};
       float d = 0.f;
@@ -425,8 +441,6 @@ __device__ void x_prep(const StreamParams& p, SkTab& tb, uint8_t* smem, int tid)
   }
   __syncthreads();
   if (tid < N) {
-    // max |x| * 2^-e in [2^14, 2^15): every BF16 value down to 2^-10 of the
-    // maximum stays exact in f16
     const float m = __uint_as_float(tb.xmax[tid]);
     const int e = (m > 0.f && isfinite(m)) ? ilog2f(m) - 14 : 0;
     tb.xe[tid] = e;
@@ -434,94 +448,78 @@ __device__ void x_prep(const StreamParams& p, SkTab& tb, uint8_t* smem, int tid)
     tb.gsig[tid] = p.shw ? sigmoid_fast(tb.xdot[tid]) : 1.0f;
   }
   __syncthreads();
-  // pass 2: f16 fragments from the kept pieces
-  uint4* xs = reinterpret_cast<uint4*>(smem + p.off_x16);
 #pragma unroll 1
   for (int idx = tid; idx < pieces; idx += kT) {
-    const int r = (idx - tid) / kT;
     int n, k0;
-    coords(idx, n, k0);
-    uint4 o = make_uint4(0u, 0u, 0u, 0u);
-    if (k0 < H) {
-      uint4 v;
-      if (r < R) {
-        v = xv[0];
+    x_coords(idx, N, n, k0);
+    const uint4 v = xs[idx];
+    const uint32_t xa[4] = {v.x, v.y, v.z, v.w};
+    const float sc = pow2f(-tb.xe[n]);
+    uint32_t h[4];
 #pragma unroll
-        for (int q = 1; q < R; ++q)
-          if (r == q) v = xv[q];
-      } else {
-        v = ld_nc_u4(p.x + (size_t)n * H + k0);
-      }
-      const float sc = pow2f(-tb.xe[n]);
-      const uint32_t xa[4] = {v.x, v.y, v.z, v.w};
-      uint32_t h[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        __half2 hv = __floats2half2_rn(bf_lo(xa[j]) * sc, bf_hi(xa[j]) * sc);
-        h[j] = *reinterpret_cast<uint32_t*>(&hv);
-      }
-      o = make_uint4(h[0], h[1], h[2], h[3]);
+    for (int j = 0; j < 4; ++j) {
+      __half2 hv = __floats2half2_rn(bf_lo(xa[j]) * sc, bf_hi(xa[j]) * sc);
+      h[j] = *reinterpret_cast<uint32_t*>(&hv);
     }
-    xs[idx] = o;
+    xs[idx] = make_uint4(h[0], h[1], h[2], h[3]);
   }
   __syncthreads();
 }
 
-// Router rows of this CTA.  The first part's weight loads were issued before
-// x_prep (wv); the dot products read x from the f16 copy (exact for every
-// BF16 value above 2^-32 of the token's maximum; FP32 accumulation).
-__device__ void router_phase(const StreamParams& p, SkTab& tb, const uint8_t* smem, int c, int G,
-                             int warp, int lane, int tid, uint4 (&wv)[8]) {
+// Router logits of this CTA's rows e = c + G q (q < nq) for the N tokens:
+// FP32 dot products of the BF16 rows (staged in the ring) with the raw BF16 x
+// (in its fragment slots, before x_prep scales it), one warp per (row, token,
+// 256-element block) with a fixed-order sum of the blocks; published as
+// tagged words (tag << 32 | f32 bits).
+__device__ void router_phase(const StreamParams& p, SkTab& tb, uint8_t* smem, int c, int G, int nq,
+                             int warp, int lane, int tid) {
   const int H = p.H, N = p.N, E = p.E;
-  const int nq = c < E ? divs(E - 1 - c, G) + 1 : 0;
-  const int parts = (H + kRouterPart - 1) / kRouterPart;
+  const int nb = (H + 255) >> 8;
   const uint32_t xs = smem_u32(smem + p.off_x16);
-  #pragma unroll 1
-  for (int pr = warp; pr < nq * parts; pr += kW) {
-    const int q = divs(pr, parts), part = pr - q * parts;
-    const int e = c + G * q;
-    const int kb = part * kRouterPart, ke = min(H, kb + kRouterPart);
-    if (pr != warp) {   // later parts of this warp: load now
+  const uint32_t rw = smem_u32(smem + p.off_ring);
+  float* part = reinterpret_cast<float*>(smem + p.off_split);   // [nq * N][nb]
+#pragma unroll 1
+  for (int w = warp; w < nq * N * nb; w += kW) {
+    const int qn = divs(w, nb), b = w - qn * nb;
+    const int q = divs(qn, N), n = qn - q * N;
+    const int k0 = 256 * b + 8 * lane;
+    float a = 0.f;
+    if (k0 < H) {
+      const uint4 wv = lds128(rw + (q * H + k0) * 2);
+      const uint4 xv = lds128(xs + ((((k0 >> 7) * 4 + ((k0 >> 3) & 3)) * N + n) * 4 +
+                                    ((k0 >> 5) & 3)) * 16);
+      const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w};
+      const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int k0 = kb + (lane + 32 * i) * 8;
-        wv[i] = k0 < ke ? ld_nc_u4(p.router + (size_t)e * H + k0) : make_uint4(0u, 0u, 0u, 0u);
+      for (int j = 0; j < 4; ++j) {
+        a = fmaf(bf_lo(wa[j]), bf_lo(xa[j]), a);
+        a = fmaf(bf_hi(wa[j]), bf_hi(xa[j]), a);
       }
     }
-    #pragma unroll 1
-    for (int n = 0; n < N; ++n) {
-      float a = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int k0 = kb + (lane + 32 * i) * 8;
-        if (k0 < ke) {
-          const int seg = k0 >> 7, t = (k0 >> 5) & 3, ii = (k0 >> 3) & 3;
-          const uint4 xv = lds128(xs + (uint32_t)((((seg * 4 + ii) * N + n) * 4 + t) * 16));
-          const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w};
-          const uint32_t wa[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            a = fmaf(bf_lo(wa[j]), h_lo(xa[j]), a);
-            a = fmaf(bf_hi(wa[j]), h_hi(xa[j]), a);
-          }
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-      if (lane == 0) tb.rpart[(q * kMaxRouterParts + part) * kSkMaxTok + n] = a * tb.xf[n];
-    }
+    a = warp_sum(a);
+    if (lane == 0) part[w] = a;
+  }
+  // this CTA's rows of the output accumulator start at zero; ordered before
+  // the logits (release) and so before every CTA's reductions, which follow
+  // its gather of all logits (acquire)
+  {
+    const int r0 = divs(c * H, G), r1 = divs((c + 1) * H, G);
+    const int ld = (N + 1) & ~1;
+#pragma unroll 1
+    for (int i = r0 * ld + tid; i < r1 * ld; i += kT) p.oacc[i] = 0.f;
   }
   __syncthreads();
-  #pragma unroll 1
-  for (int idx = tid; idx < nq * N; idx += kT) {
-    const int q = divs(idx, N), n = idx - q * N;
+  if (tid < nq * N) fence_gpu();
+#pragma unroll 1
+  for (int qn = tid; qn < nq * N; qn += kT) {
+    const int q = divs(qn, N), n = qn - q * N;
     float s = 0.f;
-    #pragma unroll 1
-    for (int part = 0; part < parts; ++part)
-      s += tb.rpart[(q * kMaxRouterParts + part) * kSkMaxTok + n];
+#pragma unroll 1
+    for (int b = 0; b < nb; ++b) s += part[qn * nb + b];
     st_relaxed64(p.logits + (size_t)n * E + c + G * q,
                  ((unsigned long long)tb.tag << 32) | __float_as_uint(s));
   }
+  __syncthreads();   // x_prep converts the x slots in place afterwards
 }
 
 // Poll the call's tagged logits into shared memory (float [N][E]).
@@ -545,17 +543,7 @@ __device__ void gather_logits(const StreamParams& p, SkTab& tb, float* lg, int t
     }
     lg[w] = __uint_as_float((uint32_t)v);
   }
-}
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+  fence_gpu();   // acquire: every CTA's zeroed accumulator rows precede its logits
 }
 
 // Selection key, order preserving as unsigned: larger key = larger score.
@@ -564,49 +552,33 @@ __device__ __forceinline__ uint32_t okey(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Top-k routing of the N tokens from the logits in shared memory: softmax
-// (selection by logit, weights softmax over all E, optionally renormalised
-// over the selected), sigmoid + correction bias (selection by sigmoid(l) +
-// bias, weights sigmoid(l), optional renormalisation, times the routed
-// scaling factor), or softmax + correction bias (selection by softmax(l) +
-// bias, weights softmax(l), likewise).  Ties go to the lower expert index
-// (forward_k3.rs, the batched top-k step).
-//
-// A warp owns 128 experts of one token (4 keys per lane in registers) and
-// selects its local top k by k rounds of a warp max; with more than 128
-// experts one warp per token then selects the final k from the local lists
-// (at most 8 candidates per lane).
-
 // k rounds of warp arg-max over 4 (key, index) pairs per lane (key 0 =
-// empty); lane j < k returns selection j (index, 0xFFFFFFFF if none) and its
-// key.  Equal keys go to the lower index.
-__device__ __forceinline__ void best_slot(const uint32_t (&key)[4], const uint32_t (&idx)[4],
-                                          uint32_t& bk, uint32_t& bi) {
-  bk = 0u;
-  bi = 0xFFFFFFFFu;
-#pragma unroll
-  for (int s = 0; s < 4; ++s)
-    if (key[s] > bk || (key[s] == bk && idx[s] < bi)) {
-      bk = key[s];
-      bi = idx[s];
-    }
-}
+// empty, with index 0xFFFFFFFF); lane j < k returns selection j (key,
+// index; index 0xFFFFFFFF if none).  Equal keys go to the lower index.  The
+// lane that held a round's winner drops it and rescans its slots (all lanes
+// scan before round 0).
 __device__ __forceinline__ uint2 select_rounds(uint32_t (&key)[4], const uint32_t (&idx)[4], int k,
                                                int lane) {
-  uint32_t bk, bi;
-  best_slot(key, idx, bk, bi);
   uint2 mine = make_uint2(0u, 0xFFFFFFFFu);
+  uint32_t bk = 0u, bi = 0xFFFFFFFFu, we = 0xFFFFFFFFu;
 #pragma unroll 1
-  for (int j = 0; j < k; ++j) {
-    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
-    const uint32_t we = __reduce_min_sync(0xffffffffu, bk == m ? bi : 0xFFFFFFFFu);
-    if (lane == j) mine = make_uint2(m, m ? we : 0xFFFFFFFFu);
-    if (m != 0u && bi == we) {   // this lane held it: next best of its slots
+  for (int j = 0;; ++j) {
+    if (bi == we) {
+      bk = 0u;
+      bi = 0xFFFFFFFFu;
 #pragma unroll
-      for (int s = 0; s < 4; ++s)
+      for (int s = 0; s < 4; ++s) {
         if (idx[s] == we) key[s] = 0u;
-      best_slot(key, idx, bk, bi);
+        if (key[s] > bk || (key[s] == bk && idx[s] < bi)) {
+          bk = key[s];
+          bi = idx[s];
+        }
+      }
     }
+    if (j == k) break;
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+    we = __reduce_min_sync(0xffffffffu, bk == m ? bi : 0xFFFFFFFFu);
+    if (lane == j) mine = make_uint2(m, we);
   }
   return mine;
 }
@@ -784,7 +756,6 @@ __device__ void shared_gate_up(const StreamParams& p, SkTab& tb, uint8_t* smem, 
   const int h0 = sa + warp * (sb - sa) / kW, h1 = sa + (warp + 1) * (sb - sa) / kW;
   const uint32_t ring = smem_u32(smem + p.off_ring) + (uint32_t)(warp * D * kSkStageCodes + lane * 16);
   const uint32_t aux = smem_u32(smem + p.off_aux) + (uint32_t)(warp * D * kSkStageAux + lane * 16);
-  const uint64_t pol = evict_first_policy();
   const int rb = 2 * p.H;   // bytes per row
   const uint8_t* g0 = reinterpret_cast<const uint8_t*>(p.shg) + (size_t)(16 * j + g) * rb + 16 * t;
   const uint8_t* u0 = reinterpret_cast<const uint8_t*>(p.shu) + (size_t)(16 * j + g) * rb + 16 * t;
@@ -797,10 +768,10 @@ __device__ void shared_gate_up(const StreamParams& p, SkTab& tb, uint8_t* smem, 
   for (int it = 0; it < n + D - 1; ++it) {
     if (it < n) {
       const int o = 64 * (h0 + it);
-      cpa16w(piece(ring, islot, 0), g0 + o, 16u, pol);
-      cpa16w(piece(ring, islot, 1), g0 + o + 8 * rb, 16u, pol);
-      cpa16w(piece(ring, islot, 2), u0 + o, 16u, pol);
-      cpa16w(piece(ring, islot, 3), u0 + o + 8 * rb, 16u, pol);
+      cpa16w(piece(ring, islot, 0), g0 + o, 16u);
+      cpa16w(piece(ring, islot, 1), g0 + o + 8 * rb, 16u);
+      cpa16w(piece(ring, islot, 2), u0 + o, 16u);
+      cpa16w(piece(ring, islot, 3), u0 + o + 8 * rb, 16u);
       cpa16(aux + islot * 512, x0 + (vx ? o : 0), vx ? 16u : 0u);
       islot = islot + 1 == D ? 0 : islot + 1;
     }
@@ -884,18 +855,19 @@ __device__ void shared_gate_up(const StreamParams& p, SkTab& tb, uint8_t* smem, 
 }
 
 // ------------------------------------------------ P2 + P3 item pipeline
-// Items of one warp: its share of the routed gate/up items (tile, 128-column
-// segment: gate rows g, g+8 and up rows g, g+8), then its share of the down
-// items (shared-expert (segment, row tile) items first, then routed (expert,
-// segment, row tile) items; rows g, g+8).  Two loops (gate/up, then down)
-// whose bodies run once per 1-2 KB of weights; the first down items are
-// copied while the last gate/up items compute.
+// Items of one warp: its share of this CTA's routed gate/up items (tile,
+// 128-column segment: gate rows g, g+8 and up rows g, g+8), then its share of
+// the grid's down items (shared-expert (segment, row tile) items first, then
+// routed (expert, segment, 32-row tile) items; rows g + 8 i of the tile).  The down
+// list is split over all warps of the grid in order, so a warp's items mostly
+// share one (expert, segment) and its B operand; their partial sums go to the
+// FP32 output accumulator in global memory.  One loop; the first down items
+// are copied while the last gate/up items compute.
 struct Pipe {
   int c, G, g, t, lane;
   uint32_t ring, aux;
-  uint64_t pol;
   int S, tpe, a0, a1;                    // gate/up: segments per row, tiles per expert, items
-  int Sd, Sds, Mc, r0, r1, nsh, b0, b1;  // down: segments, shared segments, row tiles, items
+  int Sd, Sds, MT, nsh, b0, b1;          // down: segments, shared segments, row tiles, items
 };
 
 // Down item cursor: shared-expert items (u < 0) over (segment, row tile),
@@ -903,23 +875,25 @@ struct Pipe {
 struct DCur {
   int u, seg, m;
 };
+template <bool SH>
 __device__ __forceinline__ void dcur_init(const Pipe& P, int b, DCur& d) {
-  if (b < P.nsh) {
+  if (SH && b < P.nsh) {
     d.u = -1;
-    d.seg = divs(b, P.Mc);
-    d.m = b - d.seg * P.Mc;
+    d.seg = divs(b, P.MT);
+    d.m = b - d.seg * P.MT;
   } else {
-    const int unit = divs(b - P.nsh, P.Mc);
-    d.m = (b - P.nsh) - unit * P.Mc;
+    const int unit = divs(b - P.nsh, P.MT);
+    d.m = (b - P.nsh) - unit * P.MT;
     d.u = divs(unit, P.Sd);
     d.seg = unit - d.u * P.Sd;
   }
 }
+template <bool SH>
 __device__ __forceinline__ void dcur_next(const Pipe& P, DCur& d) {
-  if (++d.m == P.Mc) {
+  if (++d.m == P.MT) {
     d.m = 0;
     ++d.seg;
-    if (d.u < 0) {
+    if (SH && d.u < 0) {
       if (d.seg == P.Sds) {
         d.seg = 0;
         d.u = 0;
@@ -960,14 +934,13 @@ __device__ __forceinline__ void gu_issue_tile(const StreamParams& p, const SkTab
 // Copies of down item d (cursor), this lane's rows g and g+8.  Scale tensors
 // hold rows * K / gs bytes with rows a multiple of 32, so a 4-byte word never
 // reaches past the end.
-template <int FMT>
+template <int FMT, bool SH>
 __device__ __forceinline__ void dn_issue(const StreamParams& p, SkTab& tb, const Pipe& P,
                                          const DCur& d, uint32_t dc, uint32_t da, bool& sh_waited) {
   constexpr int gsz = FMT == FMT_NVFP4 ? 16 : 32;
-  const int rr = P.r0 + 16 * d.m + P.g;
-  const bool ok0 = rr < P.r1, ok8 = rr + 8 < P.r1;
+  const int rr = 32 * d.m + P.g;   // rows rr + 8 i, i < 4 (H is a multiple of 32)
   const int o = 64 * d.seg + 16 * P.t;
-  if (d.u < 0) {
+  if (SH && d.u < 0) {
     // shared-expert down: BF16 rows [H, Is] and this lane's piece of h_s,
     // copied only once every shared tile of the call is published
     if (!sh_waited) {
@@ -980,8 +953,8 @@ __device__ __forceinline__ void dn_issue(const StreamParams& p, SkTab& tb, const
     const int rb = 2 * p.Is;
     const uint8_t* base = reinterpret_cast<const uint8_t*>(p.shd);
     const uint8_t* q = base + (size_t)rr * rb + o;
-    cpa16w(dc, ok0 ? q : base, ok0 ? 16u : 0u, P.pol);
-    cpa16w(dc + 512, ok8 ? q + 8 * rb : base, ok8 ? 16u : 0u, P.pol);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cpa16w(dc + 512 * i, q + 8 * i * rb, 16u);
     const bool vx = P.g < p.N;
     cpa16(da, reinterpret_cast<const uint8_t*>(p.hs) + (vx ? (size_t)P.g * rb + o : 0),
           vx ? 16u : 0u);
@@ -989,18 +962,18 @@ __device__ __forceinline__ void dn_issue(const StreamParams& p, SkTab& tb, const
     const int rb = p.inter / 2, scb = p.inter / gsz;
     const size_t row = (size_t)tb.u_e[d.u] * p.H + rr;
     const bool kin = o < rb;
-    const bool v0 = kin && ok0, v8 = kin && ok8;
     const uint8_t* q = p.dq + row * rb + o;
-    cpa16w(dc, v0 ? q : p.dq, v0 ? 16u : 0u, P.pol);
-    cpa16w(dc + 512, v8 ? q + 8 * rb : p.dq, v8 ? 16u : 0u, P.pol);
     const size_t so = row * scb + (FMT == FMT_NVFP4 ? 8 : 4) * d.seg + (FMT == FMT_NVFP4 ? 2 * P.t : P.t);
     const uint8_t* s0 = p.dsc + (so & ~(size_t)3);
-    cpa4w(da, v0 ? s0 : p.dsc, v0 ? 4u : 0u, P.pol);
-    cpa4w(da + 4, v8 ? s0 + 8 * scb : p.dsc, v8 ? 4u : 0u, P.pol);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      cpa16w(dc + 512 * i, kin ? q + 8 * i * rb : p.dq, kin ? 16u : 0u);
+      cpa4w(da + 4 * i, kin ? s0 + 8 * i * scb : p.dsc, kin ? 4u : 0u);
+    }
   }
 }
 
-template <int FMT, int D>
+template <int FMT, int D, bool SH>
 __device__ void pipeline(const StreamParams& p, SkTab& tb, uint8_t* smem, const Pipe& P) {
   constexpr int gsz = FMT == FMT_NVFP4 ? 16 : 32;
   constexpr int sstep = FMT == FMT_NVFP4 ? 8 : 4;   // scale bytes per 128-column segment
@@ -1012,8 +985,9 @@ __device__ void pipeline(const StreamParams& p, SkTab& tb, uint8_t* smem, const 
   const int xstride = p.N * 64;   // bytes between the x pieces i of one segment
   const bool xlane = g < p.N;
   float* split = reinterpret_cast<float*>(smem + p.off_split);
-  float* oacc = reinterpret_cast<float*>(smem + p.off_oacc);
   const uint32_t tag = tb.tag;
+  const bool olane = 2 * t < p.N;   // this lane's output columns 2t, 2t+1 hold tokens
+  const int old = (p.N + 1) & ~1;   // row stride of the output accumulator
   const int soff_t = FMT == FMT_NVFP4 ? 2 * t : t;
 
   // ---- copy-side cursors
@@ -1023,7 +997,7 @@ __device__ void pipeline(const StreamParams& p, SkTab& tb, uint8_t* smem, const 
   gi.seg = P.a0 - gi.tl * P.S;
   if (ngu) gu_issue_tile<FMT>(p, tb, P, gi);
   DCur di;
-  dcur_init(P, P.b0, di);
+  dcur_init<SH>(P, P.b0, di);
   int dleft = ndn;   // down items not yet copied
   bool sh_waited = false;
   auto issue_next = [&](int k) {   // k-th item of this warp's sequence
@@ -1033,24 +1007,24 @@ __device__ void pipeline(const StreamParams& p, SkTab& tb, uint8_t* smem, const 
       const bool kin = o + 16 * t < rb;
       const uint32_t n = kin ? 16u : 0u;
       const int oo = kin ? o : 0;
-      cpa16w(dc, gi.qg + oo, n, P.pol);
-      cpa16w(dc + 512, gi.qg + oo + 8 * rb, n, P.pol);
-      cpa16w(dc + 1024, gi.qu + oo, n, P.pol);
-      cpa16w(dc + 1536, gi.qu + oo + 8 * rb, n, P.pol);
+      cpa16w(dc, gi.qg + oo, n);
+      cpa16w(dc + 512, gi.qg + oo + 8 * rb, n);
+      cpa16w(dc + 1024, gi.qu + oo, n);
+      cpa16w(dc + 1536, gi.qu + oo + 8 * rb, n);
       const int so = kin ? sstep * gi.seg : 0;
       const uint32_t n4 = kin ? 4u : 0u;
-      cpa4w(da, gi.sg + so, n4, P.pol);
-      cpa4w(da + 4, gi.sg + so + s8, n4, P.pol);
-      cpa4w(da + 8, gi.su + so, n4, P.pol);
-      cpa4w(da + 12, gi.su + so + s8, n4, P.pol);
+      cpa4w(da, gi.sg + so, n4);
+      cpa4w(da + 4, gi.sg + so + s8, n4);
+      cpa4w(da + 8, gi.su + so, n4);
+      cpa4w(da + 12, gi.su + so + s8, n4);
       if (++gi.seg == P.S) {
         gi.seg = 0;
         ++gi.tl;
         if (k + 1 < ngu) gu_issue_tile<FMT>(p, tb, P, gi);
       }
     } else if (dleft > 0) {
-      dn_issue<FMT>(p, tb, P, di, dc, da, sh_waited);
-      dcur_next(P, di);
+      dn_issue<FMT, SH>(p, tb, P, di, dc, da, sh_waited);
+      dcur_next<SH>(P, di);
       --dleft;
     }
     islot = islot + 1 == D ? 0 : islot + 1;
@@ -1063,7 +1037,7 @@ __device__ void pipeline(const StreamParams& p, SkTab& tb, uint8_t* smem, const 
   float s2g = 1.f, s2u = 1.f, s2d = 1.f;
   // down consume state
   DCur cd;
-  dcur_init(P, P.b0, cd);
+  dcur_init<SH>(P, P.b0, cd);
   int du = -2, dseg = -1, dsh = 0;
   uint32_t b[16];
   const int total = ngu + ndn;
@@ -1169,48 +1143,102 @@ __device__ void pipeline(const StreamParams& p, SkTab& tb, uint8_t* smem, const 
         b[4 * ii + 2] = v.z;
         b[4 * ii + 3] = v.w;
       }
-      cpa_wait_d<D>();
-      const uint32_t sc = P.ring + (uint32_t)(cslot * 2048);
-      const uint4 av = lds128(P.aux + (uint32_t)(cslot * 512));
-      const uint32_t m16 = FMT == FMT_NVFP4 ? 0xFFFFu : 0xFFu;
-      seg_fp4<FMT>(ag, lds128(sc), lds128(sc + 512), (av.x >> csh) & m16, (av.y >> csh) & m16, b);
-      seg_fp4<FMT>(au, lds128(sc + 1024), lds128(sc + 1536), (av.z >> csh) & m16,
-                   (av.w >> csh) & m16, b);
       ++done;
       if (++cseg == P.S) {
         cseg = 0;
         ++ctl;
       }
-    } else {
-      float cs[4] = {0.f, 0.f, 0.f, 0.f};
+    } else if (SH && cd.u < 0) {
+      // shared-expert down item (BF16 rows, B copied with them)
+      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
       const uint32_t sc = P.ring + (uint32_t)(cslot * 2048);
-      if (cd.u < 0) {
-        cpa_wait_d<D>();
-        seg_bf16(cs, lds128(sc), lds128(sc + 512), lds128(P.aux + (uint32_t)(cslot * 512)));
-      } else {
-        if (cd.u != du || cd.seg != dseg) {
-          // routed unit: wait for the eight gate/up tiles its K segment
-          // reads, then B = this lane's f16 h piece of column g
-          if (cd.u != du) {
-            const size_t row = (size_t)tb.u_e[cd.u] * p.H + P.r0 + g;
-            dsh = 8 * (int)((row * (p.inter / gsz) + soff_t) & 3u);
-          }
-          du = cd.u;
-          dseg = cd.seg;
-          const int kk = 128 * cd.seg + 32 * t;
-          const bool have = xlane && ((tb.u_mask[cd.u] >> g) & 1u) && kk < p.inter;
-          load_h(p, tb, p.hw + (have ? ((size_t)tb.u_slot[cd.u][g] * p.inter + kk) >> 1 : 0), have,
-                 tag, b);
-        }
-        cpa_wait_d<D>();
-        const uint2 sw = lds64(P.aux + (uint32_t)(cslot * 512));
-        const uint32_t m16 = FMT == FMT_NVFP4 ? 0xFFFFu : 0xFFu;
-        seg_fp4<FMT>(cs, lds128(sc), lds128(sc + 512), (sw.x >> dsh) & m16, (sw.y >> dsh) & m16, b);
+      cpa_wait_d<D>();
+      const uint4 bv = lds128(P.aux + (uint32_t)(cslot * 512));
+      seg_bf16(c0, lds128(sc), lds128(sc + 512), bv);
+      seg_bf16(c1, lds128(sc + 1024), lds128(sc + 1536), bv);
+      if (olane) {
+        red_out(p.oacc + (32 * cd.m + g) * old + 2 * t, old, c0);
+        red_out(p.oacc + (32 * cd.m + 16 + g) * old + 2 * t, old, c1);
       }
-      float* o = oacc + cd.m * 128 + lane * 4;
-#pragma unroll
-      for (int qq = 0; qq < 4; ++qq) atomicAdd(o + qq, cs[qq]);
-      dcur_next(P, cd);
+      dcur_next<SH>(P, cd);
+      cslot = cslot + 1 == D ? 0 : cslot + 1;
+      continue;
+    } else if (cd.u != du || cd.seg != dseg) {
+      // routed down item of a new (unit, segment): B = this lane's f16 h
+      // piece of column g (waits for the eight gate/up tiles it reads)
+      if (cd.u != du) {
+        // byte position of the scales in their word: the same for rows
+        // 32 m + g + 8 i of every row tile m (8 x the scale bytes per row is
+        // a multiple of 4)
+        const size_t row = (size_t)tb.u_e[cd.u] * p.H + g;
+        dsh = 8 * (int)((row * (p.inter / gsz) + soff_t) & 3u);
+      }
+      du = cd.u;
+      dseg = cd.seg;
+      const int kk = 128 * cd.seg + 32 * t;
+      const bool have = xlane && ((tb.u_mask[cd.u] >> g) & 1u) && kk < p.inter;
+      load_h(p, tb, p.hw + (have ? ((size_t)tb.u_slot[cd.u][g] * p.inter + kk) >> 1 : 0), have,
+             tag, b);
+    }
+    // the item's FP4 rows: gate and up (two row pairs) or down (one)
+    cpa_wait_d<D>();
+    {
+      const uint32_t m16 = FMT == FMT_NVFP4 ? 0xFFFFu : 0xFFu;
+      const uint32_t sc = P.ring + (uint32_t)(cslot * 2048), sa = P.aux + (uint32_t)(cslot * 512);
+      uint32_t a0, a1, b0, b1;
+      float fa, fb;
+      if (h < ngu) {
+        // gate and up: two independent MMA chains
+        const uint4 av = lds128(sa);
+        const uint4 g0 = lds128(sc), g8 = lds128(sc + 512);
+        const uint4 u0 = lds128(sc + 1024), u8 = lds128(sc + 1536);
+        if (FMT == FMT_NVFP4) {
+          seg_scales<FMT>((av.x >> csh) & m16, (av.y >> csh) & m16, a0, a1, b0, b1, fa, fb);
+          seg_mma<FMT>(ag, ag, g0, g8, a0, a1, b0, b1, b);
+          seg_scales<FMT>((av.z >> csh) & m16, (av.w >> csh) & m16, a0, a1, b0, b1, fa, fb);
+          seg_mma<FMT>(au, au, u0, u8, a0, a1, b0, b1, b);
+        } else {
+          float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
+          float ga, gb;
+          seg_scales<FMT>((av.x >> csh) & m16, (av.y >> csh) & m16, a0, a1, b0, b1, ga, gb);
+          seg_mma<FMT>(cg, cg, g0, g8, a0, a1, b0, b1, b);
+          seg_scales<FMT>((av.z >> csh) & m16, (av.w >> csh) & m16, a0, a1, b0, b1, fa, fb);
+          seg_mma<FMT>(cu, cu, u0, u8, a0, a1, b0, b1, b);
+          ag[0] = fmaf(cg[0], ga, ag[0]);
+          ag[1] = fmaf(cg[1], ga, ag[1]);
+          ag[2] = fmaf(cg[2], gb, ag[2]);
+          ag[3] = fmaf(cg[3], gb, ag[3]);
+          au[0] = fmaf(cu[0], fa, au[0]);
+          au[1] = fmaf(cu[1], fa, au[1]);
+          au[2] = fmaf(cu[2], fb, au[2]);
+          au[3] = fmaf(cu[3], fb, au[3]);
+        }
+      } else {
+        // down: two row pairs (rows 32m + g + 8i, i < 4), two MMA chains;
+        // the partial sums (columns 2t, 2t+1) go to the output accumulator
+        const uint4 sw = lds128(sa);
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+        float fc, fd;
+        seg_scales<FMT>((sw.x >> dsh) & m16, (sw.y >> dsh) & m16, a0, a1, b0, b1, fa, fb);
+        seg_mma<FMT>(c0, c0, lds128(sc), lds128(sc + 512), a0, a1, b0, b1, b);
+        seg_scales<FMT>((sw.z >> dsh) & m16, (sw.w >> dsh) & m16, a0, a1, b0, b1, fc, fd);
+        seg_mma<FMT>(c1, c1, lds128(sc + 1024), lds128(sc + 1536), a0, a1, b0, b1, b);
+        if (FMT != FMT_NVFP4) {
+          c0[0] *= fa;
+          c0[1] *= fa;
+          c0[2] *= fb;
+          c0[3] *= fb;
+          c1[0] *= fc;
+          c1[1] *= fc;
+          c1[2] *= fd;
+          c1[3] *= fd;
+        }
+        if (olane) {
+          red_out(p.oacc + (32 * cd.m + g) * old + 2 * t, old, c0);
+          red_out(p.oacc + (32 * cd.m + 16 + g) * old + 2 * t, old, c1);
+        }
+        dcur_next<SH>(P, cd);
+      }
     }
     cslot = cslot + 1 == D ? 0 : cslot + 1;
   }
@@ -1218,30 +1246,16 @@ __device__ void pipeline(const StreamParams& p, SkTab& tb, uint8_t* smem, const 
 }
 
 // ------------------------------------------------------------------ kernel
-template <int FMT, int D>
+template <int FMT, int D, bool SH>
 __global__ void __launch_bounds__(kSkThreads, 1) moe_stream_kernel(const __grid_constant__ StreamParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   SkTab& tb = *reinterpret_cast<SkTab*>(smem + p.off_tab);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, G = gridDim.x;
 
-  // router weights of this warp's first row part: requested before anything
-  // else, they are the first DRAM round trip on the critical path
-  uint4 wv[8];
-  {
-    const int nq = c < p.E ? divs(p.E - 1 - c, G) + 1 : 0;
-    const int parts = (p.H + kRouterPart - 1) / kRouterPart;
-    if (warp < nq * parts) {
-      const int q = divs(warp, parts), part = warp - q * parts;
-      const int kb = part * kRouterPart, ke = min(p.H, kb + kRouterPart);
-      const uint16_t* wr = p.router + (size_t)(c + G * q) * p.H;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int k0 = kb + (lane + 32 * i) * 8;
-        wv[i] = k0 < ke ? ld_nc_u4(wr + k0) : make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-  }
+  // the call's inputs: the first DRAM round trip on the critical path
+  const int nq = c < p.E ? divs(p.E - 1 - c, G) + 1 : 0;   // router rows of this CTA
+  issue_inputs(p, smem, c, G, nq, tid);
   if (tid == 0) {
     // the call's tag: the counter moves by exactly 256 per call (G <= 256):
     // CTA 0 adds 257 - G and the others 1, so every CTA of call c reads a
@@ -1260,18 +1274,21 @@ __global__ void __launch_bounds__(kSkThreads, 1) moe_stream_kernel(const __grid_
     tb.xmax[tid] = 0u;
     tb.xdot[tid] = 0.f;
   }
+  // the copies have landed; the barrier also publishes the tag and the
+  // zeroed tables
+  cpa_wait_all();
+  __syncthreads();
+  router_phase(p, tb, smem, c, G, nq, warp, lane, tid);
+  x_prep(p, tb, smem, tid);
   {
+    // the router's partial sums are done with the split area
     float* sp = reinterpret_cast<float*>(smem + p.off_split);
     for (int i = tid; i < kSkSplitSlots * 256; i += kT) sp[i] = 0.f;
-    float* oa = reinterpret_cast<float*>(smem + p.off_oacc);
-    for (int i = tid; i < kSkMaxMt * 128; i += kT) oa[i] = 0.f;
+    __syncthreads();
   }
-  // x_prep's first barrier also publishes the tag and the zeroed tables
-  x_prep(p, tb, smem, tid);
-  router_phase(p, tb, smem, c, G, warp, lane, tid, wv);
 
   // PS: shared-expert gate/up while the logits land
-  if (p.Is > 0) shared_gate_up<D>(p, tb, smem, c, G, warp, lane);
+  if (SH) shared_gate_up<D>(p, tb, smem, c, G, warp, lane);
 
   // P1: routing (the ring holds the float logits and keys until the weights stream)
   float* lg = reinterpret_cast<float*>(smem + p.off_ring);
@@ -1292,7 +1309,6 @@ __global__ void __launch_bounds__(kSkThreads, 1) moe_stream_kernel(const __grid_
   if (p.route_only) return;
   if (warp == 0) build_tables(p, tb, lane);
   __syncthreads();
-  if (tb.abort) return;
 
   // P2 + P3
   Pipe P;
@@ -1303,7 +1319,6 @@ __global__ void __launch_bounds__(kSkThreads, 1) moe_stream_kernel(const __grid_
   P.lane = lane;
   P.ring = smem_u32(smem + p.off_ring) + (uint32_t)(warp * D * kSkStageCodes + lane * 16);
   P.aux = smem_u32(smem + p.off_aux) + (uint32_t)(warp * D * kSkStageAux + lane * 16);
-  P.pol = evict_first_policy();
   P.S = (p.H + 127) >> 7;
   P.tpe = p.inter >> 4;
   {
@@ -1314,29 +1329,47 @@ __global__ void __launch_bounds__(kSkThreads, 1) moe_stream_kernel(const __grid_
     P.a1 = (int)((long long)(warp + 1) * tot / kW);
   }
   P.Sd = (p.inter + 127) >> 7;
-  P.Sds = p.Is >> 5;
-  P.r0 = divs(c * p.H, G);
-  P.r1 = divs((c + 1) * p.H, G);
-  P.Mc = (P.r1 - P.r0 + 15) >> 4;
-  P.nsh = P.Sds * P.Mc;
+  P.Sds = SH ? p.Is >> 5 : 0;
+  P.MT = p.H >> 5;   // 32-row down tiles
+  P.nsh = P.Sds * P.MT;
   {
-    const int tot = P.nsh + tb.U * P.Sd * P.Mc;
-    P.b0 = (int)((long long)warp * tot / kW);
-    P.b1 = (int)((long long)(warp + 1) * tot / kW);
+    // the grid's down items split over all warps in order
+    const long long tot = P.nsh + (long long)tb.U * P.Sd * P.MT;
+    const long long gw = (long long)c * kW + warp, nw = (long long)G * kW;
+    P.b0 = (int)(gw * tot / nw);
+    P.b1 = (int)((gw + 1) * tot / nw);
   }
-  pipeline<FMT, D>(p, tb, smem, P);
+  if (!tb.abort) pipeline<FMT, D, SH>(p, tb, smem, P);
+
+  // every CTA's reductions into the output accumulator are done when the
+  // end counter (+ 256 per call, like the call counter) reaches 256 x tag
   __syncthreads();
+  if (tid == 0) {
+    fence_gpu();   // no weight copies are in flight here
+    atomicAdd(&p.ctrl->fin, c == 0 ? 257ull - G : 1ull);
+    const unsigned long long target = (unsigned long long)tb.tag << 8;
+    if (ld_acquire64(&p.ctrl->fin) < target) {
+      const uint64_t t0 = global_timer_ns();
+      while (ld_acquire64(&p.ctrl->fin) < target) {
+        if (global_timer_ns() - t0 > p.timeout_ns) {
+          set_error(p, tb, kErrTimeoutBarrier);
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+  }
+  __syncthreads();
+  if (tb.abort) return;
   {
-    const int nr = P.r1 - P.r0;
-    const float* oa = reinterpret_cast<const float*>(smem + p.off_oacc);
-    #pragma unroll 1
+    // this CTA's output rows in BF16
+    const int r0 = divs(c * p.H, G), r1 = divs((c + 1) * p.H, G);
+    const int nr = r1 - r0;
+#pragma unroll 1
     for (int idx = tid; idx < nr * p.N; idx += kT) {
-      const int n = divs(idx, nr), r = idx - n * nr;
-      const int m = r >> 4, rr = r & 15;
-      const int gg = rr & 7, half = rr >> 3;
-      const int ln = 4 * gg + (n >> 1);
-      const float v = oa[m * 128 + ln * 4 + half * 2 + (n & 1)];
-      p.out[(size_t)n * p.H + P.r0 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+      const int n = divs(idx, nr), r = r0 + idx - n * nr;
+      p.out[(size_t)n * p.H + r] =
+          __bfloat16_as_ushort(__float2bfloat16_rn(__ldcg(p.oacc + r * ((p.N + 1) & ~1) + n)));
     }
   }
 }
@@ -1349,9 +1382,6 @@ bool plan_stream(StreamParams& p, int smem_budget, int grid) {
   if (p.H % 32 || p.inter % 32 || p.Is % 32) return false;
   if (p.E > kMaxE || p.N * p.k > kMaxSlots) return false;
   if (grid < 128 || grid > kSkMaxGrid || (p.E + grid - 1) / grid > kMaxRouterRows) return false;
-  if ((p.H + kRouterPart - 1) / kRouterPart > kMaxRouterParts) return false;
-  const int rows = (p.H + grid - 1) / grid;
-  if ((rows + 15) / 16 > kSkMaxMt) return false;
   if (p.Is > 0) {
     const int Ts = p.Is / 16, Sb = p.H / 32;
     if (Ts > grid) return false;   // one shared unit per CTA at most
@@ -1368,8 +1398,6 @@ bool plan_stream(StreamParams& p, int smem_budget, int grid) {
   off = al(off + (int)sizeof(SkTab));
   p.off_split = off;
   off = al(off + kSkSplitSlots * 256 * 4);
-  p.off_oacc = off;
-  off = al(off + kSkMaxMt * 128 * 4);
   p.off_x16 = off;
   off = al(off + S * 4 * p.N * 64);
   const int per_stage = kSkWarps * (kSkStageCodes + kSkStageAux);
@@ -1382,6 +1410,11 @@ bool plan_stream(StreamParams& p, int smem_budget, int grid) {
   if (Wt * p.k > 128) return false;   // the second top-k level holds 4 candidates per lane
   if (D * kSkWarps * kSkStageCodes < ((p.N * p.E * 4 + 15) & ~15) + p.N * p.E * 8 + p.N * Wt * p.k * 8)
     return false;
+  // ... and, before that, this CTA's router rows; the router's partial sums
+  // sit in the split area
+  const int nq = (p.E + grid - 1) / grid;
+  if (D * kSkWarps * kSkStageCodes < nq * p.H * 2) return false;
+  if (nq * p.N * ((p.H + 255) / 256) > kSkSplitSlots * 256) return false;
   p.stages = D;
   p.off_ring = off;
   off += D * kSkWarps * kSkStageCodes;
@@ -1391,29 +1424,35 @@ bool plan_stream(StreamParams& p, int smem_budget, int grid) {
   return off <= smem_budget;
 }
 
+// The kernel instances: block-scale format x ring depth x shared expert.
+template <int FMT, int D, bool SH>
+constexpr const void* sk_fn() {
+  return (const void*)moe_stream_kernel<FMT, D, SH>;
+}
+const void* stream_fn(int fmt, int stages, bool sh) {
+  const bool nv = fmt == FMT_NVFP4;
+  if (stages == 4)
+    return nv ? (sh ? sk_fn<FMT_NVFP4, 4, true>() : sk_fn<FMT_NVFP4, 4, false>())
+              : (sh ? sk_fn<FMT_MXFP4, 4, true>() : sk_fn<FMT_MXFP4, 4, false>());
+  return nv ? (sh ? sk_fn<FMT_NVFP4, 3, true>() : sk_fn<FMT_NVFP4, 3, false>())
+            : (sh ? sk_fn<FMT_MXFP4, 3, true>() : sk_fn<FMT_MXFP4, 3, false>());
+}
+
 cudaError_t stream_set_smem(int smem_bytes) {
-  const void* fns[4] = {(const void*)moe_stream_kernel<FMT_NVFP4, 3>,
-                        (const void*)moe_stream_kernel<FMT_NVFP4, 4>,
-                        (const void*)moe_stream_kernel<FMT_MXFP4, 3>,
-                        (const void*)moe_stream_kernel<FMT_MXFP4, 4>};
-  for (const void* f : fns) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-    if (e != cudaSuccess) return e;
-  }
+  for (int fmt : {FMT_NVFP4, FMT_MXFP4})
+    for (int stages : {3, 4})
+      for (bool sh : {false, true}) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            stream_fn(fmt, stages, sh), cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+        if (e != cudaSuccess) return e;
+      }
   return cudaSuccess;
 }
 
 cudaError_t launch_stream(const StreamParams& p, int grid, cudaStream_t stream) {
   void* args[] = {const_cast<StreamParams*>(&p)};
-  const bool nv = p.fmt == FMT_NVFP4;
-  const void* fn = p.stages == 4
-                       ? (nv ? (const void*)moe_stream_kernel<FMT_NVFP4, 4>
-                             : (const void*)moe_stream_kernel<FMT_MXFP4, 4>)
-                       : (nv ? (const void*)moe_stream_kernel<FMT_NVFP4, 3>
-                             : (const void*)moe_stream_kernel<FMT_MXFP4, 3>);
-  return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kSkThreads), args,
-                                     (size_t)p.smem_bytes, stream);
+  return cudaLaunchCooperativeKernel(stream_fn(p.fmt, p.stages, p.Is > 0), dim3(grid),
+                                     dim3(kSkThreads), args, (size_t)p.smem_bytes, stream);
 }
 
 }  // namespace moe
