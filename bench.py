@@ -2,27 +2,27 @@
 
 Workload: the Qwen3-30B-A3B-shaped layer (H 2048, inter 768, 128 NVFP4
 experts, top-8 softmax with renormalisation) at N = 1, 2, 3, 4 tokens.  One
-step = four moe_forward calls, N = 1, 2, 3, 4, on one layer copy; successive
-steps use different layer copies (L2 defeat: one cycle of copies touches many
-times the 129 MB L2).  The metric is the achieved HBM rate over algorithmic
-bytes:
+step = four moe_forward calls, N = 1, 2, 3, 4, on one layer copy; step s runs
+on copy s mod R (L2 defeat: one round of copies touches many times the
+129 MB L2).  The metric is the achieved HBM rate over algorithmic bytes:
     bytes(call) = U * expert_bytes + router_bytes + shared_bytes + x/out bytes
 with U the number of distinct routed experts the call's tokens touched (read
 back from the routing outputs before timing).  value = sum of bytes / time.
 
-Timed region: K steps replayed from a captured CUDA graph, bracketed by a
-barrier and torch.cuda.synchronize(), CUDA events on the launch stream; the
-maximum over ranks is taken.  "per_n" gives each token count's latency
-(median of five repeats of a round-robin loop) and "per_n_l2_flush" the same
-from single calls after an L2-sized buffer write.  The line also carries "grouped": the many-token
-path (gpt-oss-shaped MXFP4 layer at N = 512, tcgen05 GEMMs),
-"bf16_experts" and "fp8_experts": the same Qwen3 shape with BF16 or FP8
-(128 x 128 block-scaled) routed experts at N = 1-4, and "nvfp4_router": the
-Qwen3 shape with an NVFP4-quantised router, and "zero_experts": the Qwen3
-shape with 64 zero experts (softmax + correction-bias routing over 192
-router outputs), all timed on the same GPU after the main measurement.  --impl reference
-times the FP64 CPU oracle on a bounded sample of the same workload instead;
-"cpu_baseline" also holds the oracle's single-thread per-call times.
+Timed region: exactly --steps steps after exactly --warmup untimed ones, each
+step a replay of its copy's captured CUDA graph, bracketed by a barrier and
+torch.cuda.synchronize(), CUDA events on the launch stream; the maximum over
+ranks is taken.  "per_n" gives each token count's latency (median of five
+repeats of a round-robin loop) and "per_n_l2_flush" the same from single
+calls after an L2-sized buffer write.  "configs" holds every layer shape of
+the workload list at its token counts (the small layer, Qwen3 N=1-4,
+MTP-verify N=3, DeepSeek-V3 N=4, gpt-oss N=1-64 and N=512 on the grouped
+tcgen05 path); "bf16_experts", "fp8_experts", "nvfp4_router" and
+"zero_experts" the Qwen3 shape with BF16 or FP8 routed experts, an NVFP4
+router, or 64 zero experts; all timed on the same GPU after the main
+measurement.  --impl reference times the FP64 CPU oracle on a bounded sample
+of the same workload instead; "cpu_baseline" also holds the oracle's
+single-thread per-call times.
 """
 from __future__ import annotations
 
@@ -228,22 +228,36 @@ def measure_grouped(stream, name: str = "gpt_oss_120b", N: int = 512, reps: int 
             "reps": reps}
 
 
-def measure_decode_config(stream, name: str, tokens, copies: int = 4, reps: int = 200) -> dict:
-    """Decode-kernel latency of another layer shape (e.g. BF16 routed experts)
-    at each token count: `copies` device copies of the layer, each with its
-    own token rows, replayed round-robin from one CUDA graph so consecutive
-    calls read different weight bytes (copies x touched bytes > L2)."""
+def layer_bytes(spec) -> int:
+    """Device bytes of one copy of the layer's weights."""
+    return spec.E * spec.expert_bytes() + spec.router_bytes() + spec.shared_bytes()
+
+
+def measure_config(stream, name: str, tokens, l2_bytes: int, max_copies: int = 16,
+                   reps: int = 200) -> dict:
+    """Latency of one layer shape at each token count: enough device copies of
+    the layer (each with its own token rows) that a round of calls touches
+    about three times the L2, replayed round-robin from one CUDA graph, so
+    consecutive calls read different weight bytes; the median of five timed
+    loops.  A layer too small for that (the tiny shape) stays L2-resident, and
+    the record says so."""
     import torch
     from moe_decode_layer_topk_gb300 import _lib, synth
     from moe_decode_layer_topk_gb300.device import DeviceLayer, bf16_tensor, workspace
     spec = synth.CONFIGS[name]
-    base = DeviceLayer.upload(synth.make_layer(spec))
-    devs = [base] + [base.clone() for _ in range(copies - 1)]
     peak, _ = _peaks()
+    lb = layer_bytes(spec)
+    base = DeviceLayer.upload(synth.make_layer(spec))
     res = {}
+    devs = [base]
     for N in tokens:
+        touched = min(spec.E, N * spec.top_k) * spec.expert_bytes() + spec.router_bytes() + \
+            spec.shared_bytes()
+        copies = max(2, min(max_copies, -(-3 * l2_bytes // touched), (48 << 30) // lb))
+        while len(devs) < copies:
+            devs.append(base.clone())
         calls = []
-        for i, dev in enumerate(devs):
+        for i, dev in enumerate(devs[:copies]):
             x = bf16_tensor(synth.make_tokens(spec, N, seed=77000 + 97 * N + i))
             out, ws = torch.empty_like(x), workspace(spec, N)
             idx = torch.empty((N, spec.top_k), dtype=torch.int32, device="cuda")
@@ -256,26 +270,52 @@ def measure_decode_config(stream, name: str, tokens, copies: int = 4, reps: int 
                 _lib.moe_forward(dev.desc, dev.weights, x, out, ws, stream=stream)
         rounds = max(1, reps // len(calls))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            g.replay()
-            e0.record(stream)
-            for _ in range(rounds):
+        rep_us = []
+        for _ in range(PER_N_REPEATS):
+            with torch.cuda.stream(stream):
                 g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
+                e0.record(stream)
+                for _ in range(rounds):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            rep_us.append(e0.elapsed_time(e1) * 1e3 / (rounds * len(calls)))
         for c in calls:
             assert _lib.moe_get_error(c[3]) == _lib.MOE_OK
-        us = e0.elapsed_time(e1) * 1e3 / (rounds * len(calls))
+        us = float(np.median(rep_us))
         b = float(np.mean([c[4]["total"] for c in calls]))
+        round_bytes = sum(c[4]["total"] for c in calls)
         res[str(N)] = {"us_per_layer": round(us, 3), "tokens_per_s": round(N / us * 1e6, 1),
                        "GBps": round(b / us / 1e3, 1),
                        "hbm_frac_of_measured": round(b / us / 1e3 / peak, 4),
-                       "U_mean": float(np.mean([c[4]["U"] for c in calls])), "bytes_mean": int(b)}
+                       "U_mean": float(np.mean([c[4]["U"] for c in calls])), "bytes_mean": int(b),
+                       "copies": copies, "l2_resident": bool(round_bytes < l2_bytes),
+                       "launches_per_call": kernels_per_call(spec, N),
+                       "us_repeats": [round(u, 3) for u in rep_us]}
         del calls, g
     del devs, base
     torch.cuda.empty_cache()
-    return {"workload": f"{name} layer (fused decode kernel), {copies} copies round-robin",
+    return {"workload": f"{name} layer: H {spec.H}, inter {spec.inter}, E {spec.E}, top-{spec.top_k}, "
+                        f"{spec.wfmt} experts" + (f", shared inter {spec.shared_inter}"
+                                                  if spec.shared_inter else ""),
             "per_n": res}
+
+
+def measure_all_configs(stream, l2_bytes: int) -> dict:
+    """Every layer shape of the workload list at its token counts: the small
+    layer (N=1), the Qwen3 shape (N=1-4), the MTP-verify layer (N=3), the
+    DeepSeek-V3 shape (N=4) and the gpt-oss shape (N=1-64 on the fused
+    kernels, N=512 on the grouped path)."""
+    from moe_decode_layer_topk_gb300 import synth
+    out = {}
+    for name in ("tiny", "qwen3_30b_a3b", "mtp_verify", "deepseek_v3", "gpt_oss_120b"):
+        spec = synth.CONFIGS[name]
+        toks = [n for n in spec.tokens if n <= 64]
+        out[name] = measure_config(stream, name, toks, l2_bytes)
+        big = [n for n in spec.tokens if n > 64]
+        for n in big:
+            out[name]["per_n"][str(n)] = measure_grouped(stream, name, n)
+    return out
 
 
 def run_gpu(args):
@@ -315,32 +355,36 @@ def run_gpu(args):
         assert _lib.moe_get_error(c[4]) == _lib.MOE_OK
     launches_per_cycle = len(calls)
     kernels_per_cycle = sum(kernels_per_call(spec, c[1]) for c in calls)
+    ntok = len(tokens)
 
-    def enqueue_cycle():
-        for dev, N, x, out, ws, _ in calls:
+    # one step = the N sweep on one layer copy; step s uses copy s mod R, so
+    # consecutive steps read different weight bytes
+    def enqueue_step(r):
+        for dev, N, x, out, ws, _ in calls[r * ntok:(r + 1) * ntok]:
             _lib.moe_forward(dev.desc, dev.weights, x, out, ws, stream=stream)
 
-    graph = None
+    graphs = None
     if not args.no_graph:
         with torch.cuda.stream(stream):
-            enqueue_cycle()
+            for r in range(R):
+                enqueue_step(r)
         stream.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            enqueue_cycle()
+        graphs = []
+        for r in range(R):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                enqueue_step(r)
+            graphs.append(g)
 
-    def run_cycle():
-        if graph is not None:
-            graph.replay()
+    def run_step(s_):
+        if graphs is not None:
+            graphs[s_ % R].replay()
         else:
-            enqueue_cycle()
+            enqueue_step(s_ % R)
 
-    steps_per_cycle = R          # a step is one N sweep on one layer copy
-    cycles_warm = max(1, -(-args.warmup // steps_per_cycle))
-    cycles = max(1, -(-args.steps // steps_per_cycle))
     with torch.cuda.stream(stream):
-        for _ in range(cycles_warm):
-            run_cycle()
+        for s_ in range(args.warmup):
+            run_step(s_)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -349,8 +393,8 @@ def run_gpu(args):
     with ClockSampler(local) as clk:
         with torch.cuda.stream(stream):
             ev0.record(stream)
-            for _ in range(cycles):
-                run_cycle()
+            for s_ in range(args.warmup, args.warmup + args.steps):
+                run_step(s_)
             ev1.record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -358,11 +402,14 @@ def run_gpu(args):
     ms = max_over_ranks(ev0.elapsed_time(ev1), world)
     for c in calls:
         assert _lib.moe_get_error(c[4]) == _lib.MOE_OK, "device-side wait expired during timing"
-    steps = cycles * steps_per_cycle
-    value = job_gbps(cycles * per_cycle_bytes, world, ms)
-    launches = cycles * launches_per_cycle
+    steps = args.steps
+    step_bytes = [sum(c[5]["total"] for c in calls[r * ntok:(r + 1) * ntok]) for r in range(R)]
+    timed_bytes = sum(step_bytes[s_ % R] for s_ in range(args.warmup, args.warmup + steps))
+    value = job_gbps(timed_bytes, world, ms)
+    launches = steps * ntok
     avg_launch_us = ms * 1e3 / launches
-    achieved = per_cycle_bytes / launches_per_cycle / (avg_launch_us * 1e-6) / 1e9
+    achieved = timed_bytes / launches / (avg_launch_us * 1e-6) / 1e9
+    kernels_timed = sum(kernels_per_call(spec, N) for N in tokens) * steps
 
     # per-token-count latency (separate loop after the timed region)
     per_n = {}
@@ -440,7 +487,7 @@ def run_gpu(args):
         "unit": "GB/s",
         "n_gpus": world,
         "steps": steps,
-        "warmup": cycles_warm * steps_per_cycle,
+        "warmup": args.warmup,
         "ms_per_step": round(ms / steps, 5),
         "higher_is_better": True,
         "scaling": "weak",
@@ -451,9 +498,9 @@ def run_gpu(args):
                    "H": spec.H, "inter": spec.inter, "E": spec.E, "top_k": spec.top_k,
                    "wfmt": spec.wfmt, "shared_inter": spec.shared_inter,
                    "layer_copies": R, "l2_bytes": l2,
-                   "l2_defeat": f"inputs larger than L2: {R} layer copies cycled, "
-                                f"{per_cycle_bytes / l2:.1f}x L2 touched per cycle",
-                   "cuda_graph": graph is not None,
+                   "l2_defeat": f"inputs larger than L2: {R} layer copies cycled, step s on "
+                                f"copy s mod {R}; {per_cycle_bytes / l2:.1f}x L2 touched per cycle",
+                   "cuda_graph": graphs is not None,
                    "parallelism": f"{world} replicas" if world > 1 else "single GPU"},
         "frac_of_8TBs": round(value / world / NOMINAL_HBM_GBS, 4),
         "us_per_layer_mean": round(avg_launch_us, 3),
@@ -465,21 +512,21 @@ def run_gpu(args):
                      "traffic_source": traffic_note,
                      "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
                      "kernel": "moe::moe_decode_kernel"},
-        "gpu_launches": cycles * kernels_per_cycle,
+        "gpu_launches": kernels_timed,
         "e2e": e2e,
     }
-    if rank == 0 and not args.no_grouped:
-        result["grouped"] = measure_grouped(stream)
+    if rank == 0 and not args.no_configs:
+        result["configs"] = measure_all_configs(stream, l2)
     if rank == 0 and not args.no_bf16:
-        result["bf16_experts"] = measure_decode_config(stream, "qwen3_30b_a3b_bf16", (1, 2, 3, 4))
+        result["bf16_experts"] = measure_config(stream, "qwen3_30b_a3b_bf16", (1, 2, 3, 4), l2)
     if rank == 0 and not args.no_fp8:
-        result["fp8_experts"] = measure_decode_config(stream, "qwen3_30b_a3b_fp8", (1, 2, 3, 4))
+        result["fp8_experts"] = measure_config(stream, "qwen3_30b_a3b_fp8", (1, 2, 3, 4), l2)
     if rank == 0 and not args.no_nvfp4_router:
-        result["nvfp4_router"] = measure_decode_config(stream, "qwen3_30b_a3b_nvfp4_router",
-                                                       (1, 2, 3, 4))
+        result["nvfp4_router"] = measure_config(stream, "qwen3_30b_a3b_nvfp4_router",
+                                                (1, 2, 3, 4), l2)
     if rank == 0 and not args.no_zero_experts:
-        result["zero_experts"] = measure_decode_config(stream, "qwen3_30b_a3b_zero_experts",
-                                                       (1, 2, 3, 4))
+        result["zero_experts"] = measure_config(stream, "qwen3_30b_a3b_zero_experts",
+                                                (1, 2, 3, 4), l2)
     if rank == 0:
         result["clocks"] = clk.summary()
         if not args.no_cpu_baseline:
@@ -583,9 +630,12 @@ def cpu_baseline(spec, tokens, budget_s: float):
 
 
 def run_reference(args):
-    """Reference arm: the FP64 oracle on the host cores (rank 0 only); one step
-    is the same N sweep as our arm; K steps after W warm-up steps, stopped
-    early (and reported as such) once the sample reaches its time budget."""
+    """Reference arm: the FP64 oracle on the host cores (rank 0 only).  Each
+    step is a bounded sample of our arm's step: one moe_forward call of the N
+    sweep, round-robin over the token counts (the whole sweep takes over a
+    second on the host); when K such steps would exceed --ref-seconds (timed
+    on the warm-up steps), every step is the N = 1 call instead.  Exactly W
+    warm-up and K timed steps."""
     rank, world, _ = _dist()
     if rank != 0:
         return
@@ -594,27 +644,30 @@ def run_reference(args):
     spec = synth.CONFIGS[args.config]
     tokens = [n for n in spec.tokens if n <= 64] if args.tokens is None else args.tokens
     host = synth.make_layer(spec)
-    xs = [synth.make_tokens(spec, N, seed=70000 + N) for N in tokens]
-    for _ in range(min(args.warmup, 2)):
-        for x in xs:
-            oracle.moe_forward(host, x)
-    nbytes, steps, t0 = 0, 0, time.perf_counter()
-    while steps < args.steps:
-        for N, x in zip(tokens, xs):
-            r = oracle.moe_forward(host, x)
-            nbytes += algorithmic_bytes(spec, r["idx"], N)["total"]
-        steps += 1
-        if time.perf_counter() - t0 > args.ref_seconds:
-            break
+    xs = {N: synth.make_tokens(spec, N, seed=70000 + N) for N in tokens}
+    t0 = time.perf_counter()
+    for s_ in range(args.warmup):
+        oracle.moe_forward(host, xs[tokens[s_ % len(tokens)]])
+    per_call = (time.perf_counter() - t0) / max(1, args.warmup)
+    if args.warmup == 0:
+        t0 = time.perf_counter()
+        oracle.moe_forward(host, xs[tokens[0]])
+        per_call = time.perf_counter() - t0
+    order = tokens if per_call * args.steps <= args.ref_seconds else [min(tokens)]
+    nbytes, t0 = 0, time.perf_counter()
+    for s_ in range(args.steps):
+        N = order[s_ % len(order)]
+        r = oracle.moe_forward(host, xs[N])
+        nbytes += algorithmic_bytes(spec, r["idx"], N)["total"]
     dt = time.perf_counter() - t0
     v = nbytes / dt / 1e9
-    sample = (f"{steps} of {args.steps} steps of moe_forward at N={','.join(map(str, tokens))} on "
-              f"{spec.name} ({dt:.1f} s)")
+    sample = (f"{args.steps} steps, each one moe_forward call on {spec.name}, N round-robin over "
+              f"{','.join(map(str, order))} ({dt:.1f} s)")
     print(json.dumps({
         "impl": "reference",
         "metric": METRIC,
-        "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": steps,
-        "warmup": min(args.warmup, 2), "ms_per_step": round(dt / steps * 1e3, 3),
+        "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt / max(1, args.steps) * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (same seeded layer as our arm)",
         "config": {"workload": f"{spec.name} layer, one step = moe_forward at N={','.join(map(str, tokens))}"},
@@ -634,7 +687,7 @@ def main():
     ap.add_argument("--tokens", type=int, nargs="*", default=None)
     ap.add_argument("--copies", type=int, default=16)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--ref-seconds", type=float, default=120.0)
+    ap.add_argument("--ref-seconds", type=float, default=180.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram read+write bytes per launch from an ncu capture of this kernel")
     ap.add_argument("--no-graph", action="store_true")
@@ -650,8 +703,9 @@ def main():
                     help="skip the NVFP4-router decode measurement")
     ap.add_argument("--no-zero-experts", action="store_true",
                     help="skip the zero-expert routing decode measurement")
-    ap.add_argument("--no-grouped", action="store_true",
-                    help="skip the grouped-path (gpt-oss N=512) measurement")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-layer-shape records (all five shapes, gpt-oss N=512 "
+                         "on the grouped path)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
