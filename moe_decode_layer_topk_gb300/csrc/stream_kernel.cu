@@ -499,15 +499,9 @@ __device__ void router_phase(const StreamParams& p, SkTab& tb, uint8_t* smem, in
     a = warp_sum(a);
     if (lane == 0) part[w] = a;
   }
-  // this CTA's rows of the output accumulator start at zero; ordered before
-  // the logits (release) and so before every CTA's reductions, which follow
-  // its gather of all logits (acquire)
-  {
-    const int r0 = divs(c * H, G), r1 = divs((c + 1) * H, G);
-    const int ld = (N + 1) & ~1;
-#pragma unroll 1
-    for (int i = r0 * ld + tid; i < r1 * ld; i += kT) p.oacc[i] = 0.f;
-  }
+  // this CTA's output accumulator rows (zeroed at kernel start) are ordered
+  // before the logits (release) and so before every CTA's reductions, which
+  // follow its gather of all logits (acquire)
   __syncthreads();
   if (tid < nq * N) fence_gpu();
 #pragma unroll 1
@@ -596,10 +590,65 @@ __device__ __forceinline__ uint2 select_rounds(uint32_t (&key)[4], const uint32_
 // of one token from its W local lists (W*k <= 128 candidates).  Both levels
 // read (key, expert) pairs from shared memory: `pairs` [N][E] for level 0,
 // `cand` [N][W*k] for level 1.
+// Selection key of logit v (expert e) given the token's softmax max / sum.
+__device__ __forceinline__ uint32_t sel_key(const StreamParams& p, const SkTab& tb, float v, int e,
+                                            float gm, float gd) {
+  float sc = v;
+  if (p.scoring == 1) sc = sigmoid_fast(v) + tb.bias[e];
+  if (p.scoring == 2) sc = exp_fast(v - gm) * rcp_fast(gd) + tb.bias[e];
+  return okey(sc);
+}
+// Routing weights of token n's selections (lane j < k holds selection j,
+// expert e), stored with the experts.
+__device__ __forceinline__ void sel_weights(const StreamParams& p, SkTab& tb, const float* lg, int n,
+                                            int e, float gm, float gd, int lane) {
+  const int k = p.k;
+  float w = 0.f;
+  if (lane < k) {
+    const float v = lg[n * p.E + e];
+    w = p.scoring != 1 ? exp_fast(v - gm) * rcp_fast(gd) : sigmoid_fast(v);
+  }
+  const float ws = warp_sum(w);
+  if (lane < k) {
+    if (p.norm) w *= rcp_fast(ws);
+    if (p.scoring != 0) w *= p.rsf;
+    tb.sel_e[n * k + lane] = (int16_t)e;
+    tb.sel_w[n * k + lane] = w;
+  }
+}
+
 __device__ void routing(const StreamParams& p, SkTab& tb, const float* lg, uint2* pairs,
                         uint2* cand, int warp, int lane) {
   const int E = p.E, N = p.N, k = p.k;
   const int W = (E + 127) >> 7;   // warps per token
+  if (W == 1) {
+    // at most 128 experts: one warp per token, keys in registers
+    if (warp < N) {
+      const int n = warp;
+      float v[4], m = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? lg[n * E + e] : -INFINITY;
+        m = fmaxf(m, v[i]);
+      }
+      m = warp_max(m);
+      float d = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d += exp_fast(v[i] - m);   // exp(-inf) = 0
+      d = warp_sum(d);
+      uint32_t key[4], idx[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int e = lane + 32 * i;
+        idx[i] = e < E ? (uint32_t)e : 0xFFFFFFFFu;
+        key[i] = e < E ? sel_key(p, tb, v[i], e, m, d) : 0u;
+      }
+      const uint2 sel = select_rounds(key, idx, k, lane);
+      sel_weights(p, tb, lg, n, sel.y < (uint32_t)E ? (int)sel.y : 0, m, d, lane);
+    }
+    return;
+  }
   // softmax statistics of each token's 128-expert parts
 #pragma unroll 1
   for (int task = warp; task < N * W; task += kW) {
@@ -636,11 +685,7 @@ __device__ void routing(const StreamParams& p, SkTab& tb, const float* lg, uint2
 #pragma unroll 1
   for (int w = threadIdx.x; w < N * E; w += kT) {
     const int n = divs(w, E), e = w - n * E;
-    const float v = lg[w];
-    float sc = v;
-    if (p.scoring == 1) sc = sigmoid_fast(v) + tb.bias[e];
-    if (p.scoring == 2) sc = exp_fast(v - tb.gmax[n]) * rcp_fast(tb.gden[n]) + tb.bias[e];
-    pairs[w] = make_uint2(okey(sc), (uint32_t)e);
+    pairs[w] = make_uint2(sel_key(p, tb, lg[w], e, tb.gmax[n], tb.gden[n]), (uint32_t)e);
   }
   __syncthreads();
 #pragma unroll 1
@@ -679,21 +724,9 @@ __device__ void routing(const StreamParams& p, SkTab& tb, const float* lg, uint2
     __syncthreads();
   }
   // weights of the selected experts
-  if (warp < N) {
-    const int n = warp;
-    const int e = lane < k ? tb.sel_e[n * k + lane] : 0;
-    float w = 0.f;
-    if (lane < k) {
-      const float v = lg[n * E + e];
-      w = p.scoring != 1 ? exp_fast(v - tb.gmax[n]) * rcp_fast(tb.gden[n]) : sigmoid_fast(v);
-    }
-    const float ws = warp_sum(w);
-    if (lane < k) {
-      if (p.norm) w *= rcp_fast(ws);
-      if (p.scoring != 0) w *= p.rsf;
-      tb.sel_w[n * k + lane] = w;
-    }
-  }
+  if (warp < N)
+    sel_weights(p, tb, lg, warp, lane < k ? tb.sel_e[warp * k + lane] : 0, tb.gmax[warp],
+                tb.gden[warp], lane);
 }
 
 // Unique experts of the N*k selections (first-selection order), with the
@@ -1256,6 +1289,13 @@ __global__ void __launch_bounds__(kSkThreads, 1) moe_stream_kernel(const __grid_
   // the call's inputs: the first DRAM round trip on the critical path
   const int nq = c < p.E ? divs(p.E - 1 - c, G) + 1 : 0;   // router rows of this CTA
   issue_inputs(p, smem, c, G, nq, tid);
+  {
+    // this CTA's rows of the FP32 output accumulator start at zero (the
+    // stores retire while the copies are in flight)
+    const int r0 = divs(c * p.H, G), r1 = divs((c + 1) * p.H, G), ld = (p.N + 1) & ~1;
+#pragma unroll 1
+    for (int i = r0 * ld + tid; i < r1 * ld; i += kT) p.oacc[i] = 0.f;
+  }
   if (tid == 0) {
     // the call's tag: the counter moves by exactly 256 per call (G <= 256):
     // CTA 0 adds 257 - G and the others 1, so every CTA of call c reads a
