@@ -175,8 +175,8 @@ MOE_API size_t moe_workspace_size(const moe_layer_desc_t* desc, int32_t max_toke
 /* The path moe_forward (and moe_route, moe_forward_ids, moe_forward_host)
  * takes for N token rows of this layer: 1 = the grouped path (eight
  * kernels: router, top-k, plan, gather, gate/up GEMM, pack, down GEMM,
- * combine; moe_route stops after the top-k), 0 = the fused decode kernel
- * (one kernel), -1 = invalid descriptor or N < 1.  Host-only: makes no
+ * combine; moe_route stops after the top-k), 0 = one fused kernel (the
+ * stream or the decode kernel), -1 = invalid descriptor or N < 1.  Host-only: makes no
  * CUDA call.  The rule is the one moe_forward's description states; the
  * grouped path refuses the layers it does not run (MOE_ERR_UNSUPPORTED). */
 MOE_API int32_t moe_uses_grouped_path(const moe_layer_desc_t* desc, int32_t N);
@@ -194,13 +194,16 @@ MOE_API moe_status_t moe_workspace_init(void* workspace, size_t ws_bytes, void* 
  *   topk_w    f32 [N, top_k] device or NULL: their routing weights
  *   workspace device, >= moe_workspace_size(desc, N) bytes, zeroed once by
  *             moe_workspace_init; one workspace per concurrently running call
- * N*top_k <= 256 runs one fused decode kernel, N*top_k > 256 the grouped
- * path (per-expert token groups on the tcgen05 tensor cores, the grouped
- * GEMM forward_batched.rs switches to for larger row counts).  Layers the
- * grouped path runs (NVFP4 / MXFP4 experts, no shared expert, no zero
- * experts, no hash routing) whose experts hold >= 1 MiB of weights
- * (3 * inter * H * (1/2 + 1/gs) bytes) take it from N*top_k >= 128, where
- * it is the faster of the two.  The grouped path takes neither a shared
+ * Paths: up to 8 token rows of a layer with NVFP4 / MXFP4 experts, a BF16
+ * router, no zero experts and no hash routing run one cooperative stream
+ * kernel (router, top-k, gate/up, SiLU, down and the shared-expert blend in
+ * one launch); other layers with N*top_k <= 256 run one fused decode kernel;
+ * N*top_k > 256 runs the grouped path (per-expert token groups on the tcgen05
+ * tensor cores, the grouped GEMM forward_batched.rs switches to for larger
+ * row counts).  Layers the grouped path runs (NVFP4 / MXFP4 experts, no
+ * shared expert, no zero experts, no hash routing) whose experts hold >= 1 MiB
+ * of weights (3 * inter * H * (1/2 + 1/gs) bytes) take it for every N > 8,
+ * where it is the faster path.  The grouped path takes neither a shared
  * expert, BF16 / FP8 routed experts nor zero experts yet: N*top_k > 256
  * with shared_inter > 0, wfmt MOE_W_BF16 / MOE_W_FP8 or zero_experts > 0
  * returns MOE_ERR_UNSUPPORTED.  With zero experts, topk_idx
@@ -295,6 +298,15 @@ MOE_API moe_status_t moe_forward_noalloc(const moe_layer_desc_t* desc,
  * a test can drive the MOE_ERR_TIMEOUT path without stalling the GPU.  After
  * such a call, re-initialise the workspace with moe_workspace_init. */
 MOE_API void moe_debug_set_wait_budget_ns(unsigned long long ns);
+
+/* Tuning hook: the number of (token, slot) pairs, N x top_k, from which a
+ * layer with FP4 experts of at least 1 MiB (and no shared expert, zero experts
+ * or hash routing) takes the grouped path instead of the fused kernels; 0 or a
+ * negative value restores the built-in rule (grouped for N > 8, measured to
+ * win there on GB300).  Affects calls and moe_workspace_size /
+ * moe_uses_grouped_path from then on; size workspaces after setting it.  Used
+ * to measure where the paths cross. */
+MOE_API void moe_debug_set_grouped_min_slots(int32_t slots);
 
 #ifdef __cplusplus
 }

@@ -35,6 +35,7 @@ MOE_R_NVFP4 = 1
 EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_forward", "moe_route",
             "moe_host_staging_size", "moe_forward_host", "moe_get_error", "moe_status_string",
             "moe_abi_version", "moe_debug_set_wait_budget_ns", "moe_forward_noalloc",
+            "moe_debug_set_grouped_min_slots",
             "moe_forward_ids", "moe_uses_grouped_path")
 
 
@@ -101,6 +102,8 @@ def load() -> ctypes.CDLL:
         L.moe_forward_ids.argtypes = [pd, pw, vp, vp, i32, vp, vp, vp, vp, sz, vp]
         L.moe_debug_set_wait_budget_ns.restype = None
         L.moe_debug_set_wait_budget_ns.argtypes = [ctypes.c_ulonglong]
+        L.moe_debug_set_grouped_min_slots.restype = None
+        L.moe_debug_set_grouped_min_slots.argtypes = [i32]
         if L.moe_abi_version() != ABI_VERSION:
             raise RuntimeError("libmoe.so ABI version mismatch; rebuild it")
         _lib = L
@@ -212,3 +215,9 @@ def moe_get_error(ws, stream=None) -> int:
 
 def moe_debug_set_wait_budget_ns(ns: int):
     load().moe_debug_set_wait_budget_ns(int(ns))
+
+
+def moe_debug_set_grouped_min_slots(slots: int):
+    """Pairs N x top_k from which large FP4 layers take the grouped path
+    (0 restores the built-in threshold); size workspaces afterwards."""
+    load().moe_debug_set_grouped_min_slots(int(slots))

@@ -152,19 +152,22 @@ bool grouped_capable(const moe_layer_desc_t& d) {
 }
 
 // The decode kernel takes up to kMaxSlots (token, slot) pairs.  Layers the
-// grouped path runs switch to it from kGroupedMinSlots pairs when an expert
-// holds at least kGroupedMinExpertBytes of weights: there its GEMMs stream
-// the experts about twice as fast (GB300, same experts touched: gpt-oss
-// shape 750 us at N = 65 against 2022 us for the decode kernel at N = 64;
-// Qwen3 shape 181 us at N = 33 against 322 us at N = 32).  Monotone in N, so
-// a workspace sized for max_tokens covers every smaller N.
-constexpr long long kGroupedMinSlots = 128;
+// grouped path runs, with experts of at least kGroupedMinExpertBytes, take it
+// for every N beyond the stream kernel's kSkMaxTok rows: measured on GB300
+// (decode kernel against grouped path, layer copies cycled past L2), the
+// grouped GEMMs win from N = 9 on (gpt-oss shape 414 / 254 us at N = 9,
+// 677 / 377 us at N = 16, 2045 / 750 us at N = 64; Qwen3 shape 125 / 119 us
+// at N = 9, 188 / 146 us at N = 16).  moe_debug_set_grouped_min_slots
+// replaces the rule by a (token, slot) pair threshold.  Monotone in N, so a
+// workspace sized for max_tokens covers every smaller N.
 constexpr double kGroupedMinExpertBytes = 1024.0 * 1024.0;
+long long g_grouped_min_slots = 0;   // 0: the N > kSkMaxTok rule
 
 bool grouped_path(const moe_layer_desc_t& d, int32_t N) {
   const long long slots = (long long)N * d.top_k;
   if (slots > moe::kMaxSlots) return true;
-  if (slots < kGroupedMinSlots || !grouped_capable(d)) return false;
+  if (!grouped_capable(d)) return false;
+  if (g_grouped_min_slots > 0 ? slots < g_grouped_min_slots : N <= moe::kSkMaxTok) return false;
   const double per_byte = 0.5 + (d.wfmt == MOE_W_NVFP4 ? 1.0 / 16 : 1.0 / 32);   // codes + scales
   return 3.0 * d.inter * d.H * per_byte >= kGroupedMinExpertBytes;
 }
@@ -847,5 +850,9 @@ moe_status_t moe_forward_noalloc(const moe_layer_desc_t* desc, const moe_weights
  * already satisfied expire at once, which exercises the MOE_ERR_TIMEOUT path
  * without hanging the GPU. */
 void moe_debug_set_wait_budget_ns(unsigned long long ns) { g_timeout_ns = ns; }
+
+/* Tuning hook: (token, slot) pairs from which layers with large FP4 experts
+ * take the grouped path; slots <= 0 restores the built-in rule. */
+void moe_debug_set_grouped_min_slots(int32_t slots) { g_grouped_min_slots = slots > 0 ? slots : 0; }
 
 }  // extern "C"

@@ -96,18 +96,26 @@ def _forward(lib, d, w, N=1, x=1 << 24, out=1 << 25, ws=1 << 26, ws_bytes=1 << 3
 
 
 def test_dispatch_rule(lib):
-    """Decode kernel up to 256 (token, slot) pairs, grouped path beyond; FP4
+    """Fused kernels up to 256 (token, slot) pairs, grouped path beyond; FP4
     layers without a shared expert, zero experts or hash routing whose
-    experts hold >= 1 MiB of weights switch at 128 pairs.  Host-only."""
+    experts hold >= 1 MiB of weights switch for N > 8 (the measured
+    crossing); the tuning hook replaces that by a pair threshold.  Host-only."""
     from moe_decode_layer_topk_gb300.device import layer_desc
 
     def g(spec, N):
         return _lib.moe_uses_grouped_path(layer_desc(spec), N)
 
     oss, q3 = synth.CONFIGS["gpt_oss_120b"], synth.CONFIGS["qwen3_30b_a3b"]
-    assert [g(oss, n) for n in (1, 4, 31, 32, 64, 65, 512)] == [0, 0, 0, 1, 1, 1, 1]
-    assert [g(q3, n) for n in (1, 4, 15, 16, 32, 33)] == [0, 0, 0, 1, 1, 1]
+    assert [g(oss, n) for n in (1, 4, 8, 9, 16, 64, 65, 512)] == [0, 0, 0, 1, 1, 1, 1, 1]
+    assert [g(q3, n) for n in (1, 4, 8, 9, 16, 33)] == [0, 0, 0, 1, 1, 1]
     assert g(synth.CONFIGS["qwen3_30b_a3b_nvfp4_router"], 16) == 1
+    try:
+        _lib.moe_debug_set_grouped_min_slots(128)
+        assert [g(oss, n) for n in (31, 32)] == [0, 1]
+        assert [g(q3, n) for n in (15, 16)] == [0, 1]
+    finally:
+        _lib.moe_debug_set_grouped_min_slots(0)
+    assert [g(oss, n) for n in (8, 9)] == [0, 1]
     for name in ("deepseek_v3", "mtp_verify", "qwen3_30b_a3b_bf16", "qwen3_30b_a3b_fp8",
                  "qwen3_30b_a3b_zero_experts"):       # decode up to the slot limit
         sp = synth.CONFIGS[name]
