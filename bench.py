@@ -142,39 +142,34 @@ def algorithmic_bytes(spec, idx: np.ndarray, N: int) -> dict:
     return {"U": U, "routed": routed, "total": routed + other}
 
 
-def decode_traffic(calls, launches_per_cycle: int):
-    """DRAM bytes per decode-kernel launch from the committed ncu record
+def stream_traffic(calls):
+    """DRAM bytes per stream-kernel launch from the committed ncu record
     (profiles/traffic.json), or None when the kernel source changed since the
-    counters were taken.  Token counts without their own capture are scaled
-    from the captured ones by algorithmic bytes (traffic/algorithmic ratio)."""
+    counters were taken.  Calls whose token count has no capture are scaled
+    from the captured ones by algorithmic bytes (mean traffic/algorithmic
+    ratio of the captured launches)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "moe_decode_layer_topk_gb300", "csrc", "decode_kernel.cu")
     try:
         rec = json.load(open(path))
+        src = os.path.join(ROOT, rec["kernel_source"])
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    except (OSError, ValueError):
+    except (OSError, ValueError, KeyError):
         return None, "no record"
-    if rec.get("decode_kernel_cu_sha256") != h:
-        return None, "kernel changed since the ncu capture"
+    if rec.get("kernel_source_sha256") != h:
+        return None, f"{rec['kernel_source']} changed since the ncu capture"
     meas, alg = rec["dram_bytes_per_launch"], rec["algorithmic_bytes_per_launch"]
     ratio = float(np.mean([meas[k] / alg[k] for k in meas]))
-    tot, scaled = 0.0, False
-    for c in calls:
-        key = str(c[1])
-        if key in meas:
-            tot += meas[key]
-        else:
-            tot += ratio * c[5]["total"]
-            scaled = True
-    note = rec["source"] + ("; other token counts scaled by algorithmic bytes" if scaled else "")
+    tot = sum(ratio * c[5]["total"] for c in calls)
+    note = (rec["source"] + f"; per-launch traffic of this line's calls = their algorithmic bytes "
+            f"x {ratio:.4f}, the measured traffic/algorithmic ratio")
     return tot / len(calls), note
 
 
 def kernels_per_call(spec, N: int) -> int:
-    """Kernels one moe_forward enqueues, as the library reports its path: the
-    fused decode kernel, or the grouped chain (router, top-k, plan, gather,
-    gate/up GEMM, pack, down GEMM, combine)."""
+    """Kernels one moe_forward enqueues, as the library reports its path: one
+    fused kernel (the stream or the decode kernel), or the grouped chain
+    (router, top-k, plan, gather, gate/up GEMM, pack, down GEMM, combine)."""
     from moe_decode_layer_topk_gb300 import _lib
     from moe_decode_layer_topk_gb300.device import layer_desc
     g = _lib.moe_uses_grouped_path(layer_desc(spec), N)
@@ -479,8 +474,7 @@ def run_gpu(args):
                "h2d_bytes_per_step": io, "d2h_bytes_per_step": io}
 
     peak, peak_kind = _peaks()
-    traffic, traffic_note = (args.traffic, "--traffic") if args.traffic else \
-        decode_traffic(calls[:launches_per_cycle], launches_per_cycle)
+    traffic, traffic_note = (args.traffic, "--traffic") if args.traffic else stream_traffic(calls)
     result = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -511,7 +505,7 @@ def run_gpu(args):
                      "traffic": None if traffic is None else int(traffic),
                      "traffic_source": traffic_note,
                      "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
-                     "kernel": "moe::moe_decode_kernel"},
+                     "kernel": "moe::moe_stream_kernel"},
         "gpu_launches": kernels_timed,
         "e2e": e2e,
     }
