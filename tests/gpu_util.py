@@ -41,3 +41,16 @@ def run_forward(dev: DeviceLayer, x_bits: np.ndarray, ws=None, token_ids=None):
     assert _lib.moe_get_error(ws) == _lib.MOE_OK
     return (out.view(torch.int16).cpu().numpy().view(np.uint16), idx.cpu().numpy(),
             w.cpu().numpy())
+
+
+def record_headroom(name: str, N: int, err: float, tol: float, path: str = None):
+    """Append one parity case's max|err| and tolerance as a JSON line to the
+    file named by MOE_PARITY_HEADROOM (nothing when it is unset)."""
+    import json
+    import os
+    path = path or os.environ.get("MOE_PARITY_HEADROOM")
+    if not path:
+        return
+    with open(path, "a") as f:
+        f.write(json.dumps({"case": name, "N": int(N), "max_err": float(err), "tol": float(tol),
+                            "ratio": float(err) / float(tol)}) + "\n")

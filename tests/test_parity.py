@@ -14,7 +14,7 @@ from moe_decode_layer_topk_gb300 import synth
 from moe_decode_layer_topk_gb300.device import DeviceLayer
 from oracle import compare, margin, oracle
 
-from .gpu_util import full_layer, run_forward, spec_from
+from .gpu_util import full_layer, record_headroom, run_forward, spec_from
 
 NV, MX, BF, F8 = synth.NVFP4, synth.MXFP4, synth.BF16, synth.FP8
 SM, SB, SMB = synth.SOFTMAX, synth.SIGMOID_BIAS, synth.SOFTMAX_BIAS
@@ -188,4 +188,5 @@ FULL = [(name, N) for name in ("tiny", "qwen3_30b_a3b", "mtp_verify", "deepseek_
 def test_full_size(name, N):
     host, dev = full_layer(name)
     x = margin.tokens_with_margin(host, N)
-    _check(host, dev, x)
+    err, tol = _check(host, dev, x)
+    record_headroom(name, N, err, tol)
