@@ -175,10 +175,10 @@ MOE_API size_t moe_workspace_size(const moe_layer_desc_t* desc, int32_t max_toke
 /* The path moe_forward (and moe_route, moe_forward_ids, moe_forward_host)
  * takes for N token rows of this layer: 1 = the grouped path (eight
  * kernels: router, top-k, plan, gather, gate/up GEMM, pack, down GEMM,
- * combine; moe_route stops after the top-k), 0 = one fused kernel (the
- * stream or the decode kernel), -1 = invalid descriptor or N < 1.  Host-only: makes no
- * CUDA call.  The rule is the one moe_forward's description states; the
- * grouped path refuses the layers it does not run (MOE_ERR_UNSUPPORTED). */
+ * combine; moe_route stops after the top-k), 0 = the fused kernels (the
+ * stream or the decode kernel, one launch per row chunk), -1 = invalid
+ * descriptor or N < 1.  Host-only: makes no CUDA call.  The rule is the one
+ * moe_forward's description states. */
 MOE_API int32_t moe_uses_grouped_path(const moe_layer_desc_t* desc, int32_t N);
 
 /* Zero a workspace before its first use (and after MOE_ERR_TIMEOUT).  Enqueues
@@ -204,9 +204,10 @@ MOE_API moe_status_t moe_workspace_init(void* workspace, size_t ws_bytes, void* 
  * shared expert, no zero experts, no hash routing) whose experts hold >= 1 MiB
  * of weights (3 * inter * H * (1/2 + 1/gs) bytes) take it for every N > 8,
  * where it is the faster path.  The grouped path takes neither a shared
- * expert, BF16 / FP8 routed experts nor zero experts yet: N*top_k > 256
- * with shared_inter > 0, wfmt MOE_W_BF16 / MOE_W_FP8 or zero_experts > 0
- * returns MOE_ERR_UNSUPPORTED.  With zero experts, topk_idx
+ * expert, BF16 / FP8 routed experts, zero experts nor hash routing yet: such
+ * layers with N*top_k > 256 run the fused kernels in row chunks of
+ * floor(256 / top_k) tokens, one after another on the stream (each chunk
+ * reads its touched experts' weights again).  With zero experts, topk_idx
  * holds indices up to E + Z - 1 (>= E: a zero expert).  Asynchronous on `stream`; no host synchronisation,
  * no allocation, so it may be captured in a CUDA graph.  Argument errors are
  * returned before anything is enqueued; device-side timeouts are reported by
@@ -221,8 +222,9 @@ MOE_API moe_status_t moe_forward(const moe_layer_desc_t* desc, const moe_weights
  * [0, hash_vocab)); token n's experts are tid2eid row token_ids[n] in table
  * order (ids outside [0, E) are clamped), weighted as top-k routing weights
  * are for the layer's scoring.  A hash-routed layer refuses moe_forward,
- * moe_route and the other entry points (MOE_ERR_INVALID_ARG: no token ids),
- * and N*top_k > 256 (MOE_ERR_UNSUPPORTED).  Otherwise as moe_forward. */
+ * moe_route and the other entry points (MOE_ERR_INVALID_ARG: no token ids).
+ * N*top_k > 256 runs in row chunks as moe_forward describes.  Otherwise as
+ * moe_forward. */
 MOE_API moe_status_t moe_forward_ids(const moe_layer_desc_t* desc, const moe_weights_t* weights,
                                      const void* x, const int32_t* token_ids, int32_t N,
                                      void* out, int32_t* topk_idx, float* topk_w,

@@ -165,8 +165,8 @@ long long g_grouped_min_slots = 0;   // 0: the N > kSkMaxTok rule
 
 bool grouped_path(const moe_layer_desc_t& d, int32_t N) {
   const long long slots = (long long)N * d.top_k;
+  if (!grouped_capable(d)) return false;   // run() splits such calls into row chunks
   if (slots > moe::kMaxSlots) return true;
-  if (!grouped_capable(d)) return false;
   if (g_grouped_min_slots > 0 ? slots < g_grouped_min_slots : N <= moe::kSkMaxTok) return false;
   const double per_byte = 0.5 + (d.wfmt == MOE_W_NVFP4 ? 1.0 / 16 : 1.0 / 32);   // codes + scales
   return 3.0 * d.inter * d.H * per_byte >= kGroupedMinExpertBytes;
@@ -575,6 +575,23 @@ moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* 
       return MOE_ERR_CUDA;
     return MOE_OK;
   };
+  if ((long long)N * d->top_k > moe::kMaxSlots && !grouped_capable(*d)) {
+    // layers the grouped path does not take (a shared expert, BF16 / FP8
+    // experts, zero experts, hash routing): the fused kernels in row chunks
+    // of kMaxSlots / top_k tokens, one after another on the stream (each
+    // chunk streams its experts again)
+    const int32_t C = moe::kMaxSlots / d->top_k;
+    for (int32_t n0 = 0; n0 < N; n0 += C) {
+      const int32_t nc = std::min(C, N - n0);
+      const size_t xo = (size_t)n0 * d->H, so = (size_t)n0 * d->top_k;
+      st = run(d, w, static_cast<const uint16_t*>(x) + xo, nc,
+               out ? static_cast<uint16_t*>(out) + xo : nullptr, topk_idx ? topk_idx + so : nullptr,
+               topk_w ? topk_w + so : nullptr, ws, ws_bytes, stream, route_only,
+               token_ids ? token_ids + n0 : nullptr, clear_head);
+      if (st != MOE_OK) return st;
+    }
+    return MOE_OK;
+  }
   if (grouped_path(*d, N))
     return run_grouped(d, w, x, N, out, topk_idx, topk_w, ws, ws_bytes, stream, route_only, head);
   if (stream_capable(*d, N)) {

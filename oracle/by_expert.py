@@ -11,8 +11,10 @@ tokens of one expert taken together: each expert's projections are
 dequantised once by the oracle (oracle_dequant, FP64) and applied to its
 tokens with FP64 matrix products (numpy), so every token's result is the
 same sum of the same FP64 products as in the per-token loop, in another
-order.  Routing comes from the oracle (router logits + route).  Layers with
-a shared expert or hash routing are not taken here.
+order.  Routing comes from the oracle (router logits + route).  A shared
+expert (BF16) is added the same way over all tokens, times its gate
+sigmoid(w_s . x) when the layer has a gate vector.  Hash-routed layers are
+not taken here.
 """
 from __future__ import annotations
 
@@ -32,10 +34,10 @@ def _bf16_rows(x_bits: np.ndarray) -> np.ndarray:
 
 def moe_forward_by_expert(layer, x: np.ndarray) -> dict:
     """-> dict(out_f64 [N, H], idx [N, k], w [N, k]) for a synth.HostLayer
-    without a shared expert (zero experts allowed: they add nothing)."""
+    with FP4 routed experts (zero experts allowed: they add nothing)."""
     sp = layer.spec
-    if sp.shared_inter or sp.hash_vocab or sp.wfmt not in ("nvfp4", "mxfp4"):
-        raise ValueError("by-expert oracle: FP4 experts, no shared expert or hash routing")
+    if sp.hash_vocab or sp.wfmt not in ("nvfp4", "mxfp4"):
+        raise ValueError("by-expert oracle: FP4 experts, no hash routing")
     x = np.ascontiguousarray(x, dtype=np.uint16)
     N, H = x.shape
     logits = oracle.layer_router_logits(layer, x)
@@ -62,4 +64,13 @@ def moe_forward_by_expert(layer, x: np.ndarray) -> dict:
     with concurrent.futures.ThreadPoolExecutor(max(1, min(16, os.cpu_count() or 1))) as ex:
         for rows, part in ex.map(one, experts):
             out[rows] += part
+    if sp.shared_inter:
+        g = xf @ _bf16_rows(layer.sh_gate).T
+        u = xf @ _bf16_rows(layer.sh_up).T
+        sh = (g / (1.0 + np.exp(-g)) * u) @ _bf16_rows(layer.sh_down).T
+        gate = np.ones(N)
+        if layer.sh_gate_w is not None:
+            d = xf @ _bf16_rows(layer.sh_gate_w)
+            gate = 1.0 / (1.0 + np.exp(-d))
+        out += gate[:, None] * sh
     return {"out_f64": out, "idx": idx, "w": w}

@@ -96,10 +96,11 @@ def _forward(lib, d, w, N=1, x=1 << 24, out=1 << 25, ws=1 << 26, ws_bytes=1 << 3
 
 
 def test_dispatch_rule(lib):
-    """Fused kernels up to 256 (token, slot) pairs, grouped path beyond; FP4
-    layers without a shared expert, zero experts or hash routing whose
-    experts hold >= 1 MiB of weights switch for N > 8 (the measured
-    crossing); the tuning hook replaces that by a pair threshold.  Host-only."""
+    """Fused kernels up to 256 (token, slot) pairs, grouped path beyond for
+    the layers it takes (FP4 experts, no shared expert, zero experts or hash
+    routing; the others stay fused, in row chunks); those whose experts hold
+    >= 1 MiB of weights switch for N > 8 (the measured crossing); the tuning
+    hook replaces that by a pair threshold.  Host-only."""
     from moe_decode_layer_topk_gb300.device import layer_desc
 
     def g(spec, N):
@@ -117,9 +118,9 @@ def test_dispatch_rule(lib):
         _lib.moe_debug_set_grouped_min_slots(0)
     assert [g(oss, n) for n in (8, 9)] == [0, 1]
     for name in ("deepseek_v3", "mtp_verify", "qwen3_30b_a3b_bf16", "qwen3_30b_a3b_fp8",
-                 "qwen3_30b_a3b_zero_experts"):       # decode up to the slot limit
+                 "qwen3_30b_a3b_zero_experts"):       # no grouped path: fused, in row chunks
         sp = synth.CONFIGS[name]
-        assert (g(sp, 256 // sp.top_k), g(sp, 256 // sp.top_k + 1)) == (0, 1), name
+        assert (g(sp, 256 // sp.top_k), g(sp, 256 // sp.top_k + 1), g(sp, 512)) == (0, 0, 0), name
     tiny = synth.CONFIGS["tiny"]                      # 55 KB experts
     assert (g(tiny, 128), g(tiny, 129)) == (0, 1)
     assert g(tiny, 0) == -1
@@ -131,11 +132,15 @@ def test_argument_refusals_happen_before_any_cuda_call(lib):
     """Every case below is refused by the host checks (no GPU needed)."""
     d, w = _desc(), _fake_weights()
     assert _forward(lib, d, w, N=0) == _lib.MOE_ERR_INVALID_ARG
-    # N*k > 256 takes the grouped path: its own workspace check, and no shared expert yet
+    # N*k > 256 takes the grouped path: its own workspace check; a layer it
+    # does not take (here a shared expert) runs the fused kernels in row chunks
     assert _forward(lib, d, w, N=300, ws_bytes=1 << 20) == _lib.MOE_ERR_WORKSPACE_TOO_SMALL
     assert _lib.moe_workspace_size(d, 300) > _lib.moe_workspace_size(d, 128)
-    assert _forward(lib, _desc(shared_inter=64), _fake_weights(shared=True), N=300) == \
-        _lib.MOE_ERR_UNSUPPORTED
+    dsh = _desc(shared_inter=64)
+    assert _lib.moe_uses_grouped_path(dsh, 300) == 0
+    assert _lib.moe_workspace_size(dsh, 300) == _lib.moe_workspace_size(dsh, 128)
+    assert _forward(lib, dsh, _fake_weights(shared=True), N=300, ws_bytes=1 << 10) == \
+        _lib.MOE_ERR_WORKSPACE_TOO_SMALL
     assert _forward(lib, d, w, x=(1 << 24) + 8) == _lib.MOE_ERR_INVALID_ARG
     assert _forward(lib, d, w, out=None) == _lib.MOE_ERR_INVALID_ARG
     assert _forward(lib, d, w, ws_bytes=16) == _lib.MOE_ERR_WORKSPACE_TOO_SMALL
@@ -148,17 +153,17 @@ def test_argument_refusals_happen_before_any_cuda_call(lib):
     w4 = _fake_weights()                                                  # FP4 experts need scales
     w4.up_s = None
     assert _forward(lib, d, w4) == _lib.MOE_ERR_INVALID_ARG
-    # BF16 routed experts: no grouped path yet (N*k > 256)
+    # BF16 routed experts: no grouped path yet (N*k > 256: row chunks)
     db = _desc(wfmt=_lib.MOE_W_BF16)
     wb = _fake_weights()
     wb.gate_s = wb.up_s = wb.down_s = wb.gate_s2 = wb.up_s2 = wb.down_s2 = None
-    assert _forward(lib, db, wb, N=300) == _lib.MOE_ERR_UNSUPPORTED
+    assert _lib.moe_uses_grouped_path(db, 300) == 0
     wb.gate_q = None
     assert _forward(lib, db, wb) == _lib.MOE_ERR_INVALID_ARG
     # FP8 routed experts: block scales required, no grouped path yet
     d8 = _desc(wfmt=_lib.MOE_W_FP8)
     w8 = _fake_weights()
-    assert _forward(lib, d8, w8, N=300) == _lib.MOE_ERR_UNSUPPORTED
+    assert _lib.moe_uses_grouped_path(d8, 300) == 0
     w8.down_s = None
     assert _forward(lib, d8, w8) == _lib.MOE_ERR_INVALID_ARG
     # NVFP4 router: its scales are required
@@ -173,7 +178,7 @@ def test_argument_refusals_happen_before_any_cuda_call(lib):
     assert _forward(lib, dz, _fake_weights()) == _lib.MOE_ERR_INVALID_ARG
     wz = _fake_weights()
     wz.bias = 1 << 21
-    assert _forward(lib, dz, wz, N=300) == _lib.MOE_ERR_UNSUPPORTED
+    assert _lib.moe_uses_grouped_path(dz, 300) == 0
     assert _lib.moe_workspace_size(dz, 4) > _lib.moe_workspace_size(_desc(), 4)
     # hash routing: token ids required (and only for hash routing), the table
     # required, no grouped path, no zero experts with it
@@ -181,9 +186,7 @@ def test_argument_refusals_happen_before_any_cuda_call(lib):
     dh.hash_vocab = 100
     assert _forward(lib, dh, _fake_weights()) == _lib.MOE_ERR_INVALID_ARG
     ids = 1 << 22
-    assert lib.moe_forward_ids(ctypes.byref(dh), ctypes.byref(_fake_weights()), 1 << 24, ids,
-                               300, 1 << 25, None, None, 1 << 26, 1 << 30,
-                               None) == _lib.MOE_ERR_UNSUPPORTED
+    assert _lib.moe_uses_grouped_path(dh, 300) == 0
     wt = _fake_weights()
     wt.tid2eid = None
     assert lib.moe_forward_ids(ctypes.byref(dh), ctypes.byref(wt), 1 << 24, ids, 1, 1 << 25,

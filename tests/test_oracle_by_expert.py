@@ -24,6 +24,9 @@ CASES = {
                                routed_scaling_factor=2.5),
     "zero_experts": dict(H=256, inter=128, E=16, top_k=4, scoring=synth.SOFTMAX_BIAS,
                          zero_experts=8),
+    "shared_ungated": dict(H=256, inter=96, E=16, top_k=4, scoring=synth.SIGMOID_BIAS,
+                           routed_scaling_factor=2.5, shared_inter=64),
+    "shared_gated": dict(H=256, inter=128, E=24, top_k=6, shared_inter=96, shared_gated=True),
 }
 
 
@@ -44,8 +47,8 @@ def test_by_expert_matches_the_per_token_oracle(case):
     assert np.abs(got["out_f64"] - ref["out_f64"]).max() <= 1e-12 * scale
 
 
-def test_by_expert_refuses_shared_experts():
-    spec = _spec(name="shared", H=256, inter=128, E=8, top_k=2, shared_inter=64)
+def test_by_expert_refuses_other_expert_formats():
+    spec = _spec(name="bf16", H=256, inter=128, E=8, top_k=2, wfmt=synth.BF16)
     host = synth.make_layer(spec, seed=1)
     with pytest.raises(ValueError):
         moe_forward_by_expert(host, synth.make_tokens(spec, 2, seed=2))
