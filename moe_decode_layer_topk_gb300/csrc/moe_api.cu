@@ -547,7 +547,26 @@ bool stream_params(moe::StreamParams& p, const moe_layer_desc_t* d, const moe_we
   p.shpart = reinterpret_cast<float*>(b + L.shpart);
   p.oacc = reinterpret_cast<float*>(b + L.oacc);
   p.timeout_ns = g_timeout_ns;
-  return moe::plan_stream(p, budget, grid);
+  if (!moe::plan_stream(p, budget, grid)) return false;
+  // weight codes by TMA: gate / up rows [E*inter, H/2] (16-row boxes), down
+  // rows [E*H, inter/2] (32-row boxes), the shared down rows [H, 2*Is] bytes
+  const uint64_t E = (uint64_t)d->E;
+  if (!encode_2d(&p.tm_gq, w->gate_q, d->H / 2, E * d->inter, 64, 0, 16) ||
+      !encode_2d(&p.tm_uq, w->up_q, d->H / 2, E * d->inter, 64, 0, 16) ||
+      !encode_2d(&p.tm_dq, w->down_q, d->inter / 2, E * d->H, 64, 0, 32))
+    return false;
+  if (d->shared_inter > 0 &&
+      !encode_2d(&p.tm_shd, w->sh_down, 2 * (uint64_t)d->shared_inter, d->H, 64, 0, 32))
+    return false;
+  // block scales by TMA where each scale row is a multiple of 16 bytes,
+  // otherwise by per-lane 4-byte copies
+  const int gs = d->wfmt == MOE_W_NVFP4 ? 16 : 32;
+  const uint64_t shb = d->H / gs, sib = d->inter / gs;
+  p.sc_tma = shb % 16 == 0 && sib % 16 == 0 &&
+             encode_2d(&p.tm_gs, w->gate_s, shb, E * d->inter, 16, 0, 16) &&
+             encode_2d(&p.tm_us, w->up_s, shb, E * d->inter, 16, 0, 16) &&
+             encode_2d(&p.tm_ds, w->down_s, sib, E * d->H, 16, 0, 32);
+  return true;
 }
 
 moe_status_t run(const moe_layer_desc_t* d, const moe_weights_t* w, const void* x, int32_t N,

@@ -147,6 +147,15 @@ constexpr int kSkMaxGrid = 256;   // CTAs; bounds the shared-expert K-part slots
 constexpr uint32_t kErrRange = 8u;       // an activation left the f16 range
 
 struct StreamParams {
+  // tensor maps of the weight codes (2D uint8 [rows, row bytes]): gate / up
+  // box 64 B x 16 rows, down box 64 B x 32 rows; the shared expert's down rows
+  // (BF16 [H, Is] as bytes) box 64 B x 32 rows
+  CUtensorMap tm_gq, tm_uq, tm_dq, tm_shd;
+  // and of the block scales (2D uint8 [rows, K / gs]) when their rows are
+  // 16-byte multiples (sc_tma): gate / up box 16 B x 16 rows (two NVFP4 or
+  // four MXFP4 K segments), down box 16 B x 32 rows
+  CUtensorMap tm_gs, tm_us, tm_ds;
+  int sc_tma;
   // layer
   int H, inter, E, k, scoring, norm, fmt, N, Is, route_only;
   float rsf;

@@ -86,6 +86,7 @@ struct SkTab {
   float u_w[kMaxSlots][kSkMaxTok];
   int16_t u_slot[kMaxSlots][kSkMaxTok];
   uint32_t split_cnt[kSkSplitSlots];
+  uint64_t full[kSkWarps][4];   // per warp and ring stage: the stage's TMA bytes have landed
   float part[kSkMaxTok][8][2];   // per token and 128-expert part: max, sum exp(l - max)
   uint32_t xmax[kSkMaxTok];   // max |x| per token (float bits)
   float xdot[kSkMaxTok];       // w_s . x per token
@@ -103,6 +104,11 @@ __device__ __forceinline__ void cpa16w(uint32_t dst, const void* src, uint32_t n
 __device__ __forceinline__ void cpa4w(uint32_t dst, const void* src, uint32_t n) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(n)
                : "memory");
+}
+// Prior generic-proxy accesses to shared memory before later async-proxy
+// (TMA) writes of this thread.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 // 16-byte activation piece (x or h), default L2 policy.
 __device__ __forceinline__ void cpa16(uint32_t dst, const void* src, uint32_t n) {
@@ -149,12 +155,6 @@ __device__ __forceinline__ void fence_gpu() { asm volatile("fence.acq_rel.gpu;" 
 
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-__device__ __forceinline__ float h_lo(uint32_t v) {
-  return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu)));
-}
-__device__ __forceinline__ float h_hi(uint32_t v) {
-  return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
-}
 
 // floor(log2(m)) of a positive finite float.
 __device__ __forceinline__ int ilog2f(float m) {
@@ -947,7 +947,8 @@ __device__ __forceinline__ void cpa_wait_d() {
 // tile (gate and up rows g; row g+8 is 8 * rb further), advanced by one
 // segment per item.
 struct GuIssue {
-  const uint8_t *qg, *qu, *sg, *su;
+  const uint8_t *sg, *su;   // this lane's scale words (row g)
+  int row0;                 // first row of the tile in the [E * inter] code tensors
   int seg, tl;
 };
 template <int FMT>
@@ -956,10 +957,9 @@ __device__ __forceinline__ void gu_issue_tile(const StreamParams& p, const SkTab
   constexpr int gsz = FMT == FMT_NVFP4 ? 16 : 32;
   const int i = P.c + P.G * s.tl;
   const int u = divs(i, P.tpe), j = i - u * P.tpe;
-  const size_t row = (size_t)tb.u_e[u] * p.inter + 16 * j + P.g;
+  s.row0 = tb.u_e[u] * p.inter + 16 * j;
+  const size_t row = (size_t)s.row0 + P.g;
   const size_t so = row * (p.H / gsz) + (FMT == FMT_NVFP4 ? 2 * P.t : P.t);
-  s.qg = p.gq + row * (p.H / 2) + 16 * P.t;
-  s.qu = p.uq + row * (p.H / 2) + 16 * P.t;
   s.sg = p.gsc + (so & ~(size_t)3);
   s.su = p.usc + (so & ~(size_t)3);
 }
@@ -969,7 +969,8 @@ __device__ __forceinline__ void gu_issue_tile(const StreamParams& p, const SkTab
 // reaches past the end.
 template <int FMT, bool SH>
 __device__ __forceinline__ void dn_issue(const StreamParams& p, SkTab& tb, const Pipe& P,
-                                         const DCur& d, uint32_t dc, uint32_t da, bool& sh_waited) {
+                                         const DCur& d, uint8_t* dst, uint64_t* bar, uint32_t da,
+                                         uint8_t* daux, bool& sh_waited) {
   constexpr int gsz = FMT == FMT_NVFP4 ? 16 : 32;
   const int rr = 32 * d.m + P.g;   // rows rr + 8 i, i < 4 (H is a multiple of 32)
   const int o = 64 * d.seg + 16 * P.t;
@@ -984,10 +985,10 @@ __device__ __forceinline__ void dn_issue(const StreamParams& p, SkTab& tb, const
       sh_waited = true;
     }
     const int rb = 2 * p.Is;
-    const uint8_t* base = reinterpret_cast<const uint8_t*>(p.shd);
-    const uint8_t* q = base + (size_t)rr * rb + o;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) cpa16w(dc + 512 * i, q + 8 * i * rb, 16u);
+    if (P.lane == 0) {
+      mbar_arrive_expect_tx(bar, 2048u);
+      tma_load_2d(dst, &p.tm_shd, 64 * d.seg, 32 * d.m, bar);
+    }
     const bool vx = P.g < p.N;
     cpa16(da, reinterpret_cast<const uint8_t*>(p.hs) + (vx ? (size_t)P.g * rb + o : 0),
           vx ? 16u : 0u);
@@ -995,15 +996,29 @@ __device__ __forceinline__ void dn_issue(const StreamParams& p, SkTab& tb, const
     const int rb = p.inter / 2, scb = p.inter / gsz;
     const size_t row = (size_t)tb.u_e[d.u] * p.H + rr;
     const bool kin = o < rb;
-    const uint8_t* q = p.dq + row * rb + o;
-    const size_t so = row * scb + (FMT == FMT_NVFP4 ? 8 : 4) * d.seg + (FMT == FMT_NVFP4 ? 2 * P.t : P.t);
-    const uint8_t* s0 = p.dsc + (so & ~(size_t)3);
+    if (P.lane == 0) {
+      const int y = tb.u_e[d.u] * p.H + 32 * d.m;
+      mbar_arrive_expect_tx(bar, p.sc_tma ? 2560u : 2048u);
+      tma_load_2d(dst, &p.tm_dq, 64 * d.seg, y, bar);
+      if (p.sc_tma)   // the 16-byte scale column holding this segment's, 32 rows
+        tma_load_2d(daux, &p.tm_ds, ((FMT == FMT_NVFP4 ? 8 : 4) * d.seg) & ~15, y, bar);
+    }
+    if (!p.sc_tma) {
+      const size_t so = row * scb + (FMT == FMT_NVFP4 ? 8 : 4) * d.seg + (FMT == FMT_NVFP4 ? 2 * P.t : P.t);
+      const uint8_t* s0 = p.dsc + (so & ~(size_t)3);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      cpa16w(dc + 512 * i, kin ? q + 8 * i * rb : p.dq, kin ? 16u : 0u);
-      cpa4w(da + 4 * i, kin ? s0 + 8 * i * scb : p.dsc, kin ? 4u : 0u);
+      for (int i = 0; i < 4; ++i) cpa4w(da + 4 * i, kin ? s0 + 8 * i * scb : p.dsc, kin ? 4u : 0u);
     }
   }
+}
+
+// Byte offset of lane t's scale word for K segment seg within a 16-byte row
+// of a scale box (NVFP4: 8 bytes per segment, two per box row, the lane's
+// two scales at byte 2t; MXFP4: 4 bytes per segment, four per row, its scale
+// at byte t); the shift inside the word is the one of the per-lane copies.
+template <int FMT>
+__device__ __forceinline__ int scw_t(int seg, int t) {
+  return FMT == FMT_NVFP4 ? ((seg & 1) * 8 + 2 * t) & ~3 : (seg & 3) * 4;
 }
 
 template <int FMT, int D, bool SH>
@@ -1011,6 +1026,7 @@ __device__ void pipeline(const StreamParams& p, SkTab& tb, uint8_t* smem, const 
   constexpr int gsz = FMT == FMT_NVFP4 ? 16 : 32;
   constexpr int sstep = FMT == FMT_NVFP4 ? 8 : 4;   // scale bytes per 128-column segment
   const int ngu = P.a1 - P.a0, ndn = P.b1 - P.b0;
+  const int total = ngu + ndn;
   const int g = P.g, t = P.t, lane = P.lane;
   const int rb = p.H / 2;
   const int s8 = 8 * (p.H / gsz);   // scale bytes of 8 rows
@@ -1022,8 +1038,15 @@ __device__ void pipeline(const StreamParams& p, SkTab& tb, uint8_t* smem, const 
   const bool olane = 2 * t < p.N;   // this lane's output columns 2t, 2t+1 hold tokens
   const int old = (p.N + 1) & ~1;   // row stride of the output accumulator
   const int soff_t = FMT == FMT_NVFP4 ? 2 * t : t;
+  auto scw = [](int seg, int tt) { return scw_t<FMT>(seg, tt); };
 
-  // ---- copy-side cursors
+  // ---- copy-side cursors; the code rows of a stage come by TMA (lane 0),
+  // their scale words by per-lane cp.async
+  const int warp = threadIdx.x >> 5;
+  uint8_t* wring = smem + p.off_ring + warp * D * kSkStageCodes;
+  uint8_t* daux = smem + p.off_aux + warp * D * kSkStageAux;   // this warp's side slots
+  const uint32_t auxw = smem_u32(daux);
+  uint64_t* full = tb.full[warp];
   int islot = 0;
   GuIssue gi;
   gi.tl = divs(P.a0, P.S);
@@ -1034,38 +1057,58 @@ __device__ void pipeline(const StreamParams& p, SkTab& tb, uint8_t* smem, const 
   int dleft = ndn;   // down items not yet copied
   bool sh_waited = false;
   auto issue_next = [&](int k) {   // k-th item of this warp's sequence
-    const uint32_t dc = P.ring + (uint32_t)(islot * 2048), da = P.aux + (uint32_t)(islot * 512);
+    const uint32_t da = P.aux + (uint32_t)(islot * 512);
+    uint8_t* dst = wring + islot * 2048;
+    if (k < total) {
+      // the stage was last read (generic proxy) by the item consumed just
+      // before; order those reads before the TMA's writes
+      __syncwarp();
+      if (lane == 0) fence_proxy_async_smem();
+    }
     if (k < ngu) {
       const int o = 64 * gi.seg;
       const bool kin = o + 16 * t < rb;
-      const uint32_t n = kin ? 16u : 0u;
-      const int oo = kin ? o : 0;
-      cpa16w(dc, gi.qg + oo, n);
-      cpa16w(dc + 512, gi.qg + oo + 8 * rb, n);
-      cpa16w(dc + 1024, gi.qu + oo, n);
-      cpa16w(dc + 1536, gi.qu + oo + 8 * rb, n);
-      const int so = kin ? sstep * gi.seg : 0;
-      const uint32_t n4 = kin ? 4u : 0u;
-      cpa4w(da, gi.sg + so, n4);
-      cpa4w(da + 4, gi.sg + so + s8, n4);
-      cpa4w(da + 8, gi.su + so, n4);
-      cpa4w(da + 12, gi.su + so + s8, n4);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full + islot, p.sc_tma ? 2560u : 2048u);
+        tma_load_2d(dst, &p.tm_gq, o, gi.row0, full + islot);
+        tma_load_2d(dst + 1024, &p.tm_uq, o, gi.row0, full + islot);
+        if (p.sc_tma) {   // the 16-byte scale column holding this segment's, 16 rows
+          const int sx = (sstep * gi.seg) & ~15;
+          tma_load_2d(daux + islot * 512, &p.tm_gs, sx, gi.row0, full + islot);
+          tma_load_2d(daux + islot * 512 + 256, &p.tm_us, sx, gi.row0, full + islot);
+        }
+      }
+      if (!p.sc_tma) {
+        const int so = kin ? sstep * gi.seg : 0;
+        const uint32_t n4 = kin ? 4u : 0u;
+        cpa4w(da, gi.sg + so, n4);
+        cpa4w(da + 4, gi.sg + so + s8, n4);
+        cpa4w(da + 8, gi.su + so, n4);
+        cpa4w(da + 12, gi.su + so + s8, n4);
+      }
       if (++gi.seg == P.S) {
         gi.seg = 0;
         ++gi.tl;
         if (k + 1 < ngu) gu_issue_tile<FMT>(p, tb, P, gi);
       }
     } else if (dleft > 0) {
-      dn_issue<FMT, SH>(p, tb, P, di, dc, da, sh_waited);
+      dn_issue<FMT, SH>(p, tb, P, di, dst, full + islot, da, daux + islot * 512, sh_waited);
       dcur_next<SH>(P, di);
       --dleft;
     }
     islot = islot + 1 == D ? 0 : islot + 1;
   };
   int cslot = 0;
+  // item h's stage: its TMA bytes (phase h / D of the stage's mbarrier) and
+  // its scale copies (cp.async group)
+  auto wait_stage = [&](int h) {
+    if (!mbar_wait_bounded(full + cslot, (uint32_t)(h / D) & 1u, p.timeout_ns) && lane == 0)
+      set_error(p, tb, kErrTimeoutStage);
+    cpa_wait_d<D>();
+  };
   // gate/up consume state
   int ctl = divs(P.a0, P.S), cseg = P.a0 - ctl * P.S;
-  int cur_tile = -1, done = 0, u = 0, j = 0, csh = 0;
+  int cur_tile = -1, done = 0, u = 0, j = 0, csh = 0, useg = 0;
   float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
   float s2g = 1.f, s2u = 1.f, s2d = 1.f;
   // down consume state
@@ -1073,7 +1116,6 @@ __device__ void pipeline(const StreamParams& p, SkTab& tb, uint8_t* smem, const 
   dcur_init<SH>(P, P.b0, cd);
   int du = -2, dseg = -1, dsh = 0;
   uint32_t b[16];
-  const int total = ngu + ndn;
   // one loop over this warp's items (gate/up, then down) with the copies of
   // item h + D - 1 issued at step h; steps before 0 only fill the ring
 #pragma unroll 1
@@ -1176,6 +1218,7 @@ __device__ void pipeline(const StreamParams& p, SkTab& tb, uint8_t* smem, const 
         b[4 * ii + 2] = v.z;
         b[4 * ii + 3] = v.w;
       }
+      useg = cseg;
       ++done;
       if (++cseg == P.S) {
         cseg = 0;
@@ -1185,7 +1228,7 @@ __device__ void pipeline(const StreamParams& p, SkTab& tb, uint8_t* smem, const 
       // shared-expert down item (BF16 rows, B copied with them)
       float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
       const uint32_t sc = P.ring + (uint32_t)(cslot * 2048);
-      cpa_wait_d<D>();
+      wait_stage(h);
       const uint4 bv = lds128(P.aux + (uint32_t)(cslot * 512));
       seg_bf16(c0, lds128(sc), lds128(sc + 512), bv);
       seg_bf16(c1, lds128(sc + 1024), lds128(sc + 1536), bv);
@@ -1214,7 +1257,7 @@ __device__ void pipeline(const StreamParams& p, SkTab& tb, uint8_t* smem, const 
              tag, b);
     }
     // the item's FP4 rows: gate and up (two row pairs) or down (one)
-    cpa_wait_d<D>();
+    wait_stage(h);
     {
       const uint32_t m16 = FMT == FMT_NVFP4 ? 0xFFFFu : 0xFFu;
       const uint32_t sc = P.ring + (uint32_t)(cslot * 2048), sa = P.aux + (uint32_t)(cslot * 512);
@@ -1222,7 +1265,14 @@ __device__ void pipeline(const StreamParams& p, SkTab& tb, uint8_t* smem, const 
       float fa, fb;
       if (h < ngu) {
         // gate and up: two independent MMA chains
-        const uint4 av = lds128(sa);
+        uint4 av;
+        if (p.sc_tma) {
+          // box rows of 16 bytes: gate rows at 0, up rows at 256
+          const uint32_t wb = auxw + (uint32_t)(cslot * 512 + g * 16 + scw(useg, t));
+          av = make_uint4(lds32(wb), lds32(wb + 128), lds32(wb + 256), lds32(wb + 384));
+        } else {
+          av = lds128(sa);
+        }
         const uint4 g0 = lds128(sc), g8 = lds128(sc + 512);
         const uint4 u0 = lds128(sc + 1024), u8 = lds128(sc + 1536);
         if (FMT == FMT_NVFP4) {
@@ -1249,7 +1299,13 @@ __device__ void pipeline(const StreamParams& p, SkTab& tb, uint8_t* smem, const 
       } else {
         // down: two row pairs (rows 32m + g + 8i, i < 4), two MMA chains;
         // the partial sums (columns 2t, 2t+1) go to the output accumulator
-        const uint4 sw = lds128(sa);
+        uint4 sw;
+        if (p.sc_tma) {   // box rows of 16 bytes: rows g, g + 8, g + 16, g + 24
+          const uint32_t wb = auxw + (uint32_t)(cslot * 512 + g * 16 + scw(cd.seg, t));
+          sw = make_uint4(lds32(wb), lds32(wb + 128), lds32(wb + 256), lds32(wb + 384));
+        } else {
+          sw = lds128(sa);
+        }
         float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
         float fc, fd;
         seg_scales<FMT>((sw.x >> dsh) & m16, (sw.y >> dsh) & m16, a0, a1, b0, b1, fa, fb);
@@ -1310,6 +1366,12 @@ __global__ void __launch_bounds__(kSkThreads, 1) moe_stream_kernel(const __grid_
     if (p.scoring != 0) tb.bias[e] = __ldg(p.bias + e);
   }
   if (tid < kSkSplitSlots) tb.split_cnt[tid] = 0u;
+  if (lane == 0) {
+    // this warp's ring stages: one arrival (lane 0's expect_tx) per use
+#pragma unroll 1
+    for (int s = 0; s < D; ++s) mbar_init(&tb.full[warp][s], 1u);
+    fence_mbar_init();
+  }
   if (tid < kSkMaxTok) {
     tb.xmax[tid] = 0u;
     tb.xdot[tid] = 0.f;
