@@ -139,7 +139,11 @@ struct Params {
 constexpr int kSkWarps = 16;
 constexpr int kSkThreads = kSkWarps * 32;
 constexpr int kSkMaxTok = 8;       // MMA N: every token of a call is one column
-constexpr int kSkMaxStages = 8;    // cp.async ring depth per warp
+// Weight ring depth per warp: the item being computed plus one in flight.
+// One 2.5 KB item per warp in flight (about 6 MB over the grid) keeps HBM
+// busy, and a shallower queue lets the first items and the gate/up -> down
+// hand-off through sooner (2 stages measured faster than 3 or 4 at every N).
+constexpr int kSkStages = 2;
 constexpr int kSkSplitSlots = 16;  // gate/up tiles shared by several warps of one CTA
 constexpr int kSkStageCodes = 4 * 32 * 16;   // bytes per warp and stage: 4 pieces of 16 B per lane
 constexpr int kSkStageAux = 32 * 16;     // 16 B per lane: block-scale words or a B piece
@@ -187,7 +191,7 @@ struct StreamParams {
   float* shpart;                // [Is/16, sh_parts, 256] K-part partial sums of shared tiles
   float* oacc;                  // [H, N rounded up to even] FP32 output accumulator (zeroed each call)
   // geometry
-  int stages;                   // cp.async ring depth
+  int stages;                   // weight ring depth (kSkStages)
   int sh_parts;                 // K-parts of one shared gate/up tile
   int off_ring, off_aux, off_x16, off_tab, off_split, smem_bytes;
   unsigned long long timeout_ns;

@@ -86,7 +86,7 @@ struct SkTab {
   float u_w[kMaxSlots][kSkMaxTok];
   int16_t u_slot[kMaxSlots][kSkMaxTok];
   uint32_t split_cnt[kSkSplitSlots];
-  uint64_t full[kSkWarps][4];   // per warp and ring stage: the stage's TMA bytes have landed
+  uint64_t full[kSkWarps][kSkStages];   // per warp and ring stage: the stage's TMA bytes have landed
   float part[kSkMaxTok][8][2];   // per token and 128-expert part: max, sum exp(l - max)
   uint32_t xmax[kSkMaxTok];   // max |x| per token (float bits)
   float xdot[kSkMaxTok];       // w_s . x per token
@@ -1502,58 +1502,49 @@ bool plan_stream(StreamParams& p, int smem_budget, int grid) {
   off = al(off + kSkSplitSlots * 256 * 4);
   p.off_x16 = off;
   off = al(off + S * 4 * p.N * 64);
-  const int per_stage = kSkWarps * (kSkStageCodes + kSkStageAux);
-  int D = (smem_budget - off) / per_stage;
-  if (D > 4) D = 4;   // built for 3 or 4 stages
-  if (D < 3) return false;
-  // the code ring also holds the float logits, their (key, expert) pairs and the top-k
-  // candidates during routing
+  // the ring region: kSkStages code stages per warp once the weights
+  // stream; before that it holds this CTA's router rows, then the float
+  // logits, their (key, expert) pairs and the top-k candidates
   const int Wt = (p.E + 127) / 128;
   if (Wt * p.k > 128) return false;   // the second top-k level holds 4 candidates per lane
-  if (D * kSkWarps * kSkStageCodes < ((p.N * p.E * 4 + 15) & ~15) + p.N * p.E * 8 + p.N * Wt * p.k * 8)
-    return false;
-  // ... and, before that, this CTA's router rows; the router's partial sums
-  // sit in the split area
   const int nq = (p.E + grid - 1) / grid;
-  if (D * kSkWarps * kSkStageCodes < nq * p.H * 2) return false;
+  int ring = kSkStages * kSkWarps * kSkStageCodes;
+  ring = max(ring, ((p.N * p.E * 4 + 15) & ~15) + p.N * p.E * 8 + p.N * Wt * p.k * 8);
+  ring = max(ring, nq * p.H * 2);
+  // the router's partial sums sit in the split area
   if (nq * p.N * ((p.H + 255) / 256) > kSkSplitSlots * 256) return false;
-  p.stages = D;
+  p.stages = kSkStages;
   p.off_ring = off;
-  off += D * kSkWarps * kSkStageCodes;
+  off = al(off + ring);
   p.off_aux = off;
-  off += D * kSkWarps * kSkStageAux;
+  off += kSkStages * kSkWarps * kSkStageAux;
   p.smem_bytes = off;
   return off <= smem_budget;
 }
 
-// The kernel instances: block-scale format x ring depth x shared expert.
-template <int FMT, int D, bool SH>
+// The kernel instances: block-scale format x shared expert.
+template <int FMT, bool SH>
 constexpr const void* sk_fn() {
-  return (const void*)moe_stream_kernel<FMT, D, SH>;
+  return (const void*)moe_stream_kernel<FMT, kSkStages, SH>;
 }
-const void* stream_fn(int fmt, int stages, bool sh) {
-  const bool nv = fmt == FMT_NVFP4;
-  if (stages == 4)
-    return nv ? (sh ? sk_fn<FMT_NVFP4, 4, true>() : sk_fn<FMT_NVFP4, 4, false>())
-              : (sh ? sk_fn<FMT_MXFP4, 4, true>() : sk_fn<FMT_MXFP4, 4, false>());
-  return nv ? (sh ? sk_fn<FMT_NVFP4, 3, true>() : sk_fn<FMT_NVFP4, 3, false>())
-            : (sh ? sk_fn<FMT_MXFP4, 3, true>() : sk_fn<FMT_MXFP4, 3, false>());
+const void* stream_fn(int fmt, bool sh) {
+  return fmt == FMT_NVFP4 ? (sh ? sk_fn<FMT_NVFP4, true>() : sk_fn<FMT_NVFP4, false>())
+                          : (sh ? sk_fn<FMT_MXFP4, true>() : sk_fn<FMT_MXFP4, false>());
 }
 
 cudaError_t stream_set_smem(int smem_bytes) {
   for (int fmt : {FMT_NVFP4, FMT_MXFP4})
-    for (int stages : {3, 4})
-      for (bool sh : {false, true}) {
-        const cudaError_t e = cudaFuncSetAttribute(
-            stream_fn(fmt, stages, sh), cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-        if (e != cudaSuccess) return e;
-      }
+    for (bool sh : {false, true}) {
+      const cudaError_t e = cudaFuncSetAttribute(stream_fn(fmt, sh),
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+      if (e != cudaSuccess) return e;
+    }
   return cudaSuccess;
 }
 
 cudaError_t launch_stream(const StreamParams& p, int grid, cudaStream_t stream) {
   void* args[] = {const_cast<StreamParams*>(&p)};
-  return cudaLaunchCooperativeKernel(stream_fn(p.fmt, p.stages, p.Is > 0), dim3(grid),
+  return cudaLaunchCooperativeKernel(stream_fn(p.fmt, p.Is > 0), dim3(grid),
                                      dim3(kSkThreads), args, (size_t)p.smem_bytes, stream);
 }
 
