@@ -31,21 +31,21 @@
 //       shared-memory accumulator and the last warp finalises it:
 //       h = w * scale2_down * SiLU(g) * u goes to f16 per (token, slot) and
 //       the tile is tagged with the call number.
-//   P3  down: each CTA owns H / G output rows (16-row MMA tiles); the warps
-//       split the (shared K segment, row tile) and (expert, K segment, row
-//       tile) items; a routed item waits only for the eight gate/up tiles its
-//       K segment reads.  Partial tiles meet in shared memory, and the CTA
-//       writes its output rows once, in BF16: no atomics in global memory and
-//       no second pass.  The item pipeline runs from P2 straight into P3, so
-//       the first down weights are in flight while the last gate/up items
-//       compute.
+//   P3  down: the grid's (shared K segment, row tile) and (expert, K segment,
+//       32-row tile) items are split over all warps in order; a routed item
+//       waits only for the eight gate/up tiles its K segment reads.  Partial
+//       sums go to an FP32 accumulator in global memory by vector reductions;
+//       once every CTA has counted itself done at the end counter, each CTA
+//       converts its H / G output rows to BF16.  The item pipeline runs from
+//       P2 straight into P3, so the first down weights are in flight while
+//       the last gate/up items compute.
 //
-// Weight streaming: every lane copies its own 16-byte pieces (32 E2M1 codes,
-// or 8 BF16 weights, of one row) with cp.async into its slot of a per-warp
-// ring of `stages` stages, plus a 16-byte side slot (the two 4-byte words
-// holding its block scales, or its piece of the B operand), so the bytes in
-// flight are bounded by shared memory, not registers, and each lane reads
-// back only what it copied.
+// Weight streaming: an item's code rows (16 rows x 64 bytes of gate and of
+// up, or 32 rows x 64 bytes of down) come by TMA, issued by lane 0, into the
+// warp's two-stage ring, with their block scales as a 16-byte column of the
+// scale rows by TMA too (by per-lane 4-byte copies when scale rows are not
+// 16-byte multiples); one mbarrier per stage counts the bytes.  With one item
+// in flight per warp the grid keeps about 6 MB of weight reads queued.
 //
 // Arithmetic: E2M1 -> f16 by cvt, times the E4M3 block scale (exact in f16:
 // at most 6 significant bits, range 2^-10 .. 2688), or for MXFP4 times
@@ -81,6 +81,7 @@ struct SkTab {
   float sel_w[kMaxSlots];
   uint32_t first[kMaxE];
   float bias[kMaxE];
+  float s2[kMaxE][3];   // per-expert second-level scales: gate, up, down (1 without)
   int16_t u_e[kMaxSlots];
   uint32_t u_mask[kMaxSlots];
   float u_w[kMaxSlots][kSkMaxTok];
@@ -1200,9 +1201,9 @@ __device__ void pipeline(const StreamParams& p, SkTab& tb, uint8_t* smem, const 
         const int e = tb.u_e[u];
         const size_t row = (size_t)e * p.inter + 16 * j + g;
         csh = 8 * (int)((row * (p.H / gsz) + soff_t) & 3u);
-        s2g = p.g2 ? __ldg(p.g2 + e) : 1.f;
-        s2u = p.u2 ? __ldg(p.u2 + e) : 1.f;
-        s2d = p.d2 ? __ldg(p.d2 + e) : 1.f;
+        s2g = tb.s2[e][0];
+        s2u = tb.s2[e][1];
+        s2d = tb.s2[e][2];
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) ag[qq] = au[qq] = 0.f;
         done = 0;
@@ -1364,6 +1365,10 @@ __global__ void __launch_bounds__(kSkThreads, 1) moe_stream_kernel(const __grid_
   for (int e = tid; e < p.E; e += kT) {
     tb.first[e] = 0xFFFFFFFFu;
     if (p.scoring != 0) tb.bias[e] = __ldg(p.bias + e);
+    // read once here, off the weight stream's path
+    tb.s2[e][0] = p.g2 ? __ldg(p.g2 + e) : 1.f;
+    tb.s2[e][1] = p.u2 ? __ldg(p.u2 + e) : 1.f;
+    tb.s2[e][2] = p.d2 ? __ldg(p.d2 + e) : 1.f;
   }
   if (tid < kSkSplitSlots) tb.split_cnt[tid] = 0u;
   if (lane == 0) {
