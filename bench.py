@@ -161,8 +161,7 @@ def stream_traffic(calls):
     meas, alg = rec["dram_bytes_per_launch"], rec["algorithmic_bytes_per_launch"]
     ratio = float(np.mean([meas[k] / alg[k] for k in meas]))
     tot = sum(ratio * c[5]["total"] for c in calls)
-    note = (rec["source"] + f"; per-launch traffic of this line's calls = their algorithmic bytes "
-            f"x {ratio:.4f}, the measured traffic/algorithmic ratio")
+    note = f"ncu dram read+write (profiles/traffic.json) = {ratio:.4f} x algorithmic bytes"
     return tot / len(calls), note
 
 
