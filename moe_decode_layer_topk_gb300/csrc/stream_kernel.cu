@@ -626,6 +626,7 @@ __device__ void routing(const StreamParams& p, SkTab& tb, const float* lg, uint2
     // at most 128 experts: one warp per token, keys in registers
     if (warp < N) {
       const int n = warp;
+      const int scoring = p.scoring;
       float v[4], m = -INFINITY;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -633,20 +634,38 @@ __device__ void routing(const StreamParams& p, SkTab& tb, const float* lg, uint2
         v[i] = e < E ? lg[n * E + e] : -INFINITY;
         m = fmaxf(m, v[i]);
       }
-      m = warp_max(m);
-      float d = 0.f;
+      // the softmax statistics over all E: needed by softmax + bias keys and
+      // by softmax weights left unnormalised; softmax weights renormalised
+      // over the selection only need a common reference (the top logit)
+      const bool stats = scoring == 2 || (scoring == 0 && !p.norm);
+      float d = 1.f;
+      if (stats) {
+        m = warp_max(m);
+        d = 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) d += exp_fast(v[i] - m);   // exp(-inf) = 0
-      d = warp_sum(d);
+        for (int i = 0; i < 4; ++i) d += exp_fast(v[i] - m);   // exp(-inf) = 0
+        d = warp_sum(d);
+      }
       uint32_t key[4], idx[4];
+      if (scoring == 0) {   // selection by the logit itself
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int e = lane + 32 * i;
-        idx[i] = e < E ? (uint32_t)e : 0xFFFFFFFFu;
-        key[i] = e < E ? sel_key(p, tb, v[i], e, m, d) : 0u;
+        for (int i = 0; i < 4; ++i) {
+          const int e = lane + 32 * i;
+          idx[i] = e < E ? (uint32_t)e : 0xFFFFFFFFu;
+          key[i] = e < E ? okey(v[i]) : 0u;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int e = lane + 32 * i;
+          idx[i] = e < E ? (uint32_t)e : 0xFFFFFFFFu;
+          key[i] = e < E ? sel_key(p, tb, v[i], e, m, d) : 0u;
+        }
       }
       const uint2 sel = select_rounds(key, idx, k, lane);
-      sel_weights(p, tb, lg, n, sel.y < (uint32_t)E ? (int)sel.y : 0, m, d, lane);
+      const int es = sel.y < (uint32_t)E ? (int)sel.y : 0;
+      if (!stats) m = lg[n * E + __shfl_sync(0xffffffffu, es, 0)];
+      sel_weights(p, tb, lg, n, es, m, d, lane);
     }
     return;
   }
@@ -1441,10 +1460,12 @@ __global__ void __launch_bounds__(kSkThreads, 1) moe_stream_kernel(const __grid_
   P.nsh = P.Sds * P.MT;
   {
     // the grid's down items split over all warps in order
-    const long long tot = P.nsh + (long long)tb.U * P.Sd * P.MT;
-    const long long gw = (long long)c * kW + warp, nw = (long long)G * kW;
-    P.b0 = (int)(gw * tot / nw);
-    P.b1 = (int)((gw + 1) * tot / nw);
+    // floor(gw * tot / nw) in 32-bit pieces: gw * r < nw^2 <= 2^24
+    const uint32_t tot = (uint32_t)(P.nsh + tb.U * P.Sd * P.MT);
+    const uint32_t gw = (uint32_t)(c * kW + warp), nw = (uint32_t)(G * kW);
+    const uint32_t q = tot / nw, r = tot - q * nw;
+    P.b0 = (int)(gw * q + gw * r / nw);
+    P.b1 = (int)((gw + 1) * q + (gw + 1) * r / nw);
   }
   if (!tb.abort) pipeline<FMT, D, SH>(p, tb, smem, P);
 
