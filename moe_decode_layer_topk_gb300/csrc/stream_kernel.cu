@@ -500,30 +500,32 @@ __device__ void router_phase(const StreamParams& p, SkTab& tb, uint8_t* smem, in
     a = warp_sum(a);
     if (lane == 0) part[w] = a;
   }
-  // this CTA's output accumulator rows (zeroed at kernel start) are ordered
-  // before the logits (release) and so before every CTA's reductions, which
-  // follow its gather of all logits (acquire)
+  // published by the last nq * N threads, whose fence at kernel start
+  // released this CTA's zeroed accumulator rows
   __syncthreads();
-  if (tid < nq * N) fence_gpu();
-#pragma unroll 1
-  for (int qn = tid; qn < nq * N; qn += kT) {
-    const int q = divs(qn, N), n = qn - q * N;
+  {
+    const int qn = kT - 1 - tid;
+    if (qn < nq * N) {
+      const int q = divs(qn, N), n = qn - q * N;
     float s = 0.f;
 #pragma unroll 1
-    for (int b = 0; b < nb; ++b) s += part[qn * nb + b];
-    st_relaxed64(p.logits + (size_t)n * E + c + G * q,
-                 ((unsigned long long)tb.tag << 32) | __float_as_uint(s));
+      for (int b = 0; b < nb; ++b) s += part[qn * nb + b];
+      st_relaxed64(p.logits + (size_t)n * E + c + G * q,
+                   ((unsigned long long)tb.tag << 32) | __float_as_uint(s));
+    }
   }
   __syncthreads();   // x_prep converts the x slots in place afterwards
 }
 
-// Poll the call's tagged logits into shared memory (float [N][E]).
+// Poll the call's tagged logits into shared memory (float [N][E]).  The
+// reads are acquires: with the barrier after this, every thread's later
+// reductions follow the publishing CTAs' release of their zeroed rows.
 __device__ void gather_logits(const StreamParams& p, SkTab& tb, float* lg, int tid) {
   const int total = p.N * p.E;
   const uint32_t tag = tb.tag;
   #pragma unroll 1
   for (int w = tid; w < total; w += kT) {
-    unsigned long long v = ld_relaxed64(p.logits + w);
+    unsigned long long v = ld_acquire64(p.logits + w);
     if ((uint32_t)(v >> 32) != tag) {
       const uint64_t t0 = global_timer_ns();
       do {
@@ -533,12 +535,11 @@ __device__ void gather_logits(const StreamParams& p, SkTab& tb, float* lg, int t
           break;
         }
         __nanosleep(100);
-        v = ld_relaxed64(p.logits + w);
+        v = ld_acquire64(p.logits + w);
       } while ((uint32_t)(v >> 32) != tag);
     }
     lg[w] = __uint_as_float((uint32_t)v);
   }
-  fence_gpu();   // acquire: every CTA's zeroed accumulator rows precede its logits
 }
 
 // Selection key, order preserving as unsigned: larger key = larger score.
@@ -1366,11 +1367,17 @@ __global__ void __launch_bounds__(kSkThreads, 1) moe_stream_kernel(const __grid_
   const int nq = c < p.E ? divs(p.E - 1 - c, G) + 1 : 0;   // router rows of this CTA
   issue_inputs(p, smem, c, G, nq, tid);
   {
-    // this CTA's rows of the FP32 output accumulator start at zero (the
-    // stores retire while the copies are in flight)
+    // this CTA's rows of the FP32 output accumulator start at zero.  The
+    // threads that later publish the logits (the last nq * N) release these
+    // stores now, while the input copies are in flight: a fence here and
+    // their logit stores after it make the release pattern that orders the
+    // zeros before every other CTA's reductions, which follow its acquire
+    // reads of the logits
     const int r0 = divs(c * p.H, G), r1 = divs((c + 1) * p.H, G), ld = (p.N + 1) & ~1;
 #pragma unroll 1
     for (int i = r0 * ld + tid; i < r1 * ld; i += kT) p.oacc[i] = 0.f;
+    __syncthreads();
+    if (tid >= kT - nq * p.N) fence_gpu();
   }
   if (tid == 0) {
     // the call's tag: the counter moves by exactly 256 per call (G <= 256):
