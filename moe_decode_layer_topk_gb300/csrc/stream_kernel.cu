@@ -418,17 +418,28 @@ __device__ void x_prep(const StreamParams& p, SkTab& tb, uint8_t* smem, int tid)
   const int H = p.H, N = p.N;
   const int pieces = ((H + 127) >> 7) * 16 * N;
   uint4* xs = reinterpret_cast<uint4*>(smem + p.off_x16);
+  const int lane = tid & 31;
+  // whole warps per step (every lane runs every step), so the per-token
+  // maxima reduce within the warp first: one shared atomic per warp and token
 #pragma unroll 1
-  for (int idx = tid; idx < pieces; idx += kT) {
-    int n, k0;
-    x_coords(idx, N, n, k0);
-    const uint4 v = xs[idx];
+  for (int base = tid & ~31; base < pieces; base += kT) {
+    const int idx = base + lane;
+    int n = -1, k0 = 0;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (idx < pieces) {
+      x_coords(idx, N, n, k0);
+      v = xs[idx];
+    }
     const uint32_t xa[4] = {v.x, v.y, v.z, v.w};
     float m = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf_lo(xa[j])), fabsf(bf_hi(xa[j]))));
-    atomicMax(&tb.xmax[n], __float_as_uint(m));   // non-negative floats order as integers
-    if (p.shw && k0 < H) {
+#pragma unroll 1
+    for (int t = 0; t < N; ++t) {   // non-negative floats order as integers
+      const uint32_t mt = __reduce_max_sync(0xffffffffu, n == t ? __float_as_uint(m) : 0u);
+      if (lane == 0 && mt) atomicMax(&tb.xmax[t], mt);
+    }
+    if (n >= 0 && p.shw && k0 < H) {
       const uint4 wv = ld_nc_u4(p.shw + k0);
       const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w};
       float d = 0.f;
