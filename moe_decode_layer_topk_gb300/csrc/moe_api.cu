@@ -269,9 +269,10 @@ struct TmKey {
   uint64_t inner, rows;
   uint32_t box, box_rows;
   int swz;
+  int promo;   // L2 promotion of the loads, bytes
   bool operator==(const TmKey& o) const {
     return ptr == o.ptr && inner == o.inner && rows == o.rows && box == o.box &&
-           box_rows == o.box_rows && swz == o.swz;
+           box_rows == o.box_rows && swz == o.swz && promo == o.promo;
   }
 };
 struct TmEntry {
@@ -284,8 +285,9 @@ TmEntry g_tm_cache[kTmCache];
 int g_tm_next = 0;
 
 bool encode_2d(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box,
-               int swz, uint32_t box_rows = moe::kRows) {   // swz: 0 none, 64 or 128 (bytes)
-  const TmKey key{ptr, inner, rows, box, box_rows, swz};
+               int swz, uint32_t box_rows = moe::kRows,
+               int promo = 256) {   // swz: 0 none, 64 or 128 (bytes); promo: 128 or 256 (bytes)
+  const TmKey key{ptr, inner, rows, box, box_rows, swz, promo};
   std::lock_guard<std::mutex> lk(g_mu);
   for (auto& e : g_tm_cache)
     if (e.used && e.key == key) {
@@ -310,7 +312,8 @@ bool encode_2d(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t rows,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                swz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                           : swz == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+               promo == 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
   TmEntry& e = g_tm_cache[g_tm_next];
   g_tm_next = (g_tm_next + 1) % kTmCache;
@@ -326,7 +329,7 @@ bool encode_2d(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t rows,
 // columns (kb % 128 == 0) so no box reaches past a row or the tensor.
 bool encode_3d(CUtensorMap* out, const void* ptr, uint64_t kb, uint64_t rows, uint32_t brows) {
   constexpr uint32_t kKey3d = 0x3D3Du;   // cache key marker of the 3D views
-  const TmKey key{ptr, kb, rows, kKey3d, brows, 128};
+  const TmKey key{ptr, kb, rows, kKey3d, brows, 128, 256};
   std::lock_guard<std::mutex> lk(g_mu);
   for (auto& e : g_tm_cache)
     if (e.used && e.key == key) {
@@ -551,12 +554,21 @@ bool stream_params(moe::StreamParams& p, const moe_layer_desc_t* d, const moe_we
   // weight codes by TMA: gate / up rows [E*inter, H/2] (16-row boxes), down
   // rows [E*H, inter/2] (32-row boxes), the shared down rows [H, 2*Is] bytes
   const uint64_t E = (uint64_t)d->E;
+  // Long down lists (at least 8 items per warp at the N * k upper bound on
+  // the units) with an even number of 128-column segments per unit run in
+  // the paired order: warp pairs read the down rows in 128-byte pieces, so
+  // the L2 promotion is the piece, not beyond it.  Short lists keep the
+  // plain order, whose partner segments already run at about the same time.
+  const long long sd = (d->inter + 127) / 128, mt = d->H / 32;
+  p.dpair = sd % 2 == 0 && (d->shared_inter / 32) % 2 == 0 &&
+            (long long)N * d->top_k * sd * mt >= 8LL * grid * moe::kSkWarps;
+  const int dpromo = p.dpair ? 128 : 256;
   if (!encode_2d(&p.tm_gq, w->gate_q, d->H / 2, E * d->inter, 64, 0, 16) ||
       !encode_2d(&p.tm_uq, w->up_q, d->H / 2, E * d->inter, 64, 0, 16) ||
-      !encode_2d(&p.tm_dq, w->down_q, d->inter / 2, E * d->H, 64, 0, 32))
+      !encode_2d(&p.tm_dq, w->down_q, d->inter / 2, E * d->H, 64, 0, 32, dpromo))
     return false;
   if (d->shared_inter > 0 &&
-      !encode_2d(&p.tm_shd, w->sh_down, 2 * (uint64_t)d->shared_inter, d->H, 64, 0, 32))
+      !encode_2d(&p.tm_shd, w->sh_down, 2 * (uint64_t)d->shared_inter, d->H, 64, 0, 32, dpromo))
     return false;
   // block scales by TMA where each scale row is a multiple of 16 bytes,
   // otherwise by per-lane 4-byte copies

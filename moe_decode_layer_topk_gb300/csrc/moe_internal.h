@@ -160,6 +160,7 @@ struct StreamParams {
   // four MXFP4 K segments), down box 16 B x 32 rows
   CUtensorMap tm_gs, tm_us, tm_ds;
   int sc_tma;
+  int dpair;   // down items in the paired order (warp pairs take segments 2p, 2p + 1)
   // layer
   int H, inter, E, k, scoring, norm, fmt, N, Is, route_only;
   float rsf;

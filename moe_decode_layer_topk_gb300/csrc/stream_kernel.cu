@@ -932,11 +932,15 @@ struct Pipe {
   int c, G, g, t, lane;
   uint32_t ring, aux;
   int S, tpe, a0, a1;                    // gate/up: segments per row, tiles per expert, items
-  int Sd, Sds, MT, nsh, b0, b1;          // down: segments, shared segments, row tiles, items
+  int Sd, Sds, MT, nsh, b0, b1;          // down: segments, shared segments, row tiles, entries
+  int sst, spar, sdp;                    // down segment step (1, or 2 when paired), parity, Sd / sst
 };
 
 // Down item cursor: shared-expert items (u < 0) over (segment, row tile),
-// then routed items over (expert, segment, row tile).
+// then routed items over (expert, segment, row tile).  Paired order (sst =
+// 2): the list runs over segment pairs, and the two warps of a pair take
+// segments 2p and 2p + 1 of the same entries (spar = the warp's parity), so
+// the two 64-byte halves of each 128-byte row piece are read together.
 struct DCur {
   int u, seg, m;
 };
@@ -944,27 +948,28 @@ template <bool SH>
 __device__ __forceinline__ void dcur_init(const Pipe& P, int b, DCur& d) {
   if (SH && b < P.nsh) {
     d.u = -1;
-    d.seg = divs(b, P.MT);
-    d.m = b - d.seg * P.MT;
+    const int sp = divs(b, P.MT);
+    d.m = b - sp * P.MT;
+    d.seg = sp * P.sst + P.spar;
   } else {
     const int unit = divs(b - P.nsh, P.MT);
     d.m = (b - P.nsh) - unit * P.MT;
-    d.u = divs(unit, P.Sd);
-    d.seg = unit - d.u * P.Sd;
+    d.u = divs(unit, P.sdp);
+    d.seg = (unit - d.u * P.sdp) * P.sst + P.spar;
   }
 }
 template <bool SH>
 __device__ __forceinline__ void dcur_next(const Pipe& P, DCur& d) {
   if (++d.m == P.MT) {
     d.m = 0;
-    ++d.seg;
+    d.seg += P.sst;
     if (SH && d.u < 0) {
-      if (d.seg == P.Sds) {
-        d.seg = 0;
+      if (d.seg >= P.Sds) {
+        d.seg = P.spar;
         d.u = 0;
       }
-    } else if (d.seg == P.Sd) {
-      d.seg = 0;
+    } else if (d.seg >= P.Sd) {
+      d.seg = P.spar;
       ++d.u;
     }
   }
@@ -1475,12 +1480,20 @@ __global__ void __launch_bounds__(kSkThreads, 1) moe_stream_kernel(const __grid_
   P.Sd = (p.inter + 127) >> 7;
   P.Sds = SH ? p.Is >> 5 : 0;
   P.MT = p.H >> 5;   // 32-row down tiles
-  P.nsh = P.Sds * P.MT;
+  // paired down order where the host chose it (long lists, an even number
+  // of segments per unit)
+  const bool paired = p.dpair != 0;
+  P.sst = paired ? 2 : 1;
+  P.spar = paired ? (warp & 1) : 0;
+  P.sdp = paired ? P.Sd >> 1 : P.Sd;
+  P.nsh = (paired ? P.Sds >> 1 : P.Sds) * P.MT;
   {
     // the grid's down items split over all warps in order
-    // floor(gw * tot / nw) in 32-bit pieces: gw * r < nw^2 <= 2^24
-    const uint32_t tot = (uint32_t)(P.nsh + tb.U * P.Sd * P.MT);
-    const uint32_t gw = (uint32_t)(c * kW + warp), nw = (uint32_t)(G * kW);
+    // floor(gw * tot / nw) in 32-bit pieces: gw * r < nw^2 <= 2^24; a pair
+    // of warps shares one range when paired
+    const uint32_t tot = (uint32_t)(P.nsh + tb.U * P.sdp * P.MT);
+    const uint32_t gw = (uint32_t)(c * kW + warp) >> (paired ? 1 : 0);
+    const uint32_t nw = (uint32_t)(G * kW) >> (paired ? 1 : 0);
     const uint32_t q = tot / nw, r = tot - q * nw;
     P.b0 = (int)(gw * q + gw * r / nw);
     P.b1 = (int)((gw + 1) * q + (gw + 1) * r / nw);
