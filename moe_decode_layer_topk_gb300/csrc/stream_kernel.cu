@@ -1455,7 +1455,12 @@ __global__ void __launch_bounds__(kSkThreads, 1) moe_stream_kernel(const __grid_
       if (p.topk_w) p.topk_w[s] = tb.sel_w[s];
     }
   }
-  if (p.route_only) return;
+  if (p.route_only) {
+    // the end counter moves with the call counter (+256 per call), so the
+    // next full call's end target stays reachable
+    if (tid == 0) atomicAdd(&p.ctrl->fin, c == 0 ? 257ull - G : 1ull);
+    return;
+  }
   if (warp == 0) build_tables(p, tb, lane);
   __syncthreads();
 
