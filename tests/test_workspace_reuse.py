@@ -9,8 +9,8 @@ fault in either; this sequence reuses one workspace across:
 
 - two stream-kernel layers, one with a gated shared expert and one MXFP4;
 - token counts that grow and shrink;
-- a route-only call;
-- a decode-kernel layer in between.
+- route-only calls on both fused kernels;
+- decode-kernel calls in between (a BF16 layer, and N = 12).
 
 Indices must match bit for bit, BF16 outputs within 1e-2*max|ref| + 2^-8.
 """
@@ -32,7 +32,11 @@ LAYERS = {
 SEQUENCE = [("nvfp4", 3, "fwd"), ("nvfp4", 1, "fwd"), ("nvfp4_gated_shared", 5, "fwd"),
             ("mxfp4", 8, "fwd"), ("nvfp4", 3, "route"), ("bf16_decode_path", 2, "fwd"),
             ("nvfp4", 2, "fwd"), ("nvfp4_gated_shared", 1, "fwd"), ("mxfp4", 4, "fwd"),
-            ("nvfp4", 8, "fwd"), ("nvfp4", 8, "fwd")]
+            ("nvfp4", 8, "fwd"), ("nvfp4", 8, "fwd"),
+            # the decode kernel: route-only then forward, and N = 12 FP4 calls
+            ("bf16_decode_path", 3, "route"), ("bf16_decode_path", 2, "fwd"),
+            ("nvfp4", 12, "fwd"), ("nvfp4", 12, "route"), ("nvfp4", 12, "fwd"),
+            ("nvfp4", 4, "fwd")]
 
 
 @pytest.mark.gpu
@@ -50,7 +54,7 @@ def test_one_workspace_through_mixed_calls():
         spec = spec_from("tiny", name=name, **kw)
         hosts[name] = synth.make_layer(spec, seed=9100 + i)
         devs[name] = DeviceLayer.upload(hosts[name])
-    n = max(_lib.moe_workspace_size(d.desc, 8) for d in devs.values())
+    n = max(_lib.moe_workspace_size(d.desc, 16) for d in devs.values())
     ws = torch.empty(n, dtype=torch.uint8, device="cuda")
     _lib.moe_workspace_init(ws)
     paths = set()
