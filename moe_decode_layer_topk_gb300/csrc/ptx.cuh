@@ -97,6 +97,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32
       : "memory");
 }
 
+// Contiguous prefetch into L2 (16-byte aligned address, size a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 2D tiled tensor-map load (box given by the map) into shared memory.
 __device__ __forceinline__ void tma_load_2d(void* dst_smem, const void* tmap, int x, int y,
                                             uint64_t* bar) {

@@ -1461,6 +1461,21 @@ __global__ void __launch_bounds__(kSkThreads, 1) moe_stream_kernel(const __grid_
     if (tid == 0) atomicAdd(&p.ctrl->fin, c == 0 ? 257ull - G : 1ull);
     return;
   }
+  if (p.N == 1 && warp == 1) {
+    // a head start for the weight stream at N = 1: the units are the
+    // token's k selections in order, so this CTA's gate/up tiles (i = c +
+    // G tl, unit i / tpe) are known now; their gate and up rows (16
+    // contiguous rows each) go to L2 while warp 0 builds the tables
+    const int tpe = p.inter >> 4;
+    const uint32_t rb = (uint32_t)(p.H >> 1);
+#pragma unroll 1
+    for (int i = c + G * lane; i < p.k * tpe; i += 32 * G) {
+      const int u = divs(i, tpe), j = i - u * tpe;
+      const size_t row0 = (size_t)tb.sel_e[u] * p.inter + 16 * j;
+      bulk_prefetch_l2(p.gq + row0 * rb, 16u * rb);
+      bulk_prefetch_l2(p.uq + row0 * rb, 16u * rb);
+    }
+  }
   if (warp == 0) build_tables(p, tb, lane);
   __syncthreads();
 
