@@ -1461,17 +1461,20 @@ __global__ void __launch_bounds__(kSkThreads, 1) moe_stream_kernel(const __grid_
     if (tid == 0) atomicAdd(&p.ctrl->fin, c == 0 ? 257ull - G : 1ull);
     return;
   }
-  if (p.N == 1 && warp == 1) {
-    // a head start for the weight stream at N = 1: the units are the
-    // token's k selections in order, so this CTA's gate/up tiles (i = c +
-    // G tl, unit i / tpe) are known now; their gate and up rows (16
-    // contiguous rows each) go to L2 while warp 0 builds the tables
+  if ((p.N == 1 || (p.N <= 3 && (size_t)p.k * p.inter * p.H <= (16u << 20))) && warp == 1) {
+    // a head start for the weight stream: the first k units are token 0's
+    // selections in order, so this CTA's gate/up tiles among them (i = c +
+    // G tl < k tpe, unit i / tpe) are known now; their gate and up rows (16
+    // contiguous rows each) go to L2 while warp 0 builds the tables.  At
+    // N = 1 these are all of the CTA's tiles.  Above that, warps whose first
+    // tiles come later wait behind the burst: measured faster for bursts up
+    // to 16 MB at N <= 3, slower at N = 4 or with larger bursts
     const int tpe = p.inter >> 4;
     const uint32_t rb = (uint32_t)(p.H >> 1);
 #pragma unroll 1
     for (int i = c + G * lane; i < p.k * tpe; i += 32 * G) {
       const int u = divs(i, tpe), j = i - u * tpe;
-      const size_t row0 = (size_t)tb.sel_e[u] * p.inter + 16 * j;
+      const size_t row0 = (size_t)tb.sel_e[u] * p.inter + 16 * j;   // u < k: token 0's
       bulk_prefetch_l2(p.gq + row0 * rb, 16u * rb);
       bulk_prefetch_l2(p.uq + row0 * rb, 16u * rb);
     }
