@@ -181,6 +181,10 @@ FULL = [(name, N) for name in ("tiny", "qwen3_30b_a3b", "mtp_verify", "deepseek_
                                "qwen3_30b_a3b_bf16", "qwen3_30b_a3b_fp8", "qwen3_30b_a3b_nvfp4_router",
                                "qwen3_30b_a3b_zero_experts")
         for N in synth.CONFIGS[name].tokens if N <= 64]
+# single-token calls of the shared-expert layers: at N = 1 the stream kernel
+# prefetches token 0's gate/up tiles into L2 for every layer size (57 KB
+# bursts of 16 rows on the DeepSeek-V3 shape)
+FULL += [("mtp_verify", 1), ("deepseek_v3", 1)]
 
 
 @pytest.mark.gpu
