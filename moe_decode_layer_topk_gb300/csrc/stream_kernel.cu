@@ -765,6 +765,37 @@ __device__ void routing(const StreamParams& p, SkTab& tb, const float* lg, uint2
 // token mask, routing weight and h slot of every (expert, token) pair.
 __device__ void build_tables(const StreamParams& p, SkTab& tb, int lane) {
   const int S = p.N * p.k, k = p.k;
+  if (S <= 32) {
+    // one selection per lane: the lanes that hold the same expert, the lowest
+    // of them (its first selection) stands for the unit, and units are
+    // numbered in first-selection order; no shared-memory atomics
+    const bool v = lane < S;
+    const int e = v ? (int)tb.sel_e[lane] : -1 - lane;   // idle lanes: keys of their own
+    const uint32_t same = __match_any_sync(0xffffffffu, e);
+    const uint32_t below = (1u << lane) - 1u;
+    const bool lead = v && (same & below) == 0u;
+    const uint32_t leads = __ballot_sync(0xffffffffu, lead);
+    const int first = __ffs(same) - 1;
+    const int u = __popc(leads & ((1u << first) - 1u));
+    if (v) {
+      const int n = divs(lane, k);
+      tb.u_w[u][n] = tb.sel_w[lane];
+      tb.u_slot[u][n] = (int16_t)lane;
+      if (lead) {
+        // token n holds this expert if one of its k slots n*k .. n*k+k-1 does
+        // (n*k < 32 for every n < N since N*k <= 32)
+        const uint32_t km = k >= 32 ? 0xFFFFFFFFu : (1u << k) - 1u;
+        uint32_t tm = 0u;
+#pragma unroll 1
+        for (int t = 0; t < p.N; ++t)
+          if ((same >> (t * k)) & km) tm |= 1u << t;
+        tb.u_e[u] = (int16_t)e;
+        tb.u_mask[u] = tm;
+      }
+    }
+    if (lane == 0) tb.U = __popc(leads);
+    return;
+  }
   #pragma unroll 1
   for (int s = lane; s < S; s += 32) atomicMin(&tb.first[tb.sel_e[s]], (uint32_t)s);
   __syncwarp();
