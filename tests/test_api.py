@@ -255,3 +255,23 @@ def test_gpu_wait_timeout_is_reported_not_hung(lib):
     assert _lib.moe_get_error(ws) == _lib.MOE_OK
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16)) or \
         torch.allclose(out.float(), ref.float(), rtol=1e-2, atol=2 ** -8)
+
+
+def test_every_entry_point_fails_loudly_without_the_library(monkeypatch):
+    """No CPU fallback: with libmoe.so absent, each binding raises before it
+    computes anything."""
+    import inspect
+    monkeypatch.setattr(_lib, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libmoe.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    called = 0
+    for name in _lib.EXPORTED:
+        fn = getattr(_lib, name, None)
+        if fn is None:
+            continue
+        sig = inspect.signature(fn)
+        args = [None for p in sig.parameters.values()
+                if p.default is inspect.Parameter.empty and p.kind == p.POSITIONAL_OR_KEYWORD]
+        with pytest.raises(RuntimeError, match="not built"):
+            fn(*args)
+        called += 1
+    assert called >= 8
